@@ -1,0 +1,535 @@
+"""Benchmark of the fused normalisation path on GB300.
+
+One step = one pass of the fused step over one batch: 256 uint8 images of
+224x224x3 (NHWC) -> FP16 NHWC, ImageNet mean/std, per-image flip (p=0.5) and
+RandomErasing (p=0.5, scale [0.02, 0.33], ratio [0.3, 3.3]) records sampled
+on the host from a seed.  Prints ONE JSON line.
+
+  value      images/s of the CUDA kernel with inputs resident in HBM; the
+             timed steps are replays of a CUDA graph of launches that rotate
+             over enough distinct (src, dst, records) sets to exceed L2 four
+             times, so no step reads what the previous one left in L2.
+  roofline   algorithmic bytes per launch (N*H*W*C*(1 + out_bytes) minus the
+             erased source reads) / average launch time, against the measured
+             HBM copy bandwidth (MEASURED_PEAKS.json).
+  e2e        images/s through the transfer station with pinned host buffers:
+             every step copies its uint8 batch and records host->device, runs
+             the kernel and copies the FP16 result device->host.
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload, on
+             the host's cores.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own replica
+of the workload (images are independent; no data-path collective); the
+timing is the max over ranks and value sums the images of all ranks.
+
+--impl reference times the CPU oracle as the reference arm instead.
+"""
+import argparse
+import concurrent.futures as cf
+import ctypes
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "images/sec and achieved HBM GB/s (fraction of peak) at 256×224×224×3"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4])
+    ap.add_argument("--layout", default=None, help="override the config's output layout (nhwc/nchw/nhwc4)")
+    ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ helpers -----
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        import torch
+        if not torch.cuda.is_available():
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return rank, local, world, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "hbm_gbs" in d:
+            return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for fn in ("fused_norm.cu", "internal.h"):
+        with open(os.path.join(ROOT, "image_preprocessing_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, enabled=True):
+        self.index = index
+        self.proc = None
+        self.enabled = enabled
+        self.lines = []
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------- workloads -----
+
+def workload(args):
+    from image_preprocessing_gb300 import synth
+    cfg = dict(synth.CONFIGS[args.config])
+    layout = args.layout or cfg["layouts"][0]
+    cfg["layout"] = layout
+    name = cfg["name"]
+    if args.layout:
+        name += "_" + layout
+    cfg["workload"] = name
+    return cfg
+
+
+def algorithmic_bytes(cfg, recs):
+    """N*H*W*C*(1 + out_bytes) minus the erased source reads (h*w*C per erased
+    image, rectangles clipped to the image)."""
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    ob = 2 if cfg["out_dtype"] == "f16" else 4
+    out_ch = 4 if cfg["layout"] == "nhwc4" else C
+    total = N * H * W * (C + out_ch * ob)
+    if recs is not None:
+        h = np.clip(recs[:, 3], 0, None).astype(np.int64)
+        w = np.clip(recs[:, 4], 0, None).astype(np.int64)
+        total -= int(np.sum(np.where((h > 0) & (w > 0), h * w, 0))) * C
+    return total
+
+
+def host_batch(cfg, seed):
+    from image_preprocessing_gb300 import synth
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    if cfg["pixels"] == "uniform":
+        return synth.pixels_uniform(seed, N, H, W, C)
+    if cfg["pixels"] == "sparse":
+        return synth.pixels_sparse(seed, N, H, W, C)
+    return synth.pixels_gaussian(seed, N, H, W, C)
+
+
+def sample_records(cfg, seed, offset, impl_sampler):
+    if not (cfg["flip"] or cfg["erase"]):
+        return None, offset
+    return impl_sampler(seed, offset, cfg["N"], cfg["H"], cfg["W"], flip=cfg["flip"], erase=cfg["erase"],
+                        erase_p=cfg["erase_p"])
+
+
+# -------------------------------------------------------------- ours ------
+
+def run_ours(args, rank, local, world, pg):
+    import torch
+    import image_preprocessing_gb300 as trfn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = workload(args)
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    dt = trfn.OUT_F16 if cfg["out_dtype"] == "f16" else trfn.OUT_F32
+    layout = {"nhwc": trfn.LAYOUT_NHWC, "nchw": trfn.LAYOUT_NCHW, "nhwc4": trfn.LAYOUT_NHWC4}[cfg["layout"]]
+    tdt = torch.float16 if dt == trfn.OUT_F16 else torch.float32
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    out_shape = trfn.out_shape(N, H, W, C, layout)
+
+    # distinct buffer sets whose total footprint is at least 4x L2
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = N * H * W * C + int(np.prod(out_shape)) * (2 if dt == trfn.OUT_F16 else 4)
+    nsets = max(2, int(np.ceil(4 * l2 / set_bytes)))
+    srcs, dsts, augs, recs_all = [], [], [], []
+    offset = rank * 10 ** 9
+    for j in range(nsets):
+        hb = host_batch(cfg, 1000 + args.config + 100 * j + 7919 * rank)
+        srcs.append(torch.from_numpy(hb).to(dev))
+        dsts.append(torch.empty(out_shape, dtype=tdt, device=dev))
+        recs, offset = sample_records(cfg, 2000 + args.config, offset, trfn.tr_sample_aug_params)
+        recs_all.append(recs)
+        augs.append(torch.from_numpy(recs).to(dev) if recs is not None else None)
+    alg_bytes = [algorithmic_bytes(cfg, r) for r in recs_all]
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def launch(j):
+        trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout, stream=stream,
+                           variant=args.variant)
+
+    # warm the library's per-kernel caches, then capture graphs of launches
+    with torch.cuda.stream(stream):
+        for j in range(nsets):
+            launch(j)
+    torch.cuda.synchronize()
+    G = nsets * max(1, 60 // nsets)
+
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(count):
+                launch(k % nsets)
+        return g
+
+    launches_before = trfn.tr_launch_count()
+    g_full = capture(G)
+    K, Wm = args.steps, args.warmup
+    g_tail = capture(K % G) if K % G else None
+    captured = trfn.tr_launch_count() - launches_before
+
+    def run_steps(steps, exact_tail=None):
+        # full graph replays, then the remainder as one tail graph (timed
+        # region) or as eager launches (warm-up)
+        for _ in range(steps // G):
+            g_full.replay()
+        rem = steps % G
+        if rem and exact_tail is not None:
+            exact_tail.replay()
+        elif rem:
+            with torch.cuda.stream(stream):
+                for k in range(rem):
+                    launch(k % nsets)
+
+    with torch.cuda.stream(stream):
+        run_steps(Wm)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    clocks.start()
+    # keep the GPU busy while the sampler starts
+    with torch.cuda.stream(stream):
+        run_steps(min(Wm, 4 * G) if Wm else 0)
+    time.sleep(0.15)
+    barrier(pg)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    run_steps(K, g_tail)
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier(pg)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(pg, ms, dev)
+    per_launch_s = (ms / 1000.0) / K
+    # average algorithmic bytes per launch over the rotation actually timed
+    seq = [k % nsets for k in range(K)]
+    avg_bytes = float(np.mean([alg_bytes[j] for j in seq]))
+    achieved_gbs = avg_bytes / per_launch_s / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # sampled parity of the last outputs against the oracle (bench's own launch configuration)
+    parity = parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg)
+
+    value = world * N * K / (ms_max / 1000.0)
+    res = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "images/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": ms_max / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": cfg["workload"], "N": N, "H": H, "W": W, "C": C, "in": "u8 NHWC",
+            "out": cfg["out_dtype"] + " " + cfg["layout"].upper(),
+            "flip_p": 0.5 if cfg["flip"] else 0.0, "erase_p": cfg["erase_p"],
+            "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB >= 4x L2 (%.0f MB)" % (
+                nsets, nsets * set_bytes / 1e6, l2 / 1e6),
+            "launch": "CUDA graph of %d launches replayed; variant %d" % (G, args.variant),
+            "parallelism": "replicas" if world > 1 else "single",
+        },
+        "hbm_gbs": achieved_gbs,
+        "roofline": {
+            "bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+            "frac": achieved_gbs / peak, "peak_kind": peak_kind,
+            "frac_of_nominal_8000": achieved_gbs / 8000.0,
+            "algorithmic_bytes_per_launch": avg_bytes,
+            "traffic": profiled_traffic(cfg["workload"]),
+        },
+        "gpu_launches": K,
+        "captured_launches": int(captured),
+        "parity_sample": parity,
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    if e2e is not None:
+        res["e2e"] = e2e
+    return res
+
+
+def parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets):
+    """A few images of the last written buffer set against the oracle."""
+    import oracle
+    import torch
+    j = (nsets - 1)
+    idx = [0, cfg["N"] // 2, cfg["N"] - 1]
+    src = srcs[j][idx].cpu().numpy()
+    recs = recs_all[j][idx] if recs_all[j] is not None else None
+    got = dsts[j][idx].cpu()
+    got = got.view(torch.int16).numpy().view(np.uint16) if dt == 1 else got.numpy()
+    ref = oracle.fused_norm(src, mean, std, recs, out_dtype=dt, layout=layout)
+    if dt == 1:
+        def ordered(b):
+            b = b.astype(np.int32)
+            return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+        err = int(np.max(np.abs(ordered(got) - ordered(ref))))
+        ok = err <= 1 and bool(np.all(got[ref == 0] == 0))
+        return {"images": len(idx), "max_f16_ulp": err, "ok": ok}
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    ok = err <= 2e-6 and bool(np.all(got.view(np.uint32)[ref.view(np.uint32) == 0] == 0))
+    return {"images": len(idx), "max_abs": err, "ok": ok}
+
+
+def run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg):
+    """Through the public API with pinned host buffers: each step copies its
+    uint8 batch and its records host->device, runs the kernel, and copies the
+    result device->host (tr_ts_submit)."""
+    import torch
+    import image_preprocessing_gb300 as trfn
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    nh = 4
+    h_src = [torch.from_numpy(host_batch(cfg, 5000 + b + 7919 * rank)).pin_memory() for b in range(nh)]
+    offset = 0
+    h_par = []
+    for b in range(nh):
+        recs, offset = sample_records(cfg, 2005, offset, trfn.tr_sample_aug_params)
+        h_par.append(torch.from_numpy(recs).pin_memory() if recs is not None else None)
+    slot_bytes = trfn.tr_ts_slot_bytes(N, H, W, C)
+    slots = [torch.empty(slot_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_out = [torch.empty(out_shape, dtype=tdt, device=dev) for _ in range(2)]
+    h_out = [torch.empty(out_shape, dtype=tdt).pin_memory() for _ in range(2)]
+    s_copy, s_comp, s_d2h = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ts = trfn.TransferStation(dev.index, slots, s_copy, s_comp, s_d2h)
+
+    def steps(k0, count):
+        for k in range(k0, k0 + count):
+            ts.submit(h_src[k % nh], d_out[k % 2], mean, std, h_params=h_par[k % nh], h_dst=h_out[k % 2],
+                      out_dtype=dt, layout=layout)
+
+    steps(0, 4)
+    assert ts.sync(60000)
+    K = args.e2e_steps
+    barrier(pg)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    steps(4, K)
+    ok = ts.sync(120000)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    ts.close()
+    assert ok, "transfer station did not finish"
+    sec = max_over_ranks(pg, t1 - t0, dev)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    ob = 2 if dt == 1 else 4
+    h2d = N * H * W * C + (N * 20 if h_par[0] is not None else 0)
+    d2h = int(np.prod(out_shape)) * ob
+    return {"value": world * N * K / sec, "unit": "images/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "path": "tr_ts_submit: pinned host u8 + records -> device slot A/B (copy stream) -> kernel "
+                    "(compute stream) -> pinned host output (d2h stream)",
+            "link_gbs": (h2d + d2h) * K / sec / 1e9}
+
+
+# ------------------------------------------------------------- oracle -----
+
+def oracle_images_per_s(cfg, seconds, threads=None):
+    """The oracle as it stands on a bounded sample of the workload, split by
+    image over host threads (ctypes releases the GIL).  Returns
+    (images/s, threads, sample text)."""
+    import oracle
+    import image_preprocessing_gb300 as trfn
+    threads = threads or os.cpu_count() or 1
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    m = min(N, max(threads, 8))
+    src = host_batch(dict(cfg, N=N), 1000 + 3)[:m].copy()
+    recs = None
+    if cfg["flip"] or cfg["erase"]:
+        recs, _ = oracle.sample_aug_params(2003, 0, m, H, W, flip=cfg["flip"], erase=cfg["erase"],
+                                           erase_p=cfg["erase_p"])
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    dt = oracle.OUT_F16 if cfg["out_dtype"] == "f16" else oracle.OUT_F32
+    layout = {"nhwc": 0, "nchw": 1, "nhwc4": 2}[cfg["layout"]]
+    done = 0
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        while time.perf_counter() - t0 < seconds:
+            futs = [ex.submit(oracle.fused_norm, src[i:i + 1], mean, std,
+                              None if recs is None else recs[i:i + 1], dt, layout) for i in range(m)]
+            for f in futs:
+                f.result()
+            done += m
+    el = time.perf_counter() - t0
+    sample = "%d passes over %d of the %d images (%dx%dx%d), %.1f s on %d threads" % (
+        done // m, m, N, H, W, C, el, threads)
+    return done / el, threads, sample
+
+
+def run_reference(args, rank, world, pg):
+    cfg = workload(args)
+    if rank != 0:
+        return None
+    K, Wm = args.steps, args.warmup
+    # each step: the oracle over a bounded sample of the batch on all host cores
+    per_step = max(0.05, min(2.0, 120.0 / max(1, K + Wm)))
+    for _ in range(min(Wm, 3)):
+        oracle_images_per_s(cfg, 0.01)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(min(K, 200)):
+        v, threads, sample = oracle_images_per_s(cfg, per_step)
+        vals.append(v)
+    el = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    return {"metric": METRIC, "value": value, "unit": "images/s", "n_gpus": world, "steps": len(vals),
+            "warmup": Wm, "ms_per_step": el * 1000 / max(1, len(vals)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg["workload"], "N": cfg["N"], "H": cfg["H"], "W": cfg["W"], "C": cfg["C"]},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "images/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, local, world, pg = dist_setup(args)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world, pg)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    res = run_ours(args, rank, local, world, pg)
+    if rank == 0:
+        if not args.no_cpu:
+            cfg = workload(args)
+            v, threads, sample = oracle_images_per_s(cfg, args.cpu_seconds)
+            res["cpu_baseline"] = {"value": v, "unit": "images/s", "cores": threads, "kind": "oracle",
+                                   "sample": sample}
+        print(json.dumps(res), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,95 @@
+"""ctypes binding to libtrfn.so: argument marshalling only.
+
+Every step of the fused path runs in the library's CUDA kernels; this module
+only turns tensors into pointers and sizes and status codes into exceptions.
+It never falls back to another implementation: if the library is missing the
+import of any entry point raises.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtrfn.so")
+
+TR_OK = 0
+STATUS_NAMES = {0: "TR_OK", 1: "TR_ERR_INVALID_ARGUMENT", 2: "TR_ERR_NOT_SUPPORTED", 3: "TR_ERR_CUDA",
+                4: "TR_ERR_TIMEOUT", 5: "TR_ERR_DEVICE"}
+
+
+class TrError(RuntimeError):
+    """A non-zero tr_status from the library."""
+
+    def __init__(self, status, where, detail=""):
+        self.status = status
+        name = STATUS_NAMES.get(status, str(status))
+        msg = "%s returned %s" % (where, name)
+        if detail:
+            msg += ": " + detail
+        super().__init__(msg)
+
+
+class AugParam(ctypes.Structure):
+    _fields_ = [("flip", ctypes.c_int32), ("y0", ctypes.c_int32), ("x0", ctypes.c_int32),
+                ("h", ctypes.c_int32), ("w", ctypes.c_int32)]
+
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_fp = ctypes.POINTER(ctypes.c_float)
+_u64 = ctypes.c_uint64
+
+_SIGNATURES = {
+    "tr_fused_norm": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp]),
+    "tr_fused_norm_variant": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i]),
+    "tr_fused_norm_plan": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]),
+    "tr_norm_preset": (_i, [_i, _fp, _fp, ctypes.POINTER(_i)]),
+    "tr_sample_aug_params": (_i, [_u64, _u64, _i, _i, _i, _i, _f, _i, _f, _f, _f, _f, _f, _vp,
+                                  ctypes.POINTER(_u64)]),
+    "tr_validate_aug_params": (_i, [_vp, _i, _i, _i, ctypes.POINTER(_i)]),
+    "tr_ts_slot_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
+    "tr_ts_create": (_i, [_i, ctypes.POINTER(_vp), ctypes.c_size_t, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
+    "tr_ts_submit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _fp, _fp, _i, _i,
+                          ctypes.POINTER(ctypes.c_longlong)]),
+    "tr_ts_sync": (_i, [_vp, _i]),
+    "tr_ts_destroy": (_i, [_vp]),
+    "tr_device_status": (_i, [ctypes.POINTER(_i), _i]),
+    "tr_launch_count": (_u64, []),
+    "tr_status_string": (ctypes.c_char_p, [_i]),
+    "tr_last_error_message": (ctypes.c_char_p, []),
+    "tr_version": (_i, []),
+}
+
+
+def lib():
+    """The loaded libtrfn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                "libtrfn.so is not built (%s); build it with `python -m image_preprocessing_gb300.build` "
+                "or __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def check(status, where):
+    if status != TR_OK:
+        detail = ""
+        if status == 3:
+            detail = lib().tr_last_error_message().decode(errors="replace")
+        raise TrError(status, where, detail)
+
+
+def float_array(values):
+    arr = (ctypes.c_float * 4)()
+    for i, v in enumerate(values):
+        arr[i] = float(v)
+    return arr

@@ -1,0 +1,187 @@
+"""Python face of libtrfn.so (the functions carry the C entry points' names).
+
+PyTorch supplies device memory and streams only; each call below marshals
+pointers, sizes and the stream handle into the C ABI declared in
+include/tr_fused_norm.h and raises TrError on a non-zero status.
+"""
+import ctypes
+
+import numpy as np
+
+from . import _native
+from ._native import AugParam, TrError, check, float_array, lib
+
+OUT_F32, OUT_F16 = 0, 1
+LAYOUT_NHWC, LAYOUT_NCHW, LAYOUT_NHWC4 = 0, 1, 2
+VARIANT_AUTO, VARIANT_TILED, VARIANT_GENERIC = 0, 1, 2
+PRESETS = {"NO_NORM": 0, "MNIST": 1, "CIFAR": 2, "IMAGENET": 3, "MLPERF": 4}
+
+_DTYPES = {"f32": OUT_F32, "float32": OUT_F32, "f16": OUT_F16, "float16": OUT_F16}
+_LAYOUTS = {"nhwc": LAYOUT_NHWC, "nchw": LAYOUT_NCHW, "nhwc4": LAYOUT_NHWC4}
+
+
+def _code(v, table):
+    return table[v.lower()] if isinstance(v, str) else int(v)
+
+
+def out_shape(N, H, W, C, layout):
+    layout = _code(layout, _LAYOUTS)
+    if layout == LAYOUT_NCHW:
+        return (N, C, H, W)
+    if layout == LAYOUT_NHWC4:
+        return (N, H, W, 4)
+    return (N, H, W, C)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev_ptr(t, what):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise TrError(1, what, "expects a CUDA tensor")
+    if not t.is_contiguous():
+        raise TrError(1, what, "expects a contiguous tensor")
+    return t.data_ptr()
+
+
+def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOUT_NHWC, stream=None,
+                  variant=VARIANT_AUTO, shape=None):
+    """Enqueue the fused step: src uint8 (N,H,W,C) CUDA tensor -> dst.
+
+    dst: CUDA tensor of float32/float16 with out_shape(N,H,W,C,layout)
+    elements; aug: CUDA int32 tensor (N,5) of {flip,y0,x0,h,w} or None;
+    raw device addresses (ints) are accepted with shape=(N,H,W,C)."""
+    dt = _code(out_dtype, _DTYPES)
+    lay = _code(layout, _LAYOUTS)
+    if shape is not None:
+        N, H, W, C = shape
+    else:
+        import torch
+        if src.dtype != torch.uint8 or src.dim() != 4:
+            raise TrError(1, "tr_fused_norm", "src must be a uint8 (N,H,W,C) tensor")
+        N, H, W, C = src.shape
+        want = torch.float16 if dt == OUT_F16 else torch.float32
+        if dst.dtype != want or dst.numel() != int(np.prod(out_shape(N, H, W, C, lay))):
+            raise TrError(1, "tr_fused_norm", "dst must be %s with %d elements" % (want, np.prod(out_shape(N, H, W, C, lay))))
+        if aug is not None and (aug.dtype != torch.int32 or aug.numel() != 5 * N):
+            raise TrError(1, "tr_fused_norm", "aug must be int32 with N*5 elements")
+    m, s = float_array(mean), float_array(std)
+    rc = lib().tr_fused_norm_variant(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
+                                     _dev_ptr(aug, "aug"), dt, lay, _stream_handle(stream), int(variant))
+    check(rc, "tr_fused_norm")
+
+
+def tr_fused_norm_plan(src, dst, N, H, W, C, out_dtype, layout):
+    v = ctypes.c_int(0)
+    check(lib().tr_fused_norm_plan(src, dst, N, H, W, C, _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS),
+                                   ctypes.byref(v)), "tr_fused_norm_plan")
+    return v.value
+
+
+def tr_norm_preset(preset):
+    pid = PRESETS[preset] if isinstance(preset, str) else int(preset)
+    m = (ctypes.c_float * 3)()
+    s = (ctypes.c_float * 3)()
+    ch = ctypes.c_int(0)
+    check(lib().tr_norm_preset(pid, m, s, ctypes.byref(ch)), "tr_norm_preset")
+    return (np.array(m[: ch.value], np.float32), np.array(s[: ch.value], np.float32), ch.value)
+
+
+def tr_sample_aug_params(seed, offset, N, H, W, flip=True, flip_p=0.5, erase=True, erase_p=0.5,
+                         scale=(0.02, 0.33), ratio=(0.3, 3.3)):
+    """Host sampling of N records; returns (int32 array (N,5), next_offset)."""
+    out = np.zeros((N, 5), np.int32)
+    nxt = ctypes.c_uint64(0)
+    check(lib().tr_sample_aug_params(seed, offset, N, H, W, int(bool(flip)), flip_p, int(bool(erase)), erase_p,
+                                     scale[0], scale[1], ratio[0], ratio[1],
+                                     out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(nxt)),
+          "tr_sample_aug_params")
+    return out, nxt.value
+
+
+def tr_validate_aug_params(records, H, W):
+    """Returns -1 when every record is valid, else the first bad index."""
+    rec = np.ascontiguousarray(records, dtype=np.int32).reshape(-1, 5)
+    bad = ctypes.c_int(-1)
+    rc = lib().tr_validate_aug_params(rec.ctypes.data_as(ctypes.c_void_p), rec.shape[0], H, W, ctypes.byref(bad))
+    if rc not in (0, 1):
+        check(rc, "tr_validate_aug_params")
+    return bad.value
+
+
+def tr_device_status(clear=False):
+    v = ctypes.c_int(0)
+    check(lib().tr_device_status(ctypes.byref(v), int(bool(clear))), "tr_device_status")
+    return v.value
+
+
+def tr_launch_count():
+    return int(lib().tr_launch_count())
+
+
+def tr_ts_slot_bytes(N, H, W, C):
+    return int(lib().tr_ts_slot_bytes(N, H, W, C))
+
+
+class TransferStation:
+    """tr_ts_* wrapper: two caller-owned device input slots and three streams.
+
+    The slots are CUDA uint8 tensors of tr_ts_slot_bytes(N,H,W,C) bytes each;
+    the streams are torch.cuda.Stream objects (d2h may be None)."""
+
+    def __init__(self, device, slots, copy_stream, compute_stream, d2h_stream=None):
+        self._slots = slots  # keep the memory alive
+        ptrs = (ctypes.c_void_p * 2)(slots[0].data_ptr(), slots[1].data_ptr())
+        nbytes = min(slots[0].numel(), slots[1].numel())
+        handle = ctypes.c_void_p(0)
+        self.streams = (copy_stream, compute_stream, d2h_stream)
+        check(lib().tr_ts_create(int(device), ptrs, nbytes, copy_stream.cuda_stream, compute_stream.cuda_stream,
+                                 d2h_stream.cuda_stream if d2h_stream is not None else None,
+                                 ctypes.byref(handle)), "tr_ts_create")
+        self._h = handle
+
+    def submit(self, h_src, d_dst, mean, std, h_params=None, h_dst=None, out_dtype=OUT_F16, layout=LAYOUT_NHWC):
+        """h_src: pinned uint8 CPU tensor (N,H,W,C); d_dst: CUDA output tensor;
+        h_params: pinned int32 CPU tensor (N,5) or None; h_dst: pinned CPU tensor or None."""
+        N, H, W, C = h_src.shape
+        k = ctypes.c_longlong(-1)
+        check(lib().tr_ts_submit(self._h, h_src.data_ptr(), None if h_params is None else h_params.data_ptr(),
+                                 d_dst.data_ptr(), None if h_dst is None else h_dst.data_ptr(), N, H, W, C,
+                                 float_array(mean), float_array(std), _code(out_dtype, _DTYPES),
+                                 _code(layout, _LAYOUTS), ctypes.byref(k)), "tr_ts_submit")
+        return k.value
+
+    def sync(self, timeout_ms=-1):
+        """True when all submitted work has finished; False on timeout."""
+        rc = lib().tr_ts_sync(self._h, int(timeout_ms))
+        if rc == 4:
+            return False
+        check(rc, "tr_ts_sync")
+        return True
+
+    def close(self):
+        if self._h:
+            h, self._h = self._h, None
+            check(lib().tr_ts_destroy(h), "tr_ts_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,183 @@
+// C ABI entry points of libtrfn.so: argument checks, folding of mean/std into
+// scale/bias, kernel choice, presets and diagnostics.  Every check here runs
+// on the host before anything touches the GPU.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+namespace trfn {
+
+namespace {
+thread_local char t_last_error[256] = "";
+}
+
+void set_last_error(const char* what, int cuda_error) {
+    std::snprintf(t_last_error, sizeof t_last_error, "%s: %s (%d)", what,
+                  cudaGetErrorString(static_cast<cudaError_t>(cuda_error)), cuda_error);
+}
+
+const char* last_error() { return t_last_error; }
+
+namespace {
+
+constexpr long long kMaxElements = 1LL << 40;
+
+// Shape/type checks shared by the launch and plan entry points.
+int check_shape(int N, int H, int W, int C, int out_dtype, int out_layout) {
+    if (N < 0 || H < 1 || W < 1 || C < 1) return TR_ERR_INVALID_ARGUMENT;
+    if (C > 4) return TR_ERR_NOT_SUPPORTED;
+    if (out_dtype != TR_OUT_F32 && out_dtype != TR_OUT_F16) return TR_ERR_INVALID_ARGUMENT;
+    if (out_layout != TR_LAYOUT_NHWC && out_layout != TR_LAYOUT_NCHW && out_layout != TR_LAYOUT_NHWC4)
+        return TR_ERR_INVALID_ARGUMENT;
+    const long long per_image = (long long)H * W;
+    if (per_image > kMaxElements) return TR_ERR_INVALID_ARGUMENT;
+    if (per_image * 4 * N > kMaxElements) return TR_ERR_INVALID_ARGUMENT;
+    return TR_OK;
+}
+
+int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,
+                    const float* stdv, const tr_aug_param* aug, int out_dtype, int out_layout,
+                    void* stream, int variant) {
+    int rc = check_shape(N, H, W, C, out_dtype, out_layout);
+    if (rc != TR_OK) return rc;
+    if (variant != TR_VARIANT_AUTO && variant != TR_VARIANT_TILED && variant != TR_VARIANT_GENERIC)
+        return TR_ERR_INVALID_ARGUMENT;
+    if (mean == nullptr || stdv == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    LaunchArgs a;
+    for (int c = 0; c < 4; ++c) { a.scale[c] = 0.0f; a.bias[c] = 0.0f; }
+    for (int c = 0; c < C; ++c) {
+        const double m = mean[c], s = stdv[c];
+        if (!std::isfinite(m) || !std::isfinite(s) || s == 0.0) return TR_ERR_INVALID_ARGUMENT;
+        // (x/255 - m)/s == x * (1/(255 s)) + (-m/s): both constants formed in
+        // binary64 and rounded once to binary32
+        a.scale[c] = (float)(1.0 / (255.0 * s));
+        a.bias[c] = (float)(-m / s);
+        if (!std::isfinite(a.scale[c]) || !std::isfinite(a.bias[c])) return TR_ERR_INVALID_ARGUMENT;
+    }
+    if (N == 0) return TR_OK;
+    if (src == nullptr || dst == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    const int ob = (out_dtype == TR_OUT_F16) ? 2 : 4;
+    const int out_ch = (out_layout == TR_LAYOUT_NHWC4) ? 4 : C;
+    const unsigned long long in_bytes = (unsigned long long)N * H * W * C;
+    const unsigned long long out_bytes = (unsigned long long)N * H * W * out_ch * ob;
+    const uintptr_t s0 = (uintptr_t)src, d0 = (uintptr_t)dst;
+    if (s0 < d0 + out_bytes && d0 < s0 + in_bytes) return TR_ERR_INVALID_ARGUMENT;   // overlap
+
+    const bool tiled_ok = tiled_supported(src, dst, N, H, W, C, out_dtype, out_layout);
+    const bool forced = (variant != TR_VARIANT_AUTO);
+    if (variant == TR_VARIANT_TILED && !tiled_ok) return TR_ERR_NOT_SUPPORTED;
+    if (variant == TR_VARIANT_AUTO) variant = tiled_ok ? TR_VARIANT_TILED : TR_VARIANT_GENERIC;
+
+    a.src = src;
+    a.dst = dst;
+    a.N = N; a.H = H; a.W = W; a.C = C;
+    a.aug = aug;
+    a.out_dtype = out_dtype;
+    a.out_layout = out_layout;
+    a.stream = stream;
+    rc = launch(a, variant);
+    if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {
+        // the tiled geometry does not fit this device's shared memory (rows
+        // of hundreds of kilobytes): the generic kernel handles any shape
+        rc = launch(a, TR_VARIANT_GENERIC);
+    }
+    return rc;
+}
+
+}  // namespace
+}  // namespace trfn
+
+using namespace trfn;
+
+extern "C" {
+
+int tr_fused_norm(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,
+                  const float* std, const tr_aug_param* aug_params, int out_dtype, int out_layout,
+                  void* stream) {
+    const int rc = fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype,
+                                   out_layout, stream, TR_VARIANT_AUTO);
+    return rc;
+}
+
+int tr_fused_norm_variant(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                          const float* mean, const float* std, const tr_aug_param* aug_params,
+                          int out_dtype, int out_layout, void* stream, int variant) {
+    return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
+                           stream, variant);
+}
+
+int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,
+                       int out_dtype, int out_layout, int* variant) {
+    const int rc = check_shape(N, H, W, C, out_dtype, out_layout);
+    if (rc != TR_OK) return rc;
+    if (variant == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    *variant = tiled_supported(src_u8, dst, N, H, W, C, out_dtype, out_layout) ? TR_VARIANT_TILED
+                                                                               : TR_VARIANT_GENERIC;
+    return TR_OK;
+}
+
+int tr_norm_preset(int preset, float mean[3], float std[3], int* channels) {
+    if (mean == nullptr || std == nullptr || channels == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    // values of the preset table in the FusedNormalization article, §九
+    static const struct { float m[3]; float s[3]; int ch; } table[5] = {
+        {{0.0f, 0.0f, 0.0f}, {1.0f, 1.0f, 1.0f}, 3},                                  // NO_NORM
+        {{0.1307f, 0.0f, 0.0f}, {0.3081f, 1.0f, 1.0f}, 1},                            // MNIST
+        {{0.4914f, 0.4822f, 0.4465f}, {0.2470f, 0.2435f, 0.2616f}, 3},                // CIFAR
+        {{0.485f, 0.456f, 0.406f}, {0.229f, 0.224f, 0.225f}, 3},                      // IMAGENET
+        {{123.68f / 255.0f, 116.78f / 255.0f, 103.94f / 255.0f},
+         {1.0f / 255.0f, 1.0f / 255.0f, 1.0f / 255.0f}, 3},                           // MLPERF
+    };
+    if (preset < 0 || preset > 4) return TR_ERR_INVALID_ARGUMENT;
+    for (int c = 0; c < 3; ++c) {
+        mean[c] = table[preset].m[c];
+        std[c] = table[preset].s[c];
+    }
+    *channels = table[preset].ch;
+    return TR_OK;
+}
+
+int tr_validate_aug_params(const tr_aug_param* p, int N, int H, int W, int* bad_index) {
+    if (bad_index) *bad_index = -1;
+    if (N < 0 || H < 1 || W < 1) return TR_ERR_INVALID_ARGUMENT;
+    if (N > 0 && p == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    for (int n = 0; n < N; ++n) {
+        const tr_aug_param& a = p[n];
+        if (a.h <= 0 || a.w <= 0) continue;
+        const long long y1 = (long long)a.y0 + a.h, x1 = (long long)a.x0 + a.w;
+        if (a.y0 < 0 || a.x0 < 0 || y1 > H || x1 > W) {
+            if (bad_index) *bad_index = n;
+            return TR_ERR_INVALID_ARGUMENT;
+        }
+    }
+    return TR_OK;
+}
+
+int tr_device_status(int* flags, int clear) {
+    if (flags == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    return read_device_status(flags, clear != 0);
+}
+
+uint64_t tr_launch_count(void) { return launch_count(); }
+
+const char* tr_status_string(int status) {
+    switch (status) {
+    case TR_OK: return "ok";
+    case TR_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case TR_ERR_NOT_SUPPORTED: return "not supported";
+    case TR_ERR_CUDA: return "CUDA error";
+    case TR_ERR_TIMEOUT: return "timed out";
+    case TR_ERR_DEVICE: return "device reported an error";
+    default: return "unknown status";
+    }
+}
+
+const char* tr_last_error_message(void) { return last_error(); }
+
+int tr_version(void) { return 100; }
+
+}  // extern "C"

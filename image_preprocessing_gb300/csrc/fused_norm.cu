@@ -1,0 +1,769 @@
+// Fused normalisation kernels for sm_103a (GB300).
+//
+// The operation is the one described in the Tech-Renaissance article
+// "(11) FusedNormalization: fuse the last step of data augmentation into one
+// memory traversal" (tech-renaissance.cn/blog/?p=487): ToTensor (x/255) and
+// Normalize ((x - mean)/std) in one pass (§五), read from the mirrored or the
+// original position when flipping (§五, §七), erased output set to +0 (§十二),
+// binary32 or binary16 output (§六), with the 4-channel padded layout (§八).
+// The article's implementation is x86 SIMD on the CPU; nothing of it carries
+// over.  This file is a GPU design:
+//
+//  * TILED: a persistent kernel.  The batch is cut into units of R rows of one
+//    image ("row bands").  One thread per CTA streams the source bytes of the
+//    next bands into a ring of shared-memory stages with TMA bulk copies
+//    (cp.async.bulk + mbarrier transaction counts), skipping 16-byte chunks
+//    that lie wholly inside an erased span.  All threads convert groups of 8
+//    (C=3), 16 (C=1), 8 (C=2) or 4 (C=4) pixels: the mirrored gather is done
+//    by choosing source byte lanes with PRMT, the byte becomes 2^23 + x by the
+//    same PRMT, one exact FADD removes 2^23, one FFMA applies scale and bias.
+//    Results go to a double-buffered shared-memory output tile that one TMA
+//    bulk store per band (per plane for NCHW) writes to global memory.
+//  * GENERIC: one thread per output element, any shape and alignment.
+//
+// Both kernels compute each value as fma(float(x), scale_c, bias_c) with the
+// same binary32 operands, so they agree bit for bit.
+//
+// Every wait in device code is bounded: a TMA stage that does not complete
+// within about a second sets bit 0 of the device status word, the CTA drains
+// what it has in flight (again bounded) and returns.
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace trfn {
+
+__device__ unsigned int g_device_status;   // bit 0: a pipeline wait timed out
+
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kHeaderBytes = 384;          // mbarriers + per-stage unit records
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+constexpr uint32_t kStatusTimeout = 1u;
+
+// ------------------------------------------------------------------ PTX ---
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false after ~1 s.
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+
+// TMA bulk copy global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// TMA bulk copy shared -> global in the current bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------ arithmetic --
+
+// Byte `sel` (0..3) of `word` as a binary32 value: PRMT builds the pattern
+// 0x4B0000xx = 2^23 + x, the subtraction of 2^23 is exact.
+__device__ __forceinline__ float byte_to_float(uint32_t word, uint32_t sel) {
+    const uint32_t bits = __byte_perm(word, 0x00004B00u, 0x5440u | sel);
+    return __fsub_rn(__uint_as_float(bits), 8388608.0f);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);   // round to nearest even
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Pixels per group: the smallest pixel count whose bytes fill 16 (C=1,2,4)
+// or 24 (C=3) bytes, so that a group's source is one or three aligned words.
+template <int C>
+struct Group {
+    static constexpr int P = (C == 3) ? 8 : 16 / C;
+    static constexpr int kBytes = P * C;   // 16 or 24
+    static constexpr int kWords = kBytes / 4;
+};
+
+// Converts one group.  Output element k is pixel k/C, channel k%C; with FLIP
+// its source is pixel P-1-k/C of the mirrored group (same channel).
+template <int C, bool FLIP>
+__device__ __forceinline__ void convert_group(const uint32_t (&w)[Group<C>::kWords],
+                                              const float* scale, const float* bias,
+                                              float (&v)[Group<C>::kBytes]) {
+    constexpr int P = Group<C>::P;
+#pragma unroll
+    for (int k = 0; k < P * C; ++k) {
+        const int i = k / C;
+        const int c = k % C;
+        const int sb = FLIP ? ((P - 1 - i) * C + c) : k;
+        v[k] = __fmaf_rn(byte_to_float(w[sb >> 2], sb & 3), scale[c], bias[c]);
+    }
+}
+
+// ---------------------------------------------------------------- tiled ---
+
+struct TiledParams {
+    const uint8_t* src;
+    uint8_t* dst;
+    const tr_aug_param* aug;
+    int N, H, W;
+    int R;                 // rows per band
+    int bands;             // bands per image
+    int num_units;         // N * bands
+    int gpr;               // groups per row, W / P
+    uint64_t gpr_inv;      // ceil(2^32 / gpr): g / gpr == (g * gpr_inv) >> 32 for g, gpr < 2^16
+    uint32_t in_stage;     // bytes per input stage (R*W*C, multiple of 16)
+    uint32_t out_stage;    // bytes per output stage
+    uint32_t plane_bytes;  // NCHW: bytes per plane of one band in the output stage (R*W*ob)
+    int stages;
+    float scale[4];
+    float bias[4];
+};
+
+// Per-stage record of the unit held in that stage.
+struct UnitRec {
+    int n, y_begin, rows, flip;
+    int erow_lo, erow_hi;  // erased output rows [lo, hi), clipped to the image
+    int ecol_lo, ecol_hi;  // erased output columns [lo, hi), clipped
+};
+static_assert(sizeof(UnitRec) == 32, "UnitRec layout");
+static_assert(64 + kMaxStages * sizeof(UnitRec) <= kHeaderBytes, "header holds barriers and records");
+
+template <int C>
+__device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem) {
+    const int n = u / p.bands;
+    const int b = u - n * p.bands;
+    const int y_begin = b * p.R;
+    const int rows = min(p.R, p.H - y_begin);
+
+    int flip = 0, erow_lo = 0, erow_hi = 0, ecol_lo = 0, ecol_hi = 0;
+    if (p.aug != nullptr) {
+        const tr_aug_param a = p.aug[n];
+        flip = (a.flip != 0);
+        if (a.h > 0 && a.w > 0) {
+            const long long y0 = a.y0, x0 = a.x0;
+            const long long ylo = max(y0, 0ll), yhi = min(y0 + a.h, (long long)p.H);
+            const long long xlo = max(x0, 0ll), xhi = min(x0 + a.w, (long long)p.W);
+            if (ylo < yhi && xlo < xhi) {
+                erow_lo = (int)ylo; erow_hi = (int)yhi;
+                ecol_lo = (int)xlo; ecol_hi = (int)xhi;
+            }
+        }
+    }
+    UnitRec* rec = reinterpret_cast<UnitRec*>(smem + 64) + s;
+    rec->n = n; rec->y_begin = y_begin; rec->rows = rows; rec->flip = flip;
+    rec->erow_lo = erow_lo; rec->erow_hi = erow_hi; rec->ecol_lo = ecol_lo; rec->ecol_hi = ecol_hi;
+
+    const uint32_t L = (uint32_t)p.W * C;
+    const uint8_t* g = p.src + ((size_t)n * p.H + y_begin) * L;
+    const uint32_t sdst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
+    const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
+    const uint32_t total = (uint32_t)rows * L;
+
+    // Rows of this band inside the erase rectangle, and the 16-byte aligned
+    // part of their erased source span (rows start 16-byte aligned).
+    const int r_lo = max(erow_lo - y_begin, 0);
+    const int r_hi = min(erow_hi - y_begin, rows);
+    const int xs_lo = flip ? p.W - ecol_hi : ecol_lo;
+    const int xs_hi = flip ? p.W - ecol_lo : ecol_hi;
+    const uint32_t a_lo = ((uint32_t)xs_lo * C + 15u) & ~15u;
+    const uint32_t a_hi = ((uint32_t)xs_hi * C) & ~15u;
+    if (r_lo >= r_hi || a_hi <= a_lo) {
+        mbar_arrive_expect_tx(bar, total);
+        bulk_g2s(sdst, g, total, bar);
+        return;
+    }
+    const uint32_t skipped = (uint32_t)(r_hi - r_lo) * (a_hi - a_lo);
+    mbar_arrive_expect_tx(bar, total - skipped);
+    uint32_t pos = 0;
+    for (int r = r_lo; r < r_hi; ++r) {
+        const uint32_t seg_end = (uint32_t)r * L + a_lo;
+        if (seg_end > pos) bulk_g2s(sdst + pos, g + pos, seg_end - pos, bar);
+        pos = (uint32_t)r * L + a_hi;
+    }
+    if (total > pos) bulk_g2s(sdst + pos, g + pos, total - pos, bar);
+}
+
+template <int C, int OUT_F16, int LAYOUT>
+__device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout, int r, int gx,
+                                            const float (&v)[Group<C>::kBytes]) {
+    constexpr int P = Group<C>::P;
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    if (LAYOUT == TR_LAYOUT_NHWC) {
+        uint8_t* o = sout + ((size_t)r * p.W + (size_t)gx * P) * C * OB;
+        if (OUT_F16) {
+#pragma unroll
+            for (int q = 0; q < P * C / 8; ++q) {
+                uint4 t;
+                t.x = pack_half2(v[8 * q + 0], v[8 * q + 1]);
+                t.y = pack_half2(v[8 * q + 2], v[8 * q + 3]);
+                t.z = pack_half2(v[8 * q + 4], v[8 * q + 5]);
+                t.w = pack_half2(v[8 * q + 6], v[8 * q + 7]);
+                reinterpret_cast<uint4*>(o)[q] = t;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < P * C / 4; ++q) {
+                reinterpret_cast<float4*>(o)[q] =
+                    make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+    } else if (LAYOUT == TR_LAYOUT_NHWC4) {
+        // four channels per pixel, channels C..3 are +0
+        uint8_t* o = sout + ((size_t)r * p.W + (size_t)gx * P) * 4 * OB;
+        if (OUT_F16) {
+#pragma unroll
+            for (int i = 0; i < P; i += 2) {
+                uint4 t;
+                t.x = pack_half2(v[i * C], C > 1 ? v[i * C + 1] : 0.0f);
+                t.y = pack_half2(C > 2 ? v[i * C + 2] : 0.0f, C > 3 ? v[i * C + 3] : 0.0f);
+                t.z = pack_half2(v[(i + 1) * C], C > 1 ? v[(i + 1) * C + 1] : 0.0f);
+                t.w = pack_half2(C > 2 ? v[(i + 1) * C + 2] : 0.0f, C > 3 ? v[(i + 1) * C + 3] : 0.0f);
+                reinterpret_cast<uint4*>(o)[i / 2] = t;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < P; ++i)
+                reinterpret_cast<float4*>(o)[i] =
+                    make_float4(v[i * C], C > 1 ? v[i * C + 1] : 0.0f, C > 2 ? v[i * C + 2] : 0.0f,
+                                C > 3 ? v[i * C + 3] : 0.0f);
+        }
+    } else {  // NCHW: channel c of the group goes to plane c
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            uint8_t* o = sout + (size_t)c * p.plane_bytes + ((size_t)r * p.W + (size_t)gx * P) * OB;
+            if (OUT_F16) {
+                if (P % 8 == 0) {
+#pragma unroll
+                    for (int q = 0; q < P / 8; ++q) {
+                        uint4 t;
+                        t.x = pack_half2(v[(8 * q + 0) * C + c], v[(8 * q + 1) * C + c]);
+                        t.y = pack_half2(v[(8 * q + 2) * C + c], v[(8 * q + 3) * C + c]);
+                        t.z = pack_half2(v[(8 * q + 4) * C + c], v[(8 * q + 5) * C + c]);
+                        t.w = pack_half2(v[(8 * q + 6) * C + c], v[(8 * q + 7) * C + c]);
+                        reinterpret_cast<uint4*>(o)[q] = t;
+                    }
+                } else {  // P == 4
+                    uint2 t;
+                    t.x = pack_half2(v[0 * C + c], v[1 * C + c]);
+                    t.y = pack_half2(v[2 * C + c], v[3 * C + c]);
+                    *reinterpret_cast<uint2*>(o) = t;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < P / 4; ++q)
+                    reinterpret_cast<float4*>(o)[q] =
+                        make_float4(v[(4 * q + 0) * C + c], v[(4 * q + 1) * C + c],
+                                    v[(4 * q + 2) * C + c], v[(4 * q + 3) * C + c]);
+            }
+        }
+    }
+}
+
+template <int C, int OUT_F16, int LAYOUT>
+__device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
+                                             uint8_t* sout, const UnitRec& rec) {
+    constexpr int P = Group<C>::P;
+    constexpr int GB = Group<C>::kBytes;
+    const int L = p.W * C;
+    const int groups = rec.rows * p.gpr;
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+        const int r = (int)(((uint64_t)(uint32_t)g * p.gpr_inv) >> 32);
+        const int gx = g - r * p.gpr;
+        const int y = rec.y_begin + r;
+        int lo = 0, hi = 0;  // erased pixels [lo, hi) of this group
+        if (y >= rec.erow_lo && y < rec.erow_hi) {
+            lo = min(max(rec.ecol_lo - gx * P, 0), P);
+            hi = min(max(rec.ecol_hi - gx * P, 0), P);
+        }
+        float v[GB];
+        if (lo == 0 && hi == P) {
+#pragma unroll
+            for (int k = 0; k < GB; ++k) v[k] = 0.0f;
+        } else {
+            const int sgx = rec.flip ? (p.gpr - 1 - gx) : gx;
+            const uint8_t* s = sin + (size_t)r * L + (size_t)sgx * GB;
+            uint32_t w[Group<C>::kWords];
+            if (GB == 16) {
+                const uint4 t = *reinterpret_cast<const uint4*>(s);
+                w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
+            } else {
+#pragma unroll
+                for (int q = 0; q < GB / 8; ++q) {
+                    const uint2 t = reinterpret_cast<const uint2*>(s)[q];
+                    w[2 * q] = t.x;
+                    w[2 * q + 1] = t.y;
+                }
+            }
+            if (rec.flip) convert_group<C, true>(w, p.scale, p.bias, v);
+            else convert_group<C, false>(w, p.scale, p.bias, v);
+            if (lo < hi) {
+#pragma unroll
+                for (int k = 0; k < GB; ++k) {
+                    const int i = k / C;
+                    if (i >= lo && i < hi) v[k] = 0.0f;
+                }
+            }
+        }
+        store_group<C, OUT_F16, LAYOUT>(p, sout, r, gx, v);
+    }
+}
+
+template <int C, int OUT_F16, int LAYOUT>
+__device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* sout,
+                                           const UnitRec& rec) {
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    const uint32_t src = smem_u32(sout);
+    if (LAYOUT == TR_LAYOUT_NCHW) {
+        const uint32_t bytes = (uint32_t)rec.rows * p.W * OB;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            uint8_t* g = p.dst + ((((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W) * OB;
+            bulk_s2g(g, src + (uint32_t)c * p.plane_bytes, bytes);
+        }
+    } else {
+        const int ch = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
+        const size_t row_bytes = (size_t)p.W * ch * OB;
+        uint8_t* g = p.dst + ((size_t)rec.n * p.H + rec.y_begin) * row_bytes;
+        bulk_s2g(g, src, (uint32_t)(rec.rows * row_bytes));
+    }
+    bulk_commit();
+}
+
+template <int C, int OUT_F16, int LAYOUT>
+__global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ TiledParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = p.stages;
+    const uint32_t bar0 = smem_u32(smem);
+    const UnitRec* recs = reinterpret_cast<const UnitRec*>(smem + 64);
+    const uint8_t* sin = smem + kHeaderBytes;
+    uint8_t* sout = smem + kHeaderBytes + (size_t)S * p.in_stage;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bar0 + 8u * s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int j = 0; j < S; ++j) {
+            const int u = blockIdx.x + j * gridDim.x;
+            if (u < p.num_units) issue_unit<C>(p, u, j, smem);
+        }
+    }
+
+    int i = 0;
+    bool aborted = false;
+    for (;; ++i) {
+        const int u = blockIdx.x + i * gridDim.x;
+        if (u >= p.num_units) break;
+        const int s = i % S;
+        const bool ok = mbar_wait_bounded(bar0 + 8u * s, (uint32_t)(i / S) & 1u);
+        uint8_t* ob = sout + (size_t)(i & 1) * p.out_stage;
+        if (ok) compute_unit<C, OUT_F16, LAYOUT>(p, sin + (size_t)s * p.in_stage, ob, recs[s]);
+        fence_proxy_async_smem();
+        // The store issued last iteration reads the other output buffer, which
+        // the next iteration overwrites: it must be done reading first.
+        if (threadIdx.x == 0) bulk_wait_read<0>();
+        if (__syncthreads_or(!ok)) { aborted = true; break; }
+        if (threadIdx.x == 0) {
+            store_unit<C, OUT_F16, LAYOUT>(p, ob, recs[s]);
+            const int un = blockIdx.x + (i + S) * gridDim.x;
+            if (un < p.num_units) issue_unit<C>(p, un, s, smem);
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (aborted) {
+            atomicOr(&g_device_status, kStatusTimeout);
+            // drain the loads still in flight (bounded) before leaving
+            for (int j = i; j < i + S; ++j) {
+                const int u = blockIdx.x + j * gridDim.x;
+                if (u >= p.num_units) break;
+                if (!mbar_wait_bounded(bar0 + 8u * (j % S), (uint32_t)(j / S) & 1u)) break;
+            }
+        }
+        bulk_wait_all<0>();
+    }
+}
+
+// -------------------------------------------------------------- generic ---
+
+struct GenericParams {
+    const uint8_t* src;
+    uint8_t* dst;
+    const tr_aug_param* aug;
+    long long total;       // output elements
+    int H, W, C;
+    float scale[4];
+    float bias[4];
+};
+
+template <int OUT_F16, int LAYOUT>
+__global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ GenericParams p) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long W = p.W, H = p.H, C = p.C;
+    for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < p.total; o += stride) {
+        long long n, y, x, c;
+        if (LAYOUT == TR_LAYOUT_NCHW) {
+            x = o % W;
+            long long t = o / W;
+            y = t % H;
+            t /= H;
+            c = t % C;
+            n = t / C;
+        } else {
+            const long long ch = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
+            c = o % ch;
+            const long long pix = o / ch;
+            x = pix % W;
+            const long long t = pix / W;
+            y = t % H;
+            n = t / H;
+        }
+        float v = 0.0f;
+        if (c < C) {
+            bool flip = false, erased = false;
+            if (p.aug != nullptr) {
+                const tr_aug_param a = p.aug[n];
+                flip = (a.flip != 0);
+                erased = a.h > 0 && a.w > 0 && y >= a.y0 && y < (long long)a.y0 + a.h &&
+                         x >= a.x0 && x < (long long)a.x0 + a.w;
+            }
+            if (!erased) {
+                const long long xs = flip ? (W - 1 - x) : x;
+                const uint8_t b = __ldg(p.src + ((n * H + y) * W + xs) * C + c);
+                v = __fmaf_rn((float)b, p.scale[c], p.bias[c]);
+            }
+        }
+        if (OUT_F16) reinterpret_cast<__half*>(p.dst)[o] = __float2half_rn(v);
+        else reinterpret_cast<float*>(p.dst)[o] = v;
+    }
+}
+
+// ------------------------------------------------------------ host side ---
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int smem_optin = 0;
+};
+
+DeviceInfo device_info(int dev) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return DeviceInfo{};
+    if (cache[dev].sm_count == 0) {
+        cudaDeviceGetAttribute(&cache[dev].sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    }
+    return cache[dev];
+}
+
+using TiledFn = void (*)(TiledParams);
+using GenericFn = void (*)(GenericParams);
+
+template <int C, int F16>
+TiledFn pick_tiled_layout(int layout) {
+    switch (layout) {
+    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC>;
+    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW>;
+    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4>;
+    }
+}
+
+template <int C>
+TiledFn pick_tiled_dtype(int f16, int layout) {
+    return f16 ? pick_tiled_layout<C, 1>(layout) : pick_tiled_layout<C, 0>(layout);
+}
+
+TiledFn pick_tiled(int C, int f16, int layout) {
+    switch (C) {
+    case 1: return pick_tiled_dtype<1>(f16, layout);
+    case 2: return pick_tiled_dtype<2>(f16, layout);
+    case 3: return pick_tiled_dtype<3>(f16, layout);
+    default: return pick_tiled_dtype<4>(f16, layout);
+    }
+}
+
+GenericFn pick_generic(int f16, int layout) {
+    if (f16) {
+        if (layout == TR_LAYOUT_NHWC) return generic_kernel<1, TR_LAYOUT_NHWC>;
+        if (layout == TR_LAYOUT_NCHW) return generic_kernel<1, TR_LAYOUT_NCHW>;
+        return generic_kernel<1, TR_LAYOUT_NHWC4>;
+    }
+    if (layout == TR_LAYOUT_NHWC) return generic_kernel<0, TR_LAYOUT_NHWC>;
+    if (layout == TR_LAYOUT_NCHW) return generic_kernel<0, TR_LAYOUT_NCHW>;
+    return generic_kernel<0, TR_LAYOUT_NHWC4>;
+}
+
+int group_pixels(int C) { return C == 3 ? 8 : 16 / C; }
+
+// Tiled launch geometry for one problem.
+struct TiledPlan {
+    bool ok = false;
+    int R = 0, bands = 0, stages = 0, threads = 0;
+    uint32_t in_stage = 0, out_stage = 0, plane_bytes = 0;
+    size_t smem = 0;
+};
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit) {
+    TiledPlan pl;
+    const int ob = f16 ? 2 : 4;
+    const int P = group_pixels(C);
+    const size_t L = (size_t)W * C;
+    const int gpr = W / P;
+    const int out_ch = (layout == TR_LAYOUT_NHWC4) ? 4 : C;
+    const size_t out_row = (size_t)W * out_ch * ob;
+    // about 6 KB of source per band; prefer a band height that divides H
+    const size_t target = 6144;
+    int R = (int)std::max<size_t>(1, std::min<size_t>((size_t)H, target / L));
+    for (int r = R; r >= (R + 1) / 2; --r) {
+        if (H % r == 0) { R = r; break; }
+    }
+    while (R > 1 && (size_t)R * gpr >= 65536) --R;
+    if ((size_t)R * gpr >= 65536) return pl;
+    int stages = std::min(4, kMaxStages);
+    for (;;) {
+        const size_t in_stage = round_up((size_t)R * L, 128);
+        const size_t out_stage = round_up((size_t)R * out_row, 128);
+        const size_t smem = kHeaderBytes + stages * in_stage + 2 * out_stage;
+        if (in_stage < (1u << 20) && smem <= (size_t)smem_limit) {
+            pl.ok = true;
+            pl.R = R;
+            pl.bands = (H + R - 1) / R;
+            pl.stages = stages;
+            pl.in_stage = (uint32_t)in_stage;
+            pl.out_stage = (uint32_t)out_stage;
+            pl.plane_bytes = (uint32_t)((size_t)R * W * ob);
+            pl.smem = smem;
+            const int groups = R * gpr;
+            pl.threads = (int)std::min<size_t>(256, std::max<size_t>(64, round_up(groups, 32)));
+            return pl;
+        }
+        if (stages > 2) { --stages; continue; }
+        if (R > 1) { R = std::max(1, R / 2); stages = 4; continue; }
+        return pl;
+    }
+}
+
+bool check_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return true;
+    set_last_error(what, (int)e);
+    return false;
+}
+
+int launch_tiled(const LaunchArgs& a) {
+    int dev = 0;
+    if (!check_cuda(cudaGetDevice(&dev), "cudaGetDevice")) return TR_ERR_CUDA;
+    const DeviceInfo di = device_info(dev);
+    if (di.sm_count <= 0) {
+        set_last_error("cudaDeviceGetAttribute", (int)cudaGetLastError());
+        return TR_ERR_CUDA;
+    }
+    const int f16 = (a.out_dtype == TR_OUT_F16);
+    const TiledPlan pl = plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin);
+    if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
+
+    TiledParams p;
+    p.src = a.src;
+    p.dst = static_cast<uint8_t*>(a.dst);
+    p.aug = a.aug;
+    p.N = a.N; p.H = a.H; p.W = a.W;
+    p.R = pl.R;
+    p.bands = pl.bands;
+    p.num_units = a.N * pl.bands;
+    p.gpr = a.W / group_pixels(a.C);
+    p.gpr_inv = ((1ull << 32) + (uint64_t)p.gpr - 1) / (uint64_t)p.gpr;
+    p.in_stage = pl.in_stage;
+    p.out_stage = pl.out_stage;
+    p.plane_bytes = pl.plane_bytes;
+    p.stages = pl.stages;
+    for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
+
+    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout);
+    // Per-kernel opt-in to the device's largest dynamic shared memory (once),
+    // and the occupancy of each (threads, shared memory) geometry.
+    struct Cached { const void* fn; int dev; size_t smem; int threads; int blocks; };
+    static std::mutex mu;
+    static Cached cache[256];
+    static int ncache = 0;
+    static const void* opted[64][32];
+    static int nopted[64];
+    int blocks_per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        bool done = false;
+        for (int k = 0; k < nopted[dev]; ++k) done = done || opted[dev][k] == (const void*)fn;
+        if (!done) {
+            if (!check_cuda(cudaFuncSetAttribute((const void*)fn,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 di.smem_optin),
+                            "cudaFuncSetAttribute"))
+                return TR_ERR_CUDA;
+            if (nopted[dev] < 32) opted[dev][nopted[dev]++] = (const void*)fn;
+        }
+        for (int k = 0; k < ncache; ++k) {
+            if (cache[k].fn == (const void*)fn && cache[k].dev == dev && cache[k].smem == pl.smem &&
+                cache[k].threads == pl.threads) {
+                blocks_per_sm = cache[k].blocks;
+                break;
+            }
+        }
+        if (blocks_per_sm == 0) {
+            if (!check_cuda(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, (const void*)fn,
+                                                                         pl.threads, pl.smem),
+                            "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
+                return TR_ERR_CUDA;
+            if (blocks_per_sm <= 0) return TR_ERR_NOT_SUPPORTED;
+            if (ncache < 256) cache[ncache++] = Cached{(const void*)fn, dev, pl.smem, pl.threads, blocks_per_sm};
+        }
+    }
+    const long long max_ctas = (long long)blocks_per_sm * di.sm_count;
+    long long grid = std::min<long long>(p.num_units, max_ctas);
+    // equalise the number of units per CTA
+    const long long waves = (p.num_units + grid - 1) / grid;
+    grid = (p.num_units + waves - 1) / waves;
+
+    fn<<<(unsigned)grid, pl.threads, pl.smem, static_cast<cudaStream_t>(a.stream)>>>(p);
+    if (!check_cuda(cudaGetLastError(), "tiled kernel launch")) return TR_ERR_CUDA;
+    count_launch();
+    return TR_OK;
+}
+
+int launch_generic(const LaunchArgs& a) {
+    int dev = 0;
+    if (!check_cuda(cudaGetDevice(&dev), "cudaGetDevice")) return TR_ERR_CUDA;
+    const DeviceInfo di = device_info(dev);
+    if (di.sm_count <= 0) {
+        set_last_error("cudaDeviceGetAttribute", (int)cudaGetLastError());
+        return TR_ERR_CUDA;
+    }
+    const int f16 = (a.out_dtype == TR_OUT_F16);
+    const int out_ch = (a.out_layout == TR_LAYOUT_NHWC4) ? 4 : a.C;
+    GenericParams p;
+    p.src = a.src;
+    p.dst = static_cast<uint8_t*>(a.dst);
+    p.aug = a.aug;
+    p.total = (long long)a.N * a.H * a.W * out_ch;
+    p.H = a.H; p.W = a.W; p.C = a.C;
+    for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
+    const int threads = 256;
+    long long grid = (p.total + threads - 1) / threads;
+    grid = std::min<long long>(grid, (long long)di.sm_count * 8);
+    if (grid < 1) grid = 1;
+    pick_generic(f16, a.out_layout)<<<(unsigned)grid, threads, 0, static_cast<cudaStream_t>(a.stream)>>>(p);
+    if (!check_cuda(cudaGetLastError(), "generic kernel launch")) return TR_ERR_CUDA;
+    count_launch();
+    return TR_OK;
+}
+
+std::atomic<uint64_t> g_launches{0};
+
+}  // namespace
+
+bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C, int out_dtype,
+                     int out_layout) {
+    const int ob = (out_dtype == TR_OUT_F16) ? 2 : 4;
+    if (C < 1 || C > 4) return false;
+    if (((uintptr_t)src & 15u) != 0 || ((uintptr_t)dst & 15u) != 0) return false;
+    if (((long long)W * C) % 16 != 0) return false;
+    if (out_layout == TR_LAYOUT_NCHW && ((long long)W * ob) % 16 != 0) return false;
+    if ((long long)N * H > (1LL << 31) - 1) return false;   // unit indices are int
+    return true;
+}
+
+int launch(const LaunchArgs& a, int variant) {
+    if (variant == TR_VARIANT_TILED) return launch_tiled(a);
+    return launch_generic(a);
+}
+
+int read_device_status(int* flags, bool clear) {
+    unsigned int v = 0;
+    if (!check_cuda(cudaMemcpyFromSymbol(&v, g_device_status, sizeof v), "cudaMemcpyFromSymbol"))
+        return TR_ERR_CUDA;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (!check_cuda(cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero), "cudaMemcpyToSymbol"))
+            return TR_ERR_CUDA;
+    }
+    if (flags) *flags = (int)v;
+    return TR_OK;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
+}  // namespace trfn

@@ -1,0 +1,44 @@
+// Internal declarations shared by the library's translation units (not part
+// of the C ABI; see include/tr_fused_norm.h for that).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "tr_fused_norm.h"
+
+namespace trfn {
+
+// Arguments of one fused-normalisation launch after host validation.
+struct LaunchArgs {
+    const uint8_t* src;
+    void* dst;
+    int N, H, W, C;
+    float scale[4];   // 1/(255*std_c), formed in binary64, rounded to binary32
+    float bias[4];    // -mean_c/std_c, formed in binary64, rounded to binary32
+    const tr_aug_param* aug;
+    int out_dtype;
+    int out_layout;
+    void* stream;
+};
+
+// Whether the tiled kernel's preconditions hold for these arguments.
+bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C,
+                     int out_dtype, int out_layout);
+
+// Launches the chosen kernel (TR_VARIANT_TILED or TR_VARIANT_GENERIC) on
+// a.stream.  Returns a tr_status.
+int launch(const LaunchArgs& a, int variant);
+
+// Reads (and optionally clears) the device status word of the current device.
+int read_device_status(int* flags, bool clear);
+
+// Per-thread last CUDA error text.
+void set_last_error(const char* what, int cuda_error);
+const char* last_error();
+
+// Count of kernels launched by this library.
+void count_launch();
+uint64_t launch_count();
+
+}  // namespace trfn

@@ -1,0 +1,227 @@
+// Double-buffered feeding of the fused kernel from pinned host memory.
+//
+// The TransferStation of the Tech-Renaissance article "(10) Multi-threaded
+// preprocessing, NUMA awareness, asynchronous double buffering"
+// (tech-renaissance.cn/blog/?p=481, §四) alternates two pinned buffers A/B with
+// four atomic readable/writeable flags and a condition variable, so that the
+// CPU fills one buffer while the GPU consumes the other.  On GB300 the
+// preprocessing itself runs on the GPU, so the buffers that alternate are two
+// device input slots, and the hand-over is expressed with CUDA events between
+// a copy stream and a compute stream instead of host flags:
+//
+//   batch k, slot s = k % 2
+//   copy stream:    wait done[s]   (the kernel that last read slot s)
+//                   H2D images (and records) -> slot s;   record copied[s]
+//   compute stream: wait copied[s]; [wait d2h[s]]  (result copy of batch k-2)
+//                   fused kernel slot s -> d_dst;         record done[s]
+//   d2h stream:     wait done[s];  D2H d_dst -> h_dst;    record d2h[s]
+//
+// so the copy of batch k+1 overlaps the kernel of batch k.  The host never
+// blocks except in tr_ts_sync(), which polls the events against a deadline.
+// Slot layout: [images][pad to 256][records], after the article's
+// [labels][padding][image] zones aligned to 256 bytes (§四).
+
+#include <cuda_runtime.h>
+
+#include <chrono>
+#include <mutex>
+#include <new>
+#include <thread>
+
+#include "internal.h"
+
+struct tr_transfer_station {
+    int device = 0;
+    uint8_t* slot[2] = {nullptr, nullptr};
+    size_t slot_bytes = 0;
+    cudaStream_t copy = nullptr, compute = nullptr, d2h = nullptr;
+    cudaEvent_t copied[2] = {nullptr, nullptr};
+    cudaEvent_t done[2] = {nullptr, nullptr};
+    cudaEvent_t d2h_done[2] = {nullptr, nullptr};
+    bool done_used[2] = {false, false};
+    bool d2h_used[2] = {false, false};
+    long long next_batch = 0;
+    std::mutex mu;
+};
+
+namespace {
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+bool ok(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return true;
+    trfn::set_last_error(what, (int)e);
+    return false;
+}
+
+// Makes `device` current for the lifetime of the guard.
+class DeviceGuard {
+ public:
+    explicit DeviceGuard(int device) {
+        if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+        if (prev_ != device) cudaSetDevice(device);
+    }
+    ~DeviceGuard() {
+        if (prev_ >= 0) cudaSetDevice(prev_);
+    }
+
+ private:
+    int prev_ = -1;
+};
+
+void destroy_events(tr_transfer_station* ts) {
+    for (int s = 0; s < 2; ++s) {
+        if (ts->copied[s]) cudaEventDestroy(ts->copied[s]);
+        if (ts->done[s]) cudaEventDestroy(ts->done[s]);
+        if (ts->d2h_done[s]) cudaEventDestroy(ts->d2h_done[s]);
+        ts->copied[s] = ts->done[s] = ts->d2h_done[s] = nullptr;
+    }
+}
+
+// TR_OK when every used event has completed, TR_ERR_TIMEOUT at the deadline.
+int wait_events(tr_transfer_station* ts, int timeout_ms) {
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        bool all = true;
+        for (int s = 0; s < 2; ++s) {
+            cudaEvent_t evs[2] = {ts->done_used[s] ? ts->done[s] : nullptr,
+                                  ts->d2h_used[s] ? ts->d2h_done[s] : nullptr};
+            for (cudaEvent_t ev : evs) {
+                if (!ev) continue;
+                const cudaError_t e = cudaEventQuery(ev);
+                if (e == cudaErrorNotReady) {
+                    all = false;
+                } else if (e != cudaSuccess) {
+                    trfn::set_last_error("cudaEventQuery", (int)e);
+                    return TR_ERR_CUDA;
+                }
+            }
+        }
+        if (all) return TR_OK;
+        if (timeout_ms >= 0) {
+            const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                                std::chrono::steady_clock::now() - t0)
+                                .count();
+            if (ms >= timeout_ms) return TR_ERR_TIMEOUT;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tr_ts_slot_bytes(int N, int H, int W, int C) {
+    if (N < 0 || H < 1 || W < 1 || C < 1) return 0;
+    return align256((size_t)N * H * W * C) + (size_t)N * sizeof(tr_aug_param);
+}
+
+int tr_ts_create(int device, void* const d_slot[2], size_t slot_bytes, void* copy_stream,
+                 void* compute_stream, void* d2h_stream, tr_transfer_station** out) {
+    if (out == nullptr || d_slot == nullptr || d_slot[0] == nullptr || d_slot[1] == nullptr ||
+        slot_bytes == 0 || copy_stream == nullptr || compute_stream == nullptr || device < 0)
+        return TR_ERR_INVALID_ARGUMENT;
+    *out = nullptr;
+    tr_transfer_station* ts = new (std::nothrow) tr_transfer_station();
+    if (ts == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    ts->device = device;
+    ts->slot[0] = static_cast<uint8_t*>(d_slot[0]);
+    ts->slot[1] = static_cast<uint8_t*>(d_slot[1]);
+    ts->slot_bytes = slot_bytes;
+    ts->copy = static_cast<cudaStream_t>(copy_stream);
+    ts->compute = static_cast<cudaStream_t>(compute_stream);
+    ts->d2h = static_cast<cudaStream_t>(d2h_stream);
+    DeviceGuard guard(device);
+    for (int s = 0; s < 2; ++s) {
+        if (!ok(cudaEventCreateWithFlags(&ts->copied[s], cudaEventDisableTiming), "cudaEventCreate") ||
+            !ok(cudaEventCreateWithFlags(&ts->done[s], cudaEventDisableTiming), "cudaEventCreate") ||
+            !ok(cudaEventCreateWithFlags(&ts->d2h_done[s], cudaEventDisableTiming), "cudaEventCreate")) {
+            destroy_events(ts);
+            delete ts;
+            return TR_ERR_CUDA;
+        }
+    }
+    *out = ts;
+    return TR_OK;
+}
+
+int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params,
+                 void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean,
+                 const float* std, int out_dtype, int out_layout, long long* batch_index) {
+    if (ts == nullptr || h_src == nullptr || d_dst == nullptr || N < 1 || H < 1 || W < 1 || C < 1 ||
+        C > 4 || mean == nullptr || std == nullptr)
+        return TR_ERR_INVALID_ARGUMENT;
+    if (out_dtype != TR_OUT_F32 && out_dtype != TR_OUT_F16) return TR_ERR_INVALID_ARGUMENT;
+    if (out_layout != TR_LAYOUT_NHWC && out_layout != TR_LAYOUT_NCHW && out_layout != TR_LAYOUT_NHWC4)
+        return TR_ERR_INVALID_ARGUMENT;
+    if (h_dst != nullptr && ts->d2h == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    const size_t in_bytes = (size_t)N * H * W * C;
+    const size_t rec_off = align256(in_bytes);
+    const size_t need = rec_off + (h_params ? (size_t)N * sizeof(tr_aug_param) : 0);
+    if (need > ts->slot_bytes) return TR_ERR_INVALID_ARGUMENT;
+    const size_t out_bytes = (size_t)N * H * W * (out_layout == TR_LAYOUT_NHWC4 ? 4 : C) *
+                             (out_dtype == TR_OUT_F16 ? 2 : 4);
+
+    std::lock_guard<std::mutex> lock(ts->mu);
+    DeviceGuard guard(ts->device);
+    const long long k = ts->next_batch;
+    const int s = (int)(k & 1);
+    uint8_t* slot = ts->slot[s];
+    const tr_aug_param* d_params =
+        h_params ? reinterpret_cast<const tr_aug_param*>(slot + rec_off) : nullptr;
+
+    if (ts->done_used[s] && !ok(cudaStreamWaitEvent(ts->copy, ts->done[s], 0), "cudaStreamWaitEvent"))
+        return TR_ERR_CUDA;
+    if (!ok(cudaMemcpyAsync(slot, h_src, in_bytes, cudaMemcpyHostToDevice, ts->copy), "cudaMemcpyAsync"))
+        return TR_ERR_CUDA;
+    if (h_params && !ok(cudaMemcpyAsync(slot + rec_off, h_params, (size_t)N * sizeof(tr_aug_param),
+                                        cudaMemcpyHostToDevice, ts->copy),
+                        "cudaMemcpyAsync"))
+        return TR_ERR_CUDA;
+    if (!ok(cudaEventRecord(ts->copied[s], ts->copy), "cudaEventRecord")) return TR_ERR_CUDA;
+
+    if (!ok(cudaStreamWaitEvent(ts->compute, ts->copied[s], 0), "cudaStreamWaitEvent")) return TR_ERR_CUDA;
+    if (ts->d2h_used[s] &&
+        !ok(cudaStreamWaitEvent(ts->compute, ts->d2h_done[s], 0), "cudaStreamWaitEvent"))
+        return TR_ERR_CUDA;
+    const int rc = tr_fused_norm(slot, d_dst, N, H, W, C, mean, std, d_params, out_dtype, out_layout,
+                                 ts->compute);
+    if (rc != TR_OK) return rc;
+    if (!ok(cudaEventRecord(ts->done[s], ts->compute), "cudaEventRecord")) return TR_ERR_CUDA;
+    ts->done_used[s] = true;
+
+    if (h_dst != nullptr) {
+        if (!ok(cudaStreamWaitEvent(ts->d2h, ts->done[s], 0), "cudaStreamWaitEvent")) return TR_ERR_CUDA;
+        if (!ok(cudaMemcpyAsync(h_dst, d_dst, out_bytes, cudaMemcpyDeviceToHost, ts->d2h),
+                "cudaMemcpyAsync"))
+            return TR_ERR_CUDA;
+        if (!ok(cudaEventRecord(ts->d2h_done[s], ts->d2h), "cudaEventRecord")) return TR_ERR_CUDA;
+        ts->d2h_used[s] = true;
+    }
+    ts->next_batch = k + 1;
+    if (batch_index) *batch_index = k;
+    return TR_OK;
+}
+
+int tr_ts_sync(tr_transfer_station* ts, int timeout_ms) {
+    if (ts == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(ts->mu);
+    DeviceGuard guard(ts->device);
+    return wait_events(ts, timeout_ms);
+}
+
+int tr_ts_destroy(tr_transfer_station* ts) {
+    if (ts == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    int rc;
+    {
+        std::lock_guard<std::mutex> lock(ts->mu);
+        DeviceGuard guard(ts->device);
+        rc = wait_events(ts, -1);
+        destroy_events(ts);
+    }
+    delete ts;
+    return rc;
+}
+
+}  // extern "C"

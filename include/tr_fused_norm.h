@@ -1,0 +1,241 @@
+/*
+ * tr_fused_norm.h — C ABI of the GB300 fused normalisation library (libtrfn.so).
+ *
+ * One memory pass turns a batch of uint8 NHWC images into normalised binary32
+ * or binary16 tensors: ToTensor (x/255) and per-channel Normalize
+ * ((x - mean)/std) folded into one multiply-add, an optional horizontal flip
+ * and an optional erase rectangle per image.  The operation is the one the
+ * Tech-Renaissance article "(11) FusedNormalization: fuse the last step of data
+ * augmentation into one memory traversal" (tech-renaissance.cn/blog/?p=487)
+ * describes as CPU SIMD code; here it runs as hand-written CUDA for sm_103a.
+ *
+ * Conventions for every entry point:
+ *   - Return a tr_status code; nothing throws across this boundary.
+ *   - Arguments are checked on the host before anything is launched; a call
+ *     that returns TR_ERR_INVALID_ARGUMENT or TR_ERR_NOT_SUPPORTED has not
+ *     touched the GPU.
+ *   - Every buffer is owned by the caller.  Nothing on the call path
+ *     allocates memory.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it; calls do not wait for the GPU.
+ *   - Device pointers must stay valid until the enqueued work has finished.
+ */
+#ifndef TR_FUSED_NORM_H
+#define TR_FUSED_NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  INVALID_ARGUMENT is the article's ValueError (its execute()
+ * rejects an externally set output stride, §五); NOT_SUPPORTED is its
+ * TR_NOT_IMPLEMENTED (§七, FP16 on a CPU without the needed extension).     */
+typedef enum tr_status {
+    TR_OK = 0,
+    TR_ERR_INVALID_ARGUMENT = 1,
+    TR_ERR_NOT_SUPPORTED = 2,
+    TR_ERR_CUDA = 3,          /* a CUDA runtime call failed; see tr_last_error_message() */
+    TR_ERR_TIMEOUT = 4,       /* a bounded wait ran out (host event wait or device pipeline wait) */
+    TR_ERR_DEVICE = 5         /* a kernel reported an error through the device status word */
+} tr_status;
+
+/* Output element type (article §六 "FP32 and FP16 output"). */
+typedef enum tr_out_dtype {
+    TR_OUT_F32 = 0,           /* binary32 */
+    TR_OUT_F16 = 1            /* binary16, round to nearest even of the binary32 value */
+} tr_out_dtype;
+
+/* Output layout.  The article writes NHWC; FP16 there is always padded to four
+ * channels (§六, §八).  N, H, W, C as in the input.                          */
+typedef enum tr_layout {
+    TR_LAYOUT_NHWC = 0,       /* out[((n*H + y)*W + x)*C + c]                     */
+    TR_LAYOUT_NCHW = 1,       /* out[((n*C + c)*H + y)*W + x]                     */
+    TR_LAYOUT_NHWC4 = 2       /* out[((n*H + y)*W + x)*4 + c], channels C..3 = +0 */
+} tr_layout;
+
+/* Normalisation presets (article §九 "Five normalisation presets"). */
+typedef enum tr_preset {
+    TR_PRESET_NO_NORM = 0,    /* mean 0, std 1 (3 channels): x/255 only          */
+    TR_PRESET_MNIST = 1,      /* 0.1307 / 0.3081 (1 channel)                     */
+    TR_PRESET_CIFAR = 2,
+    TR_PRESET_IMAGENET = 3,
+    TR_PRESET_MLPERF = 4      /* mean (123.68, 116.78, 103.94)/255, std 1/255    */
+} tr_preset;
+
+/* Per-image augmentation record (20 bytes, int32 fields).
+ *   flip      non-zero: output pixel (y, x) takes source pixel (y, W-1-x)
+ *             (article §五: read from the mirrored or the original position).
+ *   y0,x0,h,w erase rectangle in OUTPUT (post-flip) coordinates: every channel
+ *             of output pixels y0 <= y < y0+h, x0 <= x < x0+w is +0.0 (article
+ *             §十二: a memset of the normalised output after the main pass).
+ *             h <= 0 or w <= 0 means no erase.  Parts outside the image are
+ *             ignored (the kernels clip), so a bad record cannot write out of
+ *             bounds; tr_validate_aug_params() reports such records.          */
+typedef struct tr_aug_param {
+    int32_t flip;
+    int32_t y0;
+    int32_t x0;
+    int32_t h;
+    int32_t w;
+} tr_aug_param;
+
+/* Kernel selection, for tests and benchmarks.  AUTO picks TILED whenever its
+ * preconditions hold (16-byte aligned src/dst, W*C a multiple of 16, and for
+ * NCHW W*sizeof(out) a multiple of 16), else GENERIC.  Forcing TILED where
+ * its preconditions fail returns TR_ERR_NOT_SUPPORTED.                      */
+typedef enum tr_variant {
+    TR_VARIANT_AUTO = 0,
+    TR_VARIANT_TILED = 1,     /* persistent CTAs, TMA bulk row-band staging, TMA bulk stores */
+    TR_VARIANT_GENERIC = 2    /* one thread per output element, any shape and alignment      */
+} tr_variant;
+
+/* ------------------------------------------------------------------------
+ * tr_fused_norm — the fused step on a batch (article §五, §六, §八, §十二).
+ *
+ *   src_u8      device, N*H*W*C bytes, compact NHWC uint8.
+ *   dst         device, N*H*W*C' elements of out_dtype in out_layout, compact
+ *               (C' = 4 for TR_LAYOUT_NHWC4, else C).  There is no stride
+ *               argument: like the article's execute(), the output stride is
+ *               fixed by the shape, type and layout.  Must not overlap src.
+ *   N,H,W,C     N >= 0 (0 = nothing to do), H >= 1, W >= 1, 1 <= C <= 4.
+ *   mean, std   host arrays of C floats, read during the call.  std[c] must be
+ *               finite and non-zero, mean[c] finite.  The kernels use
+ *               scale = 1/(255*std) and bias = -mean/std, each formed in
+ *               binary64 and rounded to binary32, in one fused multiply-add.
+ *   aug_params  device array of N tr_aug_param, read in stream order; NULL
+ *               means no flip and no erase for every image.
+ *   out_dtype   tr_out_dtype; out_layout tr_layout.
+ *   stream      cudaStream_t as void*.
+ * Errors: TR_ERR_INVALID_ARGUMENT (bad shape, type, layout, null pointer,
+ * non-finite or zero std, overlapping src/dst, sizes beyond 2^40 elements),
+ * TR_ERR_NOT_SUPPORTED (C > 4), TR_ERR_CUDA (launch failure).  Unaligned
+ * pointers are not an error: they take the GENERIC kernel.                  */
+int tr_fused_norm(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                  const float* mean, const float* std, const tr_aug_param* aug_params,
+                  int out_dtype, int out_layout, void* stream);
+
+/* tr_fused_norm with an explicit kernel choice (tr_variant). */
+int tr_fused_norm_variant(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                          const float* mean, const float* std, const tr_aug_param* aug_params,
+                          int out_dtype, int out_layout, void* stream, int variant);
+
+/* Which kernel AUTO would pick for these arguments (TR_VARIANT_TILED or
+ * TR_VARIANT_GENERIC), through *variant; host only, launches nothing.        */
+int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,
+                       int out_dtype, int out_layout, int* variant);
+
+/* Preset mean/std (article §九).  Writes 3 floats to mean and std (unused
+ * channels get mean 0, std 1) and the channel count to *channels.           */
+int tr_norm_preset(int preset, float mean[3], float std[3], int* channels);
+
+/* ------------------------------------------------------------------------
+ * tr_sample_aug_params — host-side sampling of the per-image records with
+ * the article's random decisions (§五 execute(), §十 uniform()/randint(),
+ * §十二 generate_erase_rect()).  Per image, in this order: when
+ * flip_enabled, one draw u and flip iff u < flip_p (the article hard-codes
+ * 0.5); when erase_enabled and erase_p > 0, one gate draw (no erase unless
+ * u < erase_p), then up to ten attempts of two draws each:
+ *   area = (scale_lo + u*(scale_hi - scale_lo)) * H * W,
+ *   aspect = exp(log(ratio_lo) + u*(log(ratio_hi) - log(ratio_lo))),
+ *   h = round(sqrt(area*aspect)), w = round(sqrt(area/aspect)),
+ * accepted when 0 < h < H and 0 < w < W, followed by y0 uniform on
+ * [0, H-h] and x0 uniform on [0, W-w] (one draw each).  Binary32 arithmetic
+ * without contraction, as written in the article.
+ * Random numbers: Philox4x32-10 keyed by the 64-bit seed (low word first),
+ * counter = the 64-bit offset (low word first) and two zero words; draw k
+ * uses offset+k and its first output word w gives u = (w >> 8) * 2^-24 and
+ * integer draws lo + floor(u*(hi-lo+1)).
+ *   out_host    host array of N records.
+ *   next_offset receives the first unused offset (may be NULL): sampling N1
+ *               then N2 images from it equals sampling N1+N2 at once.
+ * Errors: TR_ERR_INVALID_ARGUMENT for N < 0, H < 1, W < 1, a NULL out_host
+ * with N > 0, non-finite or out-of-order scale/ratio bounds, ratio_lo <= 0. */
+int tr_sample_aug_params(uint64_t seed, uint64_t offset, int N, int H, int W,
+                         int flip_enabled, float flip_p, int erase_enabled, float erase_p,
+                         float scale_lo, float scale_hi, float ratio_lo, float ratio_hi,
+                         tr_aug_param* out_host, uint64_t* next_offset);
+
+/* Host check of N records: TR_OK when every rectangle is either "no erase"
+ * (h <= 0 or w <= 0) or lies inside the H x W image; else
+ * TR_ERR_INVALID_ARGUMENT with the first bad index in *bad_index (may be
+ * NULL).                                                                    */
+int tr_validate_aug_params(const tr_aug_param* host_params, int N, int H, int W, int* bad_index);
+
+/* ------------------------------------------------------------------------
+ * tr_transfer_station — double-buffered feeding of the kernel from pinned
+ * host memory (the TransferStation of the Tech-Renaissance article
+ * "(10) Multi-threaded preprocessing, NUMA awareness, asynchronous double
+ * buffering", tech-renaissance.cn/blog/?p=481, §四): two device slots A/B;
+ * the host-to-device copy of batch k+1 on the copy stream overlaps the
+ * kernel on batch k on the compute stream, with CUDA events handing each
+ * slot over.  The station owns only its events; slots, streams and host
+ * buffers belong to the caller.
+ */
+typedef struct tr_transfer_station tr_transfer_station;
+
+/* Bytes one device slot needs for a batch: the image bytes rounded up to 256,
+ * then N records (the slot layout [images][pad to 256][records]).           */
+size_t tr_ts_slot_bytes(int N, int H, int W, int C);
+
+/*   device        CUDA device ordinal the slots and streams belong to.
+ *   d_slot        two device buffers of slot_bytes each (input slots A/B).
+ *   copy_stream   stream for host-to-device copies (cudaStream_t as void*).
+ *   compute_stream stream for the kernel.
+ *   d2h_stream    stream for optional device-to-host copies of results, or
+ *                 NULL when results stay on the device.
+ * Errors: TR_ERR_INVALID_ARGUMENT for NULL slots/streams/out or a zero size,
+ * TR_ERR_CUDA when events cannot be created.                                */
+int tr_ts_create(int device, void* const d_slot[2], size_t slot_bytes,
+                 void* copy_stream, void* compute_stream, void* d2h_stream,
+                 tr_transfer_station** out);
+
+/* Enqueue batch k: copy h_src (pinned host, N*H*W*C bytes) and, when
+ * h_params is not NULL, its N records (pinned host) into slot k%2 on the copy
+ * stream once the kernel that last read that slot has finished; run
+ * tr_fused_norm from the slot into d_dst (device) on the compute stream after
+ * the copy; when h_dst is not NULL, copy d_dst to h_dst (pinned host) on the
+ * d2h stream after the kernel.  d_dst must not be reused by the caller before
+ * the work it receives has finished (tr_ts_sync, or stream order on the
+ * compute stream).  Returns without waiting for the GPU.
+ * *batch_index (may be NULL) receives k.                                     */
+int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params,
+                 void* d_dst, void* h_dst, int N, int H, int W, int C,
+                 const float* mean, const float* std, int out_dtype, int out_layout,
+                 long long* batch_index);
+
+/* Wait until everything submitted so far has finished, polling events; gives
+ * up after timeout_ms milliseconds with TR_ERR_TIMEOUT (the work stays
+ * queued; a later call may wait again).  timeout_ms < 0 waits without limit. */
+int tr_ts_sync(tr_transfer_station* ts, int timeout_ms);
+
+/* Waits (without limit) for submitted work, then destroys the events. */
+int tr_ts_destroy(tr_transfer_station* ts);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ */
+/* Reads the device status word the kernels set when a bounded pipeline wait
+ * runs out (bit 0); with clear != 0 resets it.  Synchronous (waits for the
+ * current device).                                                          */
+int tr_device_status(int* flags, int clear);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t tr_launch_count(void);
+
+/* Static text for a status code. */
+const char* tr_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread in this library ("" if none). */
+const char* tr_last_error_message(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int tr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TR_FUSED_NORM_H */

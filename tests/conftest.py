@@ -26,3 +26,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_library():
+    """Compile libtrfn.so (nvcc cross-compiles without a GPU) and the oracle
+    before any test runs; a failure to build fails the session loudly."""
+    from image_preprocessing_gb300.build import build_library
+    from oracle.build import build_oracle
+    build_library()
+    build_oracle()
+    yield

@@ -1,0 +1,200 @@
+"""Host-side tests of the C ABI: symbols, argument checks, presets, the
+sampler against the oracle's independent sampler, planning.  No GPU needed:
+every call here either stops at host validation or never touches CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+import image_preprocessing_gb300 as trfn
+from image_preprocessing_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, NOT_SUPPORTED = 0, 1, 2
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(tr_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_function():
+    names = _declared_functions()
+    assert "tr_fused_norm" in names and "tr_ts_submit" in names and len(names) >= 16
+    L = _native.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_binding_covers_every_declared_function():
+    assert set(_declared_functions()) <= set(_native._SIGNATURES)
+
+
+def _f4(v):
+    return _native.float_array(v)
+
+
+M3, S3 = _f4([0.485, 0.456, 0.406]), _f4([0.229, 0.224, 0.225])
+
+
+@pytest.mark.parametrize("args,status", [
+    ((-1, 2, 2, 3, 0, 0), INVALID),      # N < 0
+    ((1, 0, 2, 3, 0, 0), INVALID),       # H < 1
+    ((1, 2, 0, 3, 0, 0), INVALID),       # W < 1
+    ((1, 2, 2, 0, 0, 0), INVALID),       # C < 1
+    ((1, 2, 2, 5, 0, 0), NOT_SUPPORTED),  # C > 4
+    ((1, 2, 2, 3, 2, 0), INVALID),       # unknown dtype
+    ((1, 2, 2, 3, 0, 3), INVALID),       # unknown layout
+    ((1, 1 << 20, 1 << 20, 3, 0, 0), INVALID),  # beyond 2^40 elements
+])
+def test_invalid_shapes_rejected_before_launch(args, status):
+    N, H, W, C, dt, lay = args
+    L = _native.lib()
+    assert L.tr_fused_norm(0x10000, 0x100000000, N, H, W, C, M3, S3, None, dt, lay, None) == status
+
+
+def test_null_and_bad_constants_rejected():
+    L = _native.lib()
+    assert L.tr_fused_norm(None, 0x1000, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
+    assert L.tr_fused_norm(0x1000, None, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
+    assert L.tr_fused_norm(0x1000, 0x100000, 1, 2, 2, 3, None, S3, None, 0, 0, None) == INVALID
+    for bad in ([0.2, 0.0, 0.2], [0.2, float("nan"), 0.2], [0.2, float("inf"), 0.2]):
+        assert L.tr_fused_norm(0x1000, 0x100000, 1, 2, 2, 3, M3, _f4(bad), None, 0, 0, None) == INVALID
+    assert L.tr_fused_norm(0x1000, 0x100000, 1, 2, 2, 3, _f4([0, float("nan"), 0]), S3, None, 0, 0, None) == INVALID
+    # overlapping src and dst
+    assert L.tr_fused_norm(0x1000, 0x1004, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
+    # a bad kernel choice
+    assert L.tr_fused_norm_variant(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 9) == INVALID
+
+
+def test_empty_batch_is_a_no_op():
+    L = _native.lib()
+    assert L.tr_fused_norm(None, None, 0, 2, 2, 3, M3, S3, None, 1, 0, None) == OK
+
+
+def test_forced_tiled_on_unsupported_shape_is_not_supported():
+    L = _native.lib()
+    # W*C = 28 is not a multiple of 16
+    assert L.tr_fused_norm_variant(0x1000, 0x100000, 2, 28, 28, 1, M3, S3, None, 0, 0, None, 1) == NOT_SUPPORTED
+    # misaligned source pointer
+    assert L.tr_fused_norm_variant(0x1001, 0x100000, 2, 32, 32, 3, M3, S3, None, 0, 0, None, 1) == NOT_SUPPORTED
+
+
+@pytest.mark.parametrize("shape,dt,lay,src,dst,want", [
+    ((256, 224, 224, 3), 1, 0, 0x1000, 0x10000000, 1),
+    ((256, 224, 224, 3), 0, 1, 0x1000, 0x10000000, 1),
+    ((16, 32, 32, 3), 0, 0, 0x1000, 0x10000000, 1),
+    ((200, 28, 28, 1), 0, 0, 0x1000, 0x10000000, 2),  # W*C = 28
+    ((4, 8, 12, 4), 1, 1, 0x1000, 0x10000000, 2),     # NCHW fp16 row of 24 bytes
+    ((4, 8, 12, 4), 0, 1, 0x1000, 0x10000000, 1),
+    ((4, 8, 16, 3), 1, 0, 0x1008, 0x10000000, 2),     # src not 16-byte aligned
+    ((4, 8, 16, 3), 1, 0, 0x1000, 0x10000004, 2),     # dst not 16-byte aligned
+])
+def test_plan_picks_the_kernel(shape, dt, lay, src, dst, want):
+    assert trfn.tr_fused_norm_plan(src, dst, *shape, dt, lay) == want
+
+
+def test_presets_match_the_article_table():
+    expect = {
+        "NO_NORM": ([0, 0, 0], [1, 1, 1], 3),
+        "MNIST": ([0.1307], [0.3081], 1),
+        "CIFAR": ([0.4914, 0.4822, 0.4465], [0.2470, 0.2435, 0.2616], 3),
+        "IMAGENET": ([0.485, 0.456, 0.406], [0.229, 0.224, 0.225], 3),
+        "MLPERF": ([123.68 / 255, 116.78 / 255, 103.94 / 255], [1 / 255] * 3, 3),
+    }
+    for name, (m, s, ch) in expect.items():
+        mean, std, c = trfn.tr_norm_preset(name)
+        assert c == ch
+        np.testing.assert_allclose(mean, m, rtol=1e-6)
+        np.testing.assert_allclose(std, s, rtol=1e-6)
+    L = _native.lib()
+    m, s, ch = (ctypes.c_float * 3)(), (ctypes.c_float * 3)(), ctypes.c_int()
+    assert L.tr_norm_preset(5, m, s, ctypes.byref(ch)) == INVALID
+
+
+@pytest.mark.parametrize("kw", [
+    dict(seed=2003, offset=0, N=512, H=224, W=224),
+    dict(seed=1, offset=12345, N=300, H=32, W=32, erase_p=0.9),
+    dict(seed=7, offset=0, N=200, H=28, W=28, flip=False),
+    dict(seed=9, offset=5, N=100, H=5, W=3, erase_p=1.0),
+    dict(seed=2 ** 40 + 3, offset=2 ** 33, N=64, H=224, W=224, scale=(0.1, 0.5), ratio=(0.5, 2.0)),
+    dict(seed=3, offset=0, N=50, H=224, W=224, erase=False),
+    dict(seed=3, offset=0, N=50, H=224, W=224, flip_p=0.25, erase_p=0.3),
+])
+def test_sampler_matches_the_oracle_sampler(kw):
+    kw = dict(kw)
+    seed, offset, N, H, W = kw.pop("seed"), kw.pop("offset"), kw.pop("N"), kw.pop("H"), kw.pop("W")
+    a, na = trfn.tr_sample_aug_params(seed, offset, N, H, W, **kw)
+    b, nb = oracle.sample_aug_params(seed, offset, N, H, W, **kw)
+    assert np.array_equal(a, b) and na == nb
+
+
+def test_sampler_rejects_bad_arguments():
+    L = _native.lib()
+    nxt = ctypes.c_uint64()
+    assert L.tr_sample_aug_params(0, 0, -1, 4, 4, 1, 0.5, 1, 0.5, 0.02, 0.33, 0.3, 3.3, None,
+                                  ctypes.byref(nxt)) == INVALID
+    assert L.tr_sample_aug_params(0, 0, 3, 4, 4, 1, 0.5, 1, 0.5, 0.02, 0.33, 0.3, 3.3, None,
+                                  ctypes.byref(nxt)) == INVALID
+    with pytest.raises(trfn.TrError):
+        trfn.tr_sample_aug_params(0, 0, 4, 4, 4, ratio=(0.0, 3.3))
+    with pytest.raises(trfn.TrError):
+        trfn.tr_sample_aug_params(0, 0, 4, 4, 4, scale=(0.5, 0.1))
+
+
+def test_validate_aug_params():
+    good = np.array([[0, 0, 0, 0, 0], [1, 2, 3, 4, 5], [0, 0, 0, 10, 10], [1, 9, 9, -1, 3]], np.int32)
+    assert trfn.tr_validate_aug_params(good, 10, 10) == -1
+    bad = good.copy()
+    bad[2, 3] = 11
+    assert trfn.tr_validate_aug_params(bad, 10, 10) == 2
+    bad = good.copy()
+    bad[1, 2] = -1
+    assert trfn.tr_validate_aug_params(bad, 10, 10) == 1
+
+
+def test_slot_bytes_layout():
+    # images rounded up to 256 bytes, then the 20-byte records
+    assert trfn.tr_ts_slot_bytes(256, 224, 224, 3) == 256 * 224 * 224 * 3 + 256 * 20
+    assert trfn.tr_ts_slot_bytes(3, 5, 7, 3) == 512 + 60
+    assert trfn.tr_ts_slot_bytes(-1, 5, 7, 3) == 0
+
+
+def test_status_strings():
+    L = _native.lib()
+    for s in range(6):
+        assert L.tr_status_string(s)
+    assert L.tr_status_string(99) == b"unknown status"
+    assert L.tr_version() >= 100
+
+
+def test_package_does_not_import_the_oracle_and_fails_without_library():
+    code = (
+        "import sys, image_preprocessing_gb300 as t;"
+        "assert 'oracle' not in sys.modules;"
+        "from image_preprocessing_gb300 import _native;"
+        "_native.LIB_PATH = '/nonexistent/libtrfn.so'; _native._lib = None\n"
+        "try:\n    _native.lib()\nexcept ImportError:\n    print('raised')\n"
+    )
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "raised" in out.stdout
+
+
+def test_product_sources_never_reference_the_oracle():
+    pkg = os.path.join(ROOT, "image_preprocessing_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, fn), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text and "liboracle" not in text, fn

@@ -1,0 +1,167 @@
+"""GPU parity: the CUDA kernels (through the C ABI) against the CPU oracle,
+element by element on the same seeded inputs.
+
+Bars: binary32 max-abs <= 2e-6; binary16 within 1 ulp of the oracle's
+round-to-nearest binary16 of its binary32 value; erased elements and padding
+exactly +0; erase masks and flip positions exact."""
+import numpy as np
+import pytest
+
+import oracle
+import image_preprocessing_gb300 as trfn
+from image_preprocessing_gb300 import synth
+from parity_util import assert_parity, check_case, gpu_run, zero_mask
+
+pytestmark = pytest.mark.gpu
+
+F32, F16 = trfn.OUT_F32, trfn.OUT_F16
+NHWC, NCHW, NHWC4 = trfn.LAYOUT_NHWC, trfn.LAYOUT_NCHW, trfn.LAYOUT_NHWC4
+AUTO, TILED, GENERIC = trfn.VARIANT_AUTO, trfn.VARIANT_TILED, trfn.VARIANT_GENERIC
+IMNET = (np.array(synth.IMAGENET_MEAN, np.float32), np.array(synth.IMAGENET_STD, np.float32))
+
+
+def _config_case(k):
+    cfg = synth.CONFIGS[k]
+    src = synth.config_pixels(k)
+    aug = None
+    if cfg["flip"] or cfg["erase"]:
+        aug, _ = oracle.sample_aug_params(2000 + k, 0, cfg["N"], cfg["H"], cfg["W"], flip=cfg["flip"],
+                                          erase=cfg["erase"], erase_p=cfg["erase_p"])
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    dt = F16 if cfg["out_dtype"] == "f16" else F32
+    return cfg, src, aug, mean, std, dt
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_configs_full_size(k):
+    cfg, src, aug, mean, std, dt = _config_case(k)
+    for lay in cfg["layouts"]:
+        layout = NCHW if lay == "nchw" else NHWC
+        gpu, ref = check_case(src, mean, std, aug, dt, layout)
+        if cfg["mean"] != synth.MNIST_MEAN:
+            # IMAGENET has no normalised zero: the erase mask is exactly the zero mask
+            assert np.array_equal(zero_mask(gpu, layout, dt), zero_mask(ref, layout, dt))
+
+
+def test_config3_both_kernels_bit_identical():
+    cfg, src, aug, mean, std, dt = _config_case(3)
+    a, _ = gpu_run(src, mean, std, aug, dt, NHWC, TILED)
+    b, _ = gpu_run(src, mean, std, aug, dt, NHWC, GENERIC)
+    assert np.array_equal(a, b)
+
+
+def test_repeat_runs_are_bit_identical():
+    cfg, src, aug, mean, std, dt = _config_case(1)
+    a, _ = gpu_run(src, mean, std, aug, dt, NHWC)
+    b, _ = gpu_run(src, mean, std, aug, dt, NHWC)
+    assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+SHAPES_TILED = [
+    (1, 1, 16, 1), (3, 37, 64, 3), (2, 9, 48, 3), (4, 20, 40, 2), (2, 13, 12, 4),
+    (5, 64, 32, 1), (2, 70, 128, 3), (1, 224, 224, 3),
+]
+SHAPES_GENERIC = [(3, 5, 7, 3), (2, 1, 1, 1), (4, 28, 28, 1), (2, 11, 13, 2), (1, 3, 5, 4)]
+
+
+@pytest.mark.parametrize("shape", SHAPES_TILED + SHAPES_GENERIC)
+@pytest.mark.parametrize("dt", [F32, F16])
+@pytest.mark.parametrize("layout", [NHWC, NCHW, NHWC4])
+def test_shapes_with_coordinate_images(shape, dt, layout):
+    N, H, W, C = shape
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(31 + N * H + W, N, H, W, allow_outside=True)
+    check_case(src, mean, std, aug, dt, layout)
+
+
+@pytest.mark.parametrize("shape", SHAPES_TILED)
+@pytest.mark.parametrize("layout", [NHWC, NCHW, NHWC4])
+def test_tiled_and_generic_agree(shape, layout):
+    N, H, W, C = shape
+    src = synth.pixels_uniform(N + H + W + C, N, H, W, C)
+    mean, std = IMNET[0][:C] if C <= 3 else np.zeros(4, np.float32), IMNET[1][:C] if C <= 3 else np.ones(4, np.float32)
+    aug = synth.random_records(5, N, H, W)
+    for dt in (F32, F16):
+        if layout == NCHW and (W * (2 if dt == F16 else 4)) % 16:
+            continue
+        a, _ = gpu_run(src, mean, std, aug, dt, layout, TILED)
+        b, _ = gpu_run(src, mean, std, aug, dt, layout, GENERIC)
+        assert np.array_equal(a, b)
+
+
+def test_erase_edge_cases():
+    N, H, W, C = 8, 16, 32, 3
+    src = synth.pixels_uniform(3, N, H, W, C)
+    aug = np.array([
+        [0, 0, 0, H, W],            # the whole image: no source byte needed
+        [1, 0, 0, H, W],
+        [0, 3, 0, 5, W],            # full-width rows
+        [1, 0, 5, H, 11],           # full-height columns, flipped
+        [0, -5, -5, 100, 100],      # far outside on every side
+        [1, H - 1, W - 1, 1, 1],    # one pixel, flipped
+        [0, 4, 4, 0, 7],            # h = 0: no erase
+        [1, 20, 40, 3, 3],          # entirely outside: no erase
+    ], np.int32)
+    for dt in (F32, F16):
+        for layout in (NHWC, NCHW, NHWC4):
+            gpu, ref = check_case(src, IMNET[0], IMNET[1], aug, dt, layout)
+            assert np.array_equal(zero_mask(gpu, layout, dt), zero_mask(ref, layout, dt))
+
+
+def test_flip_positions_exact():
+    N, H, W, C = 4, 8, 48, 3
+    src = synth.coordinate_image(N, H, W, C)
+    aug = np.zeros((N, 5), np.int32)
+    aug[::2, 0] = 1
+    mean, std = np.zeros(3, np.float32), np.full(3, 1 / 255, np.float32)  # value ~ byte
+    gpu, _ = check_case(src, mean, std, aug, F32, NHWC)
+    x = np.rint(gpu[..., 0]).astype(int)
+    assert np.array_equal(x[0], np.broadcast_to(W - 1 - np.arange(W), (H, W)))
+    assert np.array_equal(x[1], np.broadcast_to(np.arange(W), (H, W)))
+
+
+def test_misaligned_pointers_take_the_generic_kernel():
+    N, H, W, C = 3, 10, 32, 3
+    src = synth.pixels_uniform(8, N, H, W, C)
+    aug = synth.random_records(8, N, H, W)
+    assert trfn.tr_fused_norm_plan(0x1001, 0x2000, N, H, W, C, F16, NHWC) == GENERIC
+    for dt in (F32, F16):
+        check_case(src, IMNET[0], IMNET[1], aug, dt, NHWC, src_offset=1)
+        check_case(src, IMNET[0], IMNET[1], aug, dt, NHWC, dst_offset=dt * 2 + 2)
+
+
+def test_empty_batch_writes_nothing():
+    src = np.zeros((0, 4, 16, 3), np.uint8)
+    gpu, guards = gpu_run(src, IMNET[0], IMNET[1], None, F32, NHWC, guard=64)
+    assert gpu.size == 0 and np.all(guards == 0xAB)
+
+
+def test_all_presets_full_domain():
+    img = np.repeat(np.arange(256, dtype=np.uint8)[None, None, :, None], 3, axis=3)
+    img = np.repeat(img, 4, axis=1)   # 4 rows x 256 columns, W*C = 768
+    for name in oracle.PRESETS:
+        mean, std, C = oracle.norm_preset(name)
+        src = np.ascontiguousarray(img[..., :C])
+        for dt in (F32, F16):
+            if name == "MLPERF" and dt == F32:
+                # |v| up to 152: the absolute bar becomes 4 binary32 ulps there
+                gpu, _ = gpu_run(src, mean, std, None, dt, NHWC)
+                ref = oracle.fused_norm(src, mean, std, None, out_dtype=dt)
+                ulp = np.spacing(np.abs(ref).astype(np.float32))
+                assert np.all(np.abs(gpu.astype(np.float64) - ref) <= 4 * ulp)
+                continue
+            check_case(src, mean, std, None, dt, NHWC)
+
+
+def test_device_status_is_clear():
+    assert trfn.tr_device_status() == 0
+
+
+def test_launch_counter_counts_kernels():
+    before = trfn.tr_launch_count()
+    cfg, src, aug, mean, std, dt = _config_case(1)
+    gpu_run(src, mean, std, aug, dt, NHWC)
+    assert trfn.tr_launch_count() == before + 1

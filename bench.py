@@ -47,12 +47,13 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4])
     ap.add_argument("--layout", default=None, help="override the config's output layout (nhwc/nchw/nhwc4)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
+    ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -261,10 +262,13 @@ def run_ours(args, rank, local, world, pg):
     alg_bytes = [algorithmic_bytes(cfg, r) for r in recs_all]
 
     stream = torch.cuda.Stream(device=dev)
+    # one scheduling workspace serves every launch of the stream (they run one
+    # after another); --static measures the workspace-free schedule
+    ws = None if args.static else torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
 
     def launch(j):
         trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout, stream=stream,
-                           variant=args.variant)
+                           variant=args.variant, workspace=ws)
 
     # warm the library's per-kernel caches, then capture graphs of launches
     with torch.cuda.stream(stream):
@@ -288,25 +292,24 @@ def run_ours(args, rank, local, world, pg):
 
     def run_steps(steps, exact_tail=None):
         # full graph replays, then the remainder as one tail graph (timed
-        # region) or as eager launches (warm-up)
-        for _ in range(steps // G):
-            g_full.replay()
-        rem = steps % G
-        if rem and exact_tail is not None:
-            exact_tail.replay()
-        elif rem:
-            with torch.cuda.stream(stream):
+        # region) or as eager launches (warm-up); all on `stream`, where the
+        # timing events are recorded (a replay goes to the current stream)
+        with torch.cuda.stream(stream):
+            for _ in range(steps // G):
+                g_full.replay()
+            rem = steps % G
+            if rem and exact_tail is not None:
+                exact_tail.replay()
+            elif rem:
                 for k in range(rem):
                     launch(k % nsets)
 
-    with torch.cuda.stream(stream):
-        run_steps(Wm)
+    run_steps(Wm)
     torch.cuda.synchronize()
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     clocks.start()
     # keep the GPU busy while the sampler starts
-    with torch.cuda.stream(stream):
-        run_steps(min(Wm, 4 * G) if Wm else 0)
+    run_steps(min(Wm, 4 * G) if Wm else 0)
     time.sleep(0.15)
     barrier(pg)
     torch.cuda.synchronize()
@@ -356,6 +359,7 @@ def run_ours(args, rank, local, world, pg):
             "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB >= 4x L2 (%.0f MB)" % (
                 nsets, nsets * set_bytes / 1e6, l2 / 1e6),
             "launch": "CUDA graph of %d launches replayed; variant %d" % (G, args.variant),
+            "schedule": "static (tr_fused_norm)" if args.static else "dynamic bands (tr_fused_norm_ws)",
             "parallelism": "replicas" if world > 1 else "single",
         },
         "hbm_gbs": achieved_gbs,

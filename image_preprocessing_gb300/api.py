@@ -55,12 +55,14 @@ def _dev_ptr(t, what):
 
 
 def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOUT_NHWC, stream=None,
-                  variant=VARIANT_AUTO, shape=None):
+                  variant=VARIANT_AUTO, shape=None, workspace=None):
     """Enqueue the fused step: src uint8 (N,H,W,C) CUDA tensor -> dst.
 
     dst: CUDA tensor of float32/float16 with out_shape(N,H,W,C,layout)
     elements; aug: CUDA int32 tensor (N,5) of {flip,y0,x0,h,w} or None;
-    raw device addresses (ints) are accepted with shape=(N,H,W,C)."""
+    raw device addresses (ints) are accepted with shape=(N,H,W,C).
+    workspace: zeroed CUDA buffer of tr_workspace_bytes() bytes for the
+    dynamic band schedule (tr_fused_norm_ws), or None."""
     dt = _code(out_dtype, _DTYPES)
     lay = _code(layout, _LAYOUTS)
     if shape is not None:
@@ -76,9 +78,14 @@ def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOU
         if aug is not None and (aug.dtype != torch.int32 or aug.numel() != 5 * N):
             raise TrError(1, "tr_fused_norm", "aug must be int32 with N*5 elements")
     m, s = float_array(mean), float_array(std)
-    rc = lib().tr_fused_norm_variant(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
-                                     _dev_ptr(aug, "aug"), dt, lay, _stream_handle(stream), int(variant))
+    rc = lib().tr_fused_norm_ws(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
+                                _dev_ptr(aug, "aug"), dt, lay, _stream_handle(stream), int(variant),
+                                _dev_ptr(workspace, "workspace"))
     check(rc, "tr_fused_norm")
+
+
+def tr_workspace_bytes():
+    return int(lib().tr_workspace_bytes())
 
 
 def tr_fused_norm_plan(src, dst, N, H, W, C, out_dtype, layout):
@@ -127,6 +134,11 @@ def tr_device_status(clear=False):
 
 def tr_launch_count():
     return int(lib().tr_launch_count())
+
+
+def tr_tune_tiled(band_bytes=0, stages=0, max_ctas_per_sm=0, flags=0):
+    """Set the TILED kernel's geometry knobs (0 = default); see the C header."""
+    check(lib().tr_tune_tiled(int(band_bytes), int(stages), int(max_ctas_per_sm), int(flags)), "tr_tune_tiled")
 
 
 def tr_ts_slot_bytes(N, H, W, C):

@@ -42,7 +42,7 @@ int check_shape(int N, int H, int W, int C, int out_dtype, int out_layout) {
 
 int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,
                     const float* stdv, const tr_aug_param* aug, int out_dtype, int out_layout,
-                    void* stream, int variant) {
+                    void* stream, int variant, void* workspace) {
     int rc = check_shape(N, H, W, C, out_dtype, out_layout);
     if (rc != TR_OK) return rc;
     if (variant != TR_VARIANT_AUTO && variant != TR_VARIANT_TILED && variant != TR_VARIANT_GENERIC)
@@ -62,6 +62,11 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     if (N == 0) return TR_OK;
     if (src == nullptr || dst == nullptr) return TR_ERR_INVALID_ARGUMENT;
     const int ob = (out_dtype == TR_OUT_F16) ? 2 : 4;
+    // an output array of binary32/binary16 elements starts on an element
+    // boundary; the records are int32 fields
+    if (((uintptr_t)dst % (uintptr_t)ob) != 0) return TR_ERR_INVALID_ARGUMENT;
+    if (aug != nullptr && ((uintptr_t)aug % 4u) != 0) return TR_ERR_INVALID_ARGUMENT;
+    if (workspace != nullptr && ((uintptr_t)workspace % 16u) != 0) return TR_ERR_INVALID_ARGUMENT;
     const int out_ch = (out_layout == TR_LAYOUT_NHWC4) ? 4 : C;
     const unsigned long long in_bytes = (unsigned long long)N * H * W * C;
     const unsigned long long out_bytes = (unsigned long long)N * H * W * out_ch * ob;
@@ -80,6 +85,7 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     a.out_dtype = out_dtype;
     a.out_layout = out_layout;
     a.stream = stream;
+    a.workspace = workspace;
     rc = launch(a, variant);
     if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {
         // the tiled geometry does not fit this device's shared memory (rows
@@ -99,17 +105,25 @@ extern "C" {
 int tr_fused_norm(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,
                   const float* std, const tr_aug_param* aug_params, int out_dtype, int out_layout,
                   void* stream) {
-    const int rc = fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype,
-                                   out_layout, stream, TR_VARIANT_AUTO);
-    return rc;
+    return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
+                           stream, TR_VARIANT_AUTO, nullptr);
 }
 
 int tr_fused_norm_variant(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
                           const float* mean, const float* std, const tr_aug_param* aug_params,
                           int out_dtype, int out_layout, void* stream, int variant) {
     return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
-                           stream, variant);
+                           stream, variant, nullptr);
 }
+
+int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,
+                     const float* std, const tr_aug_param* aug_params, int out_dtype, int out_layout,
+                     void* stream, int variant, void* workspace) {
+    return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
+                           stream, variant, workspace);
+}
+
+size_t tr_workspace_bytes(void) { return kWorkspaceBytes; }
 
 int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,
                        int out_dtype, int out_layout, int* variant) {
@@ -163,6 +177,13 @@ int tr_device_status(int* flags, int clear) {
 }
 
 uint64_t tr_launch_count(void) { return launch_count(); }
+
+int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags) {
+    if (band_bytes < 0 || stages < 0 || stages > 8 || stages == 1 || max_ctas_per_sm < 0)
+        return TR_ERR_INVALID_ARGUMENT;
+    tune_tiled(band_bytes, stages, max_ctas_per_sm, flags);
+    return TR_OK;
+}
 
 const char* tr_status_string(int status) {
     switch (status) {

@@ -47,6 +47,8 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 384;          // mbarriers + per-stage unit records
+constexpr int kEmptyOffset = 64;           // full[8] at 0, empty[8] at 64
+constexpr int kRecOffset = 128;            // UnitRec[8] at 128
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
 constexpr uint32_t kStatusTimeout = 1u;
 
@@ -73,6 +75,34 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier 1 over `nthreads` threads; returns whether any of them passed
+// a non-zero flag.
+__device__ __forceinline__ bool named_barrier_or(uint32_t nthreads, bool flag) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred q, p;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(any)
+        : "r"((uint32_t)flag), "r"(nthreads)
+        : "memory");
+    return any != 0;
+}
+
+// Programmatic dependent launch: wait for the preceding grid in the stream
+// (complete, memory visible) / let the next grid start its prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -108,10 +138,38 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
         : "memory");
 }
 
+// Same, with an L2 eviction-priority policy.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // TMA bulk copy shared -> global in the current bulk group.
 __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                  "r"(src_smem), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_s2g_hint(void* dst, uint32_t src_smem, uint32_t bytes,
+                                              uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(src_smem), "r"(bytes), "l"(policy)
                  : "memory");
 }
 
@@ -188,6 +246,9 @@ struct TiledParams {
     uint32_t out_stage;    // bytes per output stage
     uint32_t plane_bytes;  // NCHW: bytes per plane of one band in the output stage (R*W*ob)
     int stages;
+    unsigned int* ws;      // scheduling workspace (ticket counters, finished CTAs), or null
+    int hints;             // bit 0: loads evict-first in L2; bit 1: stores evict-first;
+                           // bit 2: stores evict-last; bit 3: early dependent launch
     float scale[4];
     float bias[4];
 };
@@ -199,39 +260,56 @@ struct UnitRec {
     int ecol_lo, ecol_hi;  // erased output columns [lo, hi), clipped
 };
 static_assert(sizeof(UnitRec) == 32, "UnitRec layout");
-static_assert(64 + kMaxStages * sizeof(UnitRec) <= kHeaderBytes, "header holds barriers and records");
+static_assert(kRecOffset + kMaxStages * sizeof(UnitRec) <= kHeaderBytes, "header holds barriers and records");
 
+// Source bytes of unit u: rows [y_begin, y_begin + rows) of image n.
+struct Band {
+    int n, y_begin, rows;
+};
+
+__device__ __forceinline__ Band band_of(const TiledParams& p, int u) {
+    Band b;
+    b.n = u / p.bands;
+    b.y_begin = (u - b.n * p.bands) * p.R;
+    b.rows = min(p.R, p.H - b.y_begin);
+    return b;
+}
+
+__device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, const void* src, uint32_t bytes,
+                                           uint32_t bar) {
+    if (p.hints & 1) bulk_g2s_hint(dst, src, bytes, bar, policy_evict_first());
+    else bulk_g2s(dst, src, bytes, bar);
+}
+
+// Fills stage s with unit u: records the unit for the consumers, arrives on
+// full[s] with the byte count and issues the band's copies, skipping the
+// 16-byte chunks that lie wholly inside the erased source span of the erased
+// rows.
 template <int C>
-__device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem) {
-    const int n = u / p.bands;
-    const int b = u - n * p.bands;
-    const int y_begin = b * p.R;
-    const int rows = min(p.R, p.H - y_begin);
-
+__device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem,
+                                           const tr_aug_param& a) {
+    const Band b = band_of(p, u);
+    const int y_begin = b.y_begin, rows = b.rows;
     int flip = 0, erow_lo = 0, erow_hi = 0, ecol_lo = 0, ecol_hi = 0;
-    if (p.aug != nullptr) {
-        const tr_aug_param a = p.aug[n];
-        flip = (a.flip != 0);
-        if (a.h > 0 && a.w > 0) {
-            const long long y0 = a.y0, x0 = a.x0;
-            const long long ylo = max(y0, 0ll), yhi = min(y0 + a.h, (long long)p.H);
-            const long long xlo = max(x0, 0ll), xhi = min(x0 + a.w, (long long)p.W);
-            if (ylo < yhi && xlo < xhi) {
-                erow_lo = (int)ylo; erow_hi = (int)yhi;
-                ecol_lo = (int)xlo; ecol_hi = (int)xhi;
-            }
+    flip = (a.flip != 0);
+    if (a.h > 0 && a.w > 0) {
+        const long long y0 = a.y0, x0 = a.x0;
+        const long long ylo = max(y0, 0ll), yhi = min(y0 + a.h, (long long)p.H);
+        const long long xlo = max(x0, 0ll), xhi = min(x0 + a.w, (long long)p.W);
+        if (ylo < yhi && xlo < xhi) {
+            erow_lo = (int)ylo; erow_hi = (int)yhi;
+            ecol_lo = (int)xlo; ecol_hi = (int)xhi;
         }
     }
-    UnitRec* rec = reinterpret_cast<UnitRec*>(smem + 64) + s;
-    rec->n = n; rec->y_begin = y_begin; rec->rows = rows; rec->flip = flip;
+    UnitRec* rec = reinterpret_cast<UnitRec*>(smem + kRecOffset) + s;
+    rec->n = b.n; rec->y_begin = y_begin; rec->rows = rows; rec->flip = flip;
     rec->erow_lo = erow_lo; rec->erow_hi = erow_hi; rec->ecol_lo = ecol_lo; rec->ecol_hi = ecol_hi;
 
     const uint32_t L = (uint32_t)p.W * C;
-    const uint8_t* g = p.src + ((size_t)n * p.H + y_begin) * L;
+    const uint8_t* g = p.src + ((size_t)b.n * p.H + y_begin) * L;
     const uint32_t sdst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
-    const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
+    const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;   // full[s]
     const uint32_t total = (uint32_t)rows * L;
-
     // Rows of this band inside the erase rectangle, and the 16-byte aligned
     // part of their erased source span (rows start 16-byte aligned).
     const int r_lo = max(erow_lo - y_begin, 0);
@@ -242,7 +320,7 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     const uint32_t a_hi = ((uint32_t)xs_hi * C) & ~15u;
     if (r_lo >= r_hi || a_hi <= a_lo) {
         mbar_arrive_expect_tx(bar, total);
-        bulk_g2s(sdst, g, total, bar);
+        load_bytes(p, sdst, g, total, bar);
         return;
     }
     const uint32_t skipped = (uint32_t)(r_hi - r_lo) * (a_hi - a_lo);
@@ -250,10 +328,10 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     uint32_t pos = 0;
     for (int r = r_lo; r < r_hi; ++r) {
         const uint32_t seg_end = (uint32_t)r * L + a_lo;
-        if (seg_end > pos) bulk_g2s(sdst + pos, g + pos, seg_end - pos, bar);
+        if (seg_end > pos) load_bytes(p, sdst + pos, g + pos, seg_end - pos, bar);
         pos = (uint32_t)r * L + a_hi;
     }
-    if (total > pos) bulk_g2s(sdst + pos, g + pos, total - pos, bar);
+    if (total > pos) load_bytes(p, sdst + pos, g + pos, total - pos, bar);
 }
 
 template <int C, int OUT_F16, int LAYOUT>
@@ -334,12 +412,12 @@ __device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout,
 
 template <int C, int OUT_F16, int LAYOUT>
 __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
-                                             uint8_t* sout, const UnitRec& rec) {
+                                             uint8_t* sout, const UnitRec& rec, int tid, int nthr) {
     constexpr int P = Group<C>::P;
     constexpr int GB = Group<C>::kBytes;
     const int L = p.W * C;
     const int groups = rec.rows * p.gpr;
-    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+    for (int g = tid; g < groups; g += nthr) {
         const int r = (int)(((uint64_t)(uint32_t)g * p.gpr_inv) >> 32);
         const int gx = g - r * p.gpr;
         const int y = rec.y_begin + r;
@@ -386,73 +464,151 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
                                            const UnitRec& rec) {
     constexpr int OB = OUT_F16 ? 2 : 4;
     const uint32_t src = smem_u32(sout);
+    const uint64_t pol = (p.hints & 2) ? policy_evict_first() : policy_evict_last();
+    auto put = [&](void* g, uint32_t from, uint32_t bytes) {
+        if (p.hints & 6) bulk_s2g_hint(g, from, bytes, pol);
+        else bulk_s2g(g, from, bytes);
+    };
     if (LAYOUT == TR_LAYOUT_NCHW) {
         const uint32_t bytes = (uint32_t)rec.rows * p.W * OB;
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             uint8_t* g = p.dst + ((((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W) * OB;
-            bulk_s2g(g, src + (uint32_t)c * p.plane_bytes, bytes);
+            put(g, src + (uint32_t)c * p.plane_bytes, bytes);
         }
     } else {
         const int ch = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
         const size_t row_bytes = (size_t)p.W * ch * OB;
         uint8_t* g = p.dst + ((size_t)rec.n * p.H + rec.y_begin) * row_bytes;
-        bulk_s2g(g, src, (uint32_t)(rec.rows * row_bytes));
+        put(g, src, (uint32_t)(rec.rows * row_bytes));
     }
     bulk_commit();
 }
 
+// Scheduling workspace: kTicketGroups ticket counters, each on its own
+// 128-byte line, then the count of finished CTAs.  With g = min(kTicketGroups,
+// gridDim.x) groups, CTA b draws from counter b % g, which hands out the
+// dynamic units whose index is congruent to b modulo g.
+constexpr int kTicketGroups = 8;
+constexpr int kTicketStride = 32;   // uint32 words between counters (128 bytes)
+constexpr int kDoneWord = kTicketGroups * kTicketStride;
+
+// Warp 0 is the producer: its lane 0 fills stage s = j % S with the CTA's
+// j-th unit once the consumers have released the stage (empty[s]), counting
+// the bytes on full[s], and ends with an empty fill (rows = 0).  Without a
+// workspace the CTA's units are blockIdx.x + j*gridDim.x; with one, the first
+// S are those and the rest come from ticket counters, so CTAs that run faster
+// take more bands and all finish together.  The last CTA to finish returns
+// the counters to zero.
+// Warps 1.. are consumers: they wait for full[s], convert the band into the
+// output tile i % 2, meet on named barrier 1, and one of them releases the
+// stage and issues the TMA store of the tile.
 template <int C, int OUT_F16, int LAYOUT>
 __global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ TiledParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
-    const uint32_t bar0 = smem_u32(smem);
-    const UnitRec* recs = reinterpret_cast<const UnitRec*>(smem + 64);
+    const uint32_t full0 = smem_u32(smem);
+    const uint32_t empty0 = full0 + kEmptyOffset;
+    const UnitRec* recs = reinterpret_cast<const UnitRec*>(smem + kRecOffset);
     const uint8_t* sin = smem + kHeaderBytes;
     uint8_t* sout = smem + kHeaderBytes + (size_t)S * p.in_stage;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(bar0 + 8u * s, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int j = 0; j < S; ++j) {
-            const int u = blockIdx.x + j * gridDim.x;
-            if (u < p.num_units) issue_unit<C>(p, u, j, smem);
-        }
-    }
+    // everything above overlaps the previous grid in the stream; global
+    // memory is touched only below
+    grid_dependency_wait();
+    if ((p.hints & 8) && threadIdx.x == 0) grid_launch_dependents();
 
-    int i = 0;
-    bool aborted = false;
-    for (;; ++i) {
-        const int u = blockIdx.x + i * gridDim.x;
-        if (u >= p.num_units) break;
-        const int s = i % S;
-        const bool ok = mbar_wait_bounded(bar0 + 8u * s, (uint32_t)(i / S) & 1u);
-        uint8_t* ob = sout + (size_t)(i & 1) * p.out_stage;
-        if (ok) compute_unit<C, OUT_F16, LAYOUT>(p, sin + (size_t)s * p.in_stage, ob, recs[s]);
-        fence_proxy_async_smem();
-        // The store issued last iteration reads the other output buffer, which
-        // the next iteration overwrites: it must be done reading first.
-        if (threadIdx.x == 0) bulk_wait_read<0>();
-        if (__syncthreads_or(!ok)) { aborted = true; break; }
+    if (threadIdx.x < 32) {
         if (threadIdx.x == 0) {
-            store_unit<C, OUT_F16, LAYOUT>(p, ob, recs[s]);
-            const int un = blockIdx.x + (i + S) * gridDim.x;
-            if (un < p.num_units) issue_unit<C>(p, un, s, smem);
-        }
-    }
-    if (threadIdx.x == 0) {
-        if (aborted) {
-            atomicOr(&g_device_status, kStatusTimeout);
-            // drain the loads still in flight (bounded) before leaving
-            for (int j = i; j < i + S; ++j) {
-                const int u = blockIdx.x + j * gridDim.x;
-                if (u >= p.num_units) break;
-                if (!mbar_wait_bounded(bar0 + 8u * (j % S), (uint32_t)(j / S) & 1u)) break;
+            const int G = gridDim.x;
+            const int ngroups = min(kTicketGroups, G);   // every group must have a CTA
+            const int group = (int)blockIdx.x % ngroups;
+            const int n_dyn = max(0, p.num_units - S * G);   // units handed out by tickets
+            int u = blockIdx.x;
+            tr_aug_param a = {0, 0, 0, 0, 0};
+            if (p.aug != nullptr) a = p.aug[u / p.bands];
+            int j = 0;
+            bool ok = true;
+            for (;; ++j) {
+                const int s = j % S;
+                if (j >= S && !mbar_wait_bounded(empty0 + 8u * s, (uint32_t)(j / S - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                if (u >= p.num_units) {
+                    UnitRec* rec = reinterpret_cast<UnitRec*>(smem + kRecOffset) + s;
+                    rec->rows = 0;
+                    mbar_arrive(full0 + 8u * s);
+                    break;
+                }
+                issue_unit<C>(p, u, s, smem, a);
+                // the next unit and its record: requested now, used after the
+                // next empty wait
+                if (p.ws == nullptr || j + 1 < S) {
+                    u = (int)blockIdx.x + (j + 1) * G;
+                } else {
+                    const int t = (int)atomicAdd(p.ws + group * kTicketStride, 1u);
+                    const int k = group + t * ngroups;
+                    u = k < n_dyn ? S * G + k : p.num_units;
+                }
+                if (p.aug != nullptr && u < p.num_units) a = p.aug[u / p.bands];
+            }
+            grid_launch_dependents();
+            if (!ok) {
+                atomicOr(&g_device_status, kStatusTimeout);
+            } else if (p.ws != nullptr) {
+                __threadfence();
+                if (atomicAdd(p.ws + kDoneWord, 1u) == (unsigned)G - 1) {
+                    for (int g = 0; g < kTicketGroups; ++g) p.ws[g * kTicketStride] = 0;
+                    p.ws[kDoneWord] = 0;
+                    __threadfence();
+                }
+            }
+            // The bands in flight must land before this thread leaves
+            // (bounded).  Fill k's phase is the latest of its stage only if no
+            // later fill used the stage: after a normal end the end mark took
+            // stage j % S, so fill j - S is done and superseded.
+            for (int k = max(0, ok ? j - S + 1 : j - S); k < j; ++k) {
+                if (!mbar_wait_bounded(full0 + 8u * (k % S), (uint32_t)(k / S) & 1u)) {
+                    atomicOr(&g_device_status, kStatusTimeout);
+                    break;
+                }
             }
         }
+        return;
+    }
+
+    const int tid = threadIdx.x - 32;
+    const int nthr = blockDim.x - 32;
+    const bool storer = (tid == 0);
+    bool aborted = false;
+    for (int i = 0;; ++i) {
+        const int s = i % S;
+        const bool ok = mbar_wait_bounded(full0 + 8u * s, (uint32_t)(i / S) & 1u);
+        const UnitRec rec = recs[s];
+        uint8_t* ob = sout + (size_t)(i & 1) * p.out_stage;
+        if (ok) compute_unit<C, OUT_F16, LAYOUT>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
+        fence_proxy_async_smem();
+        // The store issued last iteration reads the other output tile, which
+        // the next iteration overwrites: it must be done reading first.
+        if (storer) bulk_wait_read<0>();
+        if (named_barrier_or((uint32_t)nthr, !ok)) { aborted = true; break; }
+        if (rec.rows == 0) break;   // the producer's end mark
+        if (storer) {
+            mbar_arrive(empty0 + 8u * s);
+            store_unit<C, OUT_F16, LAYOUT>(p, ob, rec);
+        }
+    }
+    if (storer) {
+        if (aborted) atomicOr(&g_device_status, kStatusTimeout);
         bulk_wait_all<0>();
     }
 }
@@ -471,6 +627,7 @@ struct GenericParams {
 
 template <int OUT_F16, int LAYOUT>
 __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ GenericParams p) {
+    grid_dependency_wait();
     const long long stride = (long long)gridDim.x * blockDim.x;
     const long long W = p.W, H = p.H, C = p.C;
     for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < p.total; o += stride) {
@@ -579,6 +736,9 @@ struct TiledPlan {
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Geometry knobs (tr_tune_tiled); 0 keeps the default.
+std::atomic<int> g_band_bytes{0}, g_stages{0}, g_ctas_per_sm{0}, g_flags{0};
+
 TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit) {
     TiledPlan pl;
     const int ob = f16 ? 2 : 4;
@@ -587,15 +747,20 @@ TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit) {
     const int gpr = W / P;
     const int out_ch = (layout == TR_LAYOUT_NHWC4) ? 4 : C;
     const size_t out_row = (size_t)W * out_ch * ob;
-    // about 6 KB of source per band; prefer a band height that divides H
-    const size_t target = 6144;
-    int R = (int)std::max<size_t>(1, std::min<size_t>((size_t)H, target / L));
+    // About 32 KB of source plus output per band (band_bytes overrides the
+    // source bytes); prefer a band height that divides H.
+    const int knob = g_band_bytes.load(std::memory_order_relaxed);
+    const size_t row_total = L + out_row;
+    int R = (int)std::max<size_t>(1, std::min<size_t>((size_t)H, knob > 0 ? (size_t)knob / L
+                                                                          : 32768 / row_total));
     for (int r = R; r >= (R + 1) / 2; --r) {
         if (H % r == 0) { R = r; break; }
     }
     while (R > 1 && (size_t)R * gpr >= 65536) --R;
     if ((size_t)R * gpr >= 65536) return pl;
-    int stages = std::min(4, kMaxStages);
+    const int sknob = g_stages.load(std::memory_order_relaxed);
+    const int stages0 = std::min(sknob >= 2 ? sknob : ((size_t)R * L > 8192 ? 3 : 4), kMaxStages);
+    int stages = stages0;
     for (;;) {
         const size_t in_stage = round_up((size_t)R * L, 128);
         const size_t out_stage = round_up((size_t)R * out_row, 128);
@@ -610,13 +775,33 @@ TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit) {
             pl.plane_bytes = (uint32_t)((size_t)R * W * ob);
             pl.smem = smem;
             const int groups = R * gpr;
-            pl.threads = (int)std::min<size_t>(256, std::max<size_t>(64, round_up(groups, 32)));
+            pl.threads = 32 + (int)std::min<size_t>(224, std::max<size_t>(64, round_up(groups, 32)));
             return pl;
         }
         if (stages > 2) { --stages; continue; }
-        if (R > 1) { R = std::max(1, R / 2); stages = 4; continue; }
+        if (R > 1) { R = std::max(1, R / 2); stages = stages0; continue; }
         return pl;
     }
+}
+
+// Launch with programmatic stream serialization: the grid may be scheduled
+// while the preceding kernel in the stream drains; the kernels call
+// griddepcontrol.wait before their first global memory access, so stream
+// order is kept.
+cudaError_t launch_pdl(const void* fn, unsigned grid, int threads, size_t smem, void* stream,
+                       void* params) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* args[1] = {params};
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 bool check_cuda(cudaError_t e, const char* what) {
@@ -651,6 +836,8 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
+    p.hints = g_flags.load(std::memory_order_relaxed) & 15;
+    p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 
     const TiledFn fn = pick_tiled(a.C, f16, a.out_layout);
@@ -691,14 +878,17 @@ int launch_tiled(const LaunchArgs& a) {
             if (ncache < 256) cache[ncache++] = Cached{(const void*)fn, dev, pl.smem, pl.threads, blocks_per_sm};
         }
     }
+    const int cap = g_ctas_per_sm.load(std::memory_order_relaxed);
+    if (cap > 0) blocks_per_sm = std::min(blocks_per_sm, cap);
     const long long max_ctas = (long long)blocks_per_sm * di.sm_count;
     long long grid = std::min<long long>(p.num_units, max_ctas);
     // equalise the number of units per CTA
     const long long waves = (p.num_units + grid - 1) / grid;
     grid = (p.num_units + waves - 1) / waves;
 
-    fn<<<(unsigned)grid, pl.threads, pl.smem, static_cast<cudaStream_t>(a.stream)>>>(p);
-    if (!check_cuda(cudaGetLastError(), "tiled kernel launch")) return TR_ERR_CUDA;
+    if (!check_cuda(launch_pdl((const void*)fn, (unsigned)grid, pl.threads, pl.smem, a.stream, &p),
+                    "tiled kernel launch"))
+        return TR_ERR_CUDA;
     count_launch();
     return TR_OK;
 }
@@ -724,8 +914,10 @@ int launch_generic(const LaunchArgs& a) {
     long long grid = (p.total + threads - 1) / threads;
     grid = std::min<long long>(grid, (long long)di.sm_count * 8);
     if (grid < 1) grid = 1;
-    pick_generic(f16, a.out_layout)<<<(unsigned)grid, threads, 0, static_cast<cudaStream_t>(a.stream)>>>(p);
-    if (!check_cuda(cudaGetLastError(), "generic kernel launch")) return TR_ERR_CUDA;
+    if (!check_cuda(launch_pdl((const void*)pick_generic(f16, a.out_layout), (unsigned)grid, threads, 0,
+                               a.stream, &p),
+                    "generic kernel launch"))
+        return TR_ERR_CUDA;
     count_launch();
     return TR_OK;
 }
@@ -761,6 +953,13 @@ int read_device_status(int* flags, bool clear) {
     }
     if (flags) *flags = (int)v;
     return TR_OK;
+}
+
+void tune_tiled(int band_bytes, int stages, int ctas_per_sm, int flags) {
+    g_flags.store(flags);
+    g_band_bytes.store(band_bytes > 0 ? band_bytes : 0);
+    g_stages.store(stages > 0 ? stages : 0);
+    g_ctas_per_sm.store(ctas_per_sm > 0 ? ctas_per_sm : 0);
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }

@@ -20,7 +20,10 @@ struct LaunchArgs {
     int out_dtype;
     int out_layout;
     void* stream;
+    void* workspace;  // scheduling workspace (tr_workspace_bytes(), zeroed), or null
 };
+
+constexpr size_t kWorkspaceBytes = 2048;
 
 // Whether the tiled kernel's preconditions hold for these arguments.
 bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C,
@@ -36,6 +39,9 @@ int read_device_status(int* flags, bool clear);
 // Per-thread last CUDA error text.
 void set_last_error(const char* what, int cuda_error);
 const char* last_error();
+
+// Tiled-kernel geometry knobs (0 = default).
+void tune_tiled(int band_bytes, int stages, int ctas_per_sm, int flags);
 
 // Count of kernels launched by this library.
 void count_launch();

@@ -97,7 +97,8 @@ typedef enum tr_variant {
  *
  *   src_u8      device, N*H*W*C bytes, compact NHWC uint8.
  *   dst         device, N*H*W*C' elements of out_dtype in out_layout, compact
- *               (C' = 4 for TR_LAYOUT_NHWC4, else C).  There is no stride
+ *               (C' = 4 for TR_LAYOUT_NHWC4, else C), aligned to its element
+ *               size (4 or 2 bytes).  There is no stride
  *               argument: like the article's execute(), the output stride is
  *               fixed by the shape, type and layout.  Must not overlap src.
  *   N,H,W,C     N >= 0 (0 = nothing to do), H >= 1, W >= 1, 1 <= C <= 4.
@@ -105,14 +106,15 @@ typedef enum tr_variant {
  *               finite and non-zero, mean[c] finite.  The kernels use
  *               scale = 1/(255*std) and bias = -mean/std, each formed in
  *               binary64 and rounded to binary32, in one fused multiply-add.
- *   aug_params  device array of N tr_aug_param, read in stream order; NULL
- *               means no flip and no erase for every image.
+ *   aug_params  device array of N tr_aug_param (4-byte aligned), read in
+ *               stream order; NULL means no flip and no erase for every image.
  *   out_dtype   tr_out_dtype; out_layout tr_layout.
  *   stream      cudaStream_t as void*.
  * Errors: TR_ERR_INVALID_ARGUMENT (bad shape, type, layout, null pointer,
- * non-finite or zero std, overlapping src/dst, sizes beyond 2^40 elements),
- * TR_ERR_NOT_SUPPORTED (C > 4), TR_ERR_CUDA (launch failure).  Unaligned
- * pointers are not an error: they take the GENERIC kernel.                  */
+ * dst or aug_params off their element alignment, non-finite or zero std,
+ * overlapping src/dst, sizes beyond 2^40 elements),
+ * TR_ERR_NOT_SUPPORTED (C > 4), TR_ERR_CUDA (launch failure).  Pointers off
+ * a 16-byte boundary are not an error: they take the GENERIC kernel.         */
 int tr_fused_norm(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
                   const float* mean, const float* std, const tr_aug_param* aug_params,
                   int out_dtype, int out_layout, void* stream);
@@ -121,6 +123,25 @@ int tr_fused_norm(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
 int tr_fused_norm_variant(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
                           const float* mean, const float* std, const tr_aug_param* aug_params,
                           int out_dtype, int out_layout, void* stream, int variant);
+
+/* tr_fused_norm with a scheduling workspace.  The TILED kernel then hands
+ * out row bands dynamically (CTAs that run faster take more), so all CTAs
+ * finish together; results are identical to tr_fused_norm's.
+ *   workspace  device buffer of tr_workspace_bytes() bytes, 16-byte aligned,
+ *              all zero before its first use.  Every launch leaves it zero
+ *              again, so launches that run one after another (one stream,
+ *              or a graph's chain) may share it; launches that can run at the
+ *              same time (other streams) need their own.  NULL = the static
+ *              schedule of tr_fused_norm.  After a TR_ERR_DEVICE report the
+ *              workspace must be zeroed again.  The GENERIC kernel ignores it.
+ * Other arguments and errors as tr_fused_norm_variant; a workspace off a
+ * 16-byte boundary is TR_ERR_INVALID_ARGUMENT.                              */
+int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                     const float* mean, const float* std, const tr_aug_param* aug_params,
+                     int out_dtype, int out_layout, void* stream, int variant, void* workspace);
+
+/* Bytes of the scheduling workspace (2048). */
+size_t tr_workspace_bytes(void);
 
 /* Which kernel AUTO would pick for these arguments (TR_VARIANT_TILED or
  * TR_VARIANT_GENERIC), through *variant; host only, launches nothing.        */
@@ -221,6 +242,22 @@ int tr_ts_destroy(tr_transfer_station* ts);
  * runs out (bit 0); with clear != 0 resets it.  Synchronous (waits for the
  * current device).                                                          */
 int tr_device_status(int* flags, int clear);
+
+/* Geometry of the TILED kernel, for tuning on a given device (process-wide;
+ * 0 keeps the default for that knob):
+ *   band_bytes       source bytes per row band (default: about 32 KB of source
+ *                    plus output per band; the band height is the largest
+ *                    divisor of H near the target, else the target),
+ *   stages           shared-memory input stages, 2..8 (default 3 for bands
+ *                    above 8 KB of source, else 4),
+ *   max_ctas_per_sm  cap on resident CTAs per SM (default: occupancy limit),
+ *   flags            L2 policies: bit 0 source loads evict-first, bit 1 output
+ *                    stores evict-first, bit 2 output stores evict-last; bit 3
+ *                    lets the next kernel in the stream launch as soon as this
+ *                    one has started (default: once its loads are issued).
+ * Results do not depend on the geometry.  Errors: TR_ERR_INVALID_ARGUMENT
+ * for negative values or stages of 1 or above 8.                            */
+int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t tr_launch_count(void);

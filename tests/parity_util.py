@@ -11,7 +11,7 @@ F16_ULPS = 1     # binary16 output: at most one unit in the last place
 
 
 def gpu_run(src, mean, std, aug=None, out_dtype=trfn.OUT_F32, layout=trfn.LAYOUT_NHWC,
-            variant=trfn.VARIANT_AUTO, guard=0, src_offset=0, dst_offset=0):
+            variant=trfn.VARIANT_AUTO, guard=0, src_offset=0, dst_offset=0, workspace=None):
     """Runs the CUDA kernel; returns the output as a numpy array (uint16 bits
     for binary16), and the guard bytes around it when guard > 0."""
     N, H, W, C = src.shape
@@ -28,7 +28,8 @@ def gpu_run(src, mean, std, aug=None, out_dtype=trfn.OUT_F32, layout=trfn.LAYOUT
     src_ptr = s_buf.data_ptr() + src_offset
     dst_ptr = d_buf.data_ptr() + guard + dst_offset
     trfn.tr_fused_norm(src_ptr, dst_ptr, mean, std, aug=a.data_ptr() if a is not None else None,
-                       out_dtype=out_dtype, layout=layout, variant=variant, shape=(N, H, W, C))
+                       out_dtype=out_dtype, layout=layout, variant=variant, shape=(N, H, W, C),
+                       workspace=workspace)
     torch.cuda.synchronize()
     host = d_buf.cpu().numpy()
     body = host[guard + dst_offset: guard + dst_offset + nbytes]

@@ -71,6 +71,13 @@ def test_null_and_bad_constants_rejected():
     for bad in ([0.2, 0.0, 0.2], [0.2, float("nan"), 0.2], [0.2, float("inf"), 0.2]):
         assert L.tr_fused_norm(0x1000, 0x100000, 1, 2, 2, 3, M3, _f4(bad), None, 0, 0, None) == INVALID
     assert L.tr_fused_norm(0x1000, 0x100000, 1, 2, 2, 3, _f4([0, float("nan"), 0]), S3, None, 0, 0, None) == INVALID
+    # an output off its element alignment, records off int32 alignment
+    assert L.tr_fused_norm(0x1000, 0x100002, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
+    assert L.tr_fused_norm(0x1000, 0x100001, 1, 2, 2, 3, M3, S3, None, 1, 0, None) == INVALID
+    assert L.tr_fused_norm(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, 0x2002, 0, 0, None) == INVALID
+    # a workspace off a 16-byte boundary
+    assert L.tr_fused_norm_ws(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0, 0x3004) == INVALID
+    assert L.tr_workspace_bytes() == 2048
     # overlapping src and dst
     assert L.tr_fused_norm(0x1000, 0x1004, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
     # a bad kernel choice

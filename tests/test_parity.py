@@ -130,7 +130,8 @@ def test_misaligned_pointers_take_the_generic_kernel():
     assert trfn.tr_fused_norm_plan(0x1001, 0x2000, N, H, W, C, F16, NHWC) == GENERIC
     for dt in (F32, F16):
         check_case(src, IMNET[0], IMNET[1], aug, dt, NHWC, src_offset=1)
-        check_case(src, IMNET[0], IMNET[1], aug, dt, NHWC, dst_offset=dt * 2 + 2)
+        # element-aligned but not 16-byte aligned output
+        check_case(src, IMNET[0], IMNET[1], aug, dt, NHWC, dst_offset=2 if dt == F16 else 4)
 
 
 def test_empty_batch_writes_nothing():
@@ -147,11 +148,12 @@ def test_all_presets_full_domain():
         src = np.ascontiguousarray(img[..., :C])
         for dt in (F32, F16):
             if name == "MLPERF" and dt == F32:
-                # |v| up to 152: the absolute bar becomes 4 binary32 ulps there
+                # terms of the map reach 255 (x*scale) and 124 (bias): the
+                # absolute bar becomes 4 binary32 ulps at that magnitude
                 gpu, _ = gpu_run(src, mean, std, None, dt, NHWC)
                 ref = oracle.fused_norm(src, mean, std, None, out_dtype=dt)
-                ulp = np.spacing(np.abs(ref).astype(np.float32))
-                assert np.all(np.abs(gpu.astype(np.float64) - ref) <= 4 * ulp)
+                tol = 4 * float(np.spacing(np.float32(255.0)))
+                assert np.max(np.abs(gpu.astype(np.float64) - ref)) <= tol
                 continue
             check_case(src, mean, std, None, dt, NHWC)
 
@@ -165,3 +167,80 @@ def test_launch_counter_counts_kernels():
     cfg, src, aug, mean, std, dt = _config_case(1)
     gpu_run(src, mean, std, aug, dt, NHWC)
     assert trfn.tr_launch_count() == before + 1
+
+
+def _workspace():
+    import torch
+    return torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("k", [1, 3, 4])
+def test_dynamic_schedule_matches_static(k):
+    """tr_fused_norm_ws hands out bands dynamically; the output is the same
+    bit for bit and the workspace is zero again afterwards."""
+    cfg, src, aug, mean, std, dt = _config_case(k)
+    ws = _workspace()
+    for lay in cfg["layouts"]:
+        layout = NCHW if lay == "nchw" else NHWC
+        a, _ = gpu_run(src, mean, std, aug, dt, layout)
+        b, _ = gpu_run(src, mean, std, aug, dt, layout, workspace=ws.data_ptr())
+        assert np.array_equal(a, b)
+        assert int(ws.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("shape", SHAPES_TILED)
+def test_dynamic_schedule_on_small_shapes(shape):
+    N, H, W, C = shape
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(3 + N, N, H, W, allow_outside=True)
+    ws = _workspace()
+    for layout in (NHWC, NCHW, NHWC4):
+        check_case(src, mean, std, aug, F16, layout, workspace=ws.data_ptr())
+        assert int(ws.count_nonzero()) == 0
+
+
+def test_workspace_shared_by_back_to_back_launches():
+    import torch
+    N, H, W, C = 64, 224, 224, 3
+    ws = _workspace()
+    mean, std = IMNET
+    srcs = [synth.pixels_uniform(40 + i, N, H, W, C) for i in range(3)]
+    augs = [oracle.sample_aug_params(50 + i, 0, N, H, W)[0] for i in range(3)]
+    d_src = [torch.from_numpy(x).cuda() for x in srcs]
+    d_aug = [torch.from_numpy(a).cuda() for a in augs]
+    outs = [torch.empty((N, H, W, C), dtype=torch.float16, device="cuda") for _ in range(3)]
+    for rep in range(4):
+        for i in range(3):
+            trfn.tr_fused_norm(d_src[i], outs[i], mean, std, d_aug[i], out_dtype=F16, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    for i in range(3):
+        ref = oracle.fused_norm(srcs[i], mean, std, augs[i], out_dtype=F16)
+        assert_parity(outs[i].cpu().view(torch.int16).numpy().view(np.uint16), ref, F16)
+
+
+def test_launches_complete_quickly_and_leave_no_status():
+    """A full 256-image batch takes tens of microseconds; a launch that takes
+    anywhere near the kernels' one-second wait bound means a wait expired."""
+    import time
+    import torch
+    N, H, W, C = 256, 224, 224, 3
+    src = torch.randint(0, 256, (N, H, W, C), dtype=torch.uint8, device="cuda")
+    aug = torch.from_numpy(oracle.sample_aug_params(9, 0, N, H, W)[0]).cuda()
+    dst = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    ws = _workspace()
+    stream = torch.cuda.Stream()
+    mean, std = IMNET
+    for w in (None, ws):
+        with torch.cuda.stream(stream):
+            trfn.tr_fused_norm(src, dst, mean, std, aug, out_dtype=F16, stream=stream, workspace=w)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                trfn.tr_fused_norm(src, dst, mean, std, aug, out_dtype=F16, stream=stream, workspace=w)
+        torch.cuda.synchronize()
+        assert (time.perf_counter() - t0) / 20 < 0.05
+    assert trfn.tr_device_status() == 0

@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4])
     ap.add_argument("--layout", default=None, help="override the config's output layout (nhwc/nchw/nhwc4)")
+    ap.add_argument("--batch", type=int, default=None, help="override the config's batch size N")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
     ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
     ap.add_argument("--e2e-steps", type=int, default=64)
@@ -194,6 +195,9 @@ def workload(args):
     name = cfg["name"]
     if args.layout:
         name += "_" + layout
+    if args.batch:
+        name = name.replace("n%d_" % cfg["N"], "n%d_" % args.batch, 1)
+        cfg["N"] = args.batch
     cfg["workload"] = name
     return cfg
 

@@ -143,6 +143,29 @@ int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
 /* Bytes of the scheduling workspace (2048). */
 size_t tr_workspace_bytes(void);
 
+/* tr_fused_norm_noalloc — tr_fused_norm_ws for callers that cannot allocate
+ * device memory.  No counterpart in the FusedNormalization article: it exists
+ * for programs whose device memory is fixed by a memory plan made at start-up,
+ * loader threads that must not wait on the device-wide synchronisation of
+ * cudaFree, and plug-ins without access to their host's allocator.  Instead
+ * of a caller's workspace it uses a 2048-byte scratch array in this
+ * library's module memory (a file-scope __device__ array that every GPU which
+ * loads the library holds until the process exits), and it allocates nothing.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - Each call clears the scratch on `stream` (an asynchronous memset) before
+ *     its kernel, and the kernel leaves it zero again.  All calls on a device
+ *     share the one array: calls that overlap on the GPU (other streams or
+ *     threads) race on it and must be ordered by the caller.
+ *   - Scratch needs above the 2048-byte capacity are rejected with
+ *     TR_ERR_NOT_SUPPORTED (tr_last_error_message() says so); every shape the
+ *     kernels accept currently needs exactly tr_workspace_bytes().
+ * Other arguments, results and errors as tr_fused_norm.                      */
+int tr_fused_norm_noalloc(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                          const float* mean, const float* std, const tr_aug_param* aug_params,
+                          int out_dtype, int out_layout, void* stream);
+
 /* Which kernel AUTO would pick for these arguments (TR_VARIANT_TILED or
  * TR_VARIANT_GENERIC), through *variant; host only, launches nothing.        */
 int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,

@@ -1,0 +1,108 @@
+"""The transfer station (double-buffered feeding from pinned host memory):
+every batch's output equals the direct kernel's, slots are reused only after
+the kernel that read them, results come back to pinned host buffers, and
+tr_ts_sync gives up at its deadline without losing the queued work.
+
+The A/B hand-over follows the TransferStation of the Tech-Renaissance article
+"(10) Multi-threaded preprocessing, NUMA awareness, asynchronous double
+buffering" (tech-renaissance.cn/blog/?p=481, §四)."""
+import numpy as np
+import pytest
+
+import oracle
+import image_preprocessing_gb300 as trfn
+from image_preprocessing_gb300 import synth
+from parity_util import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+MEAN = np.array(synth.IMAGENET_MEAN, np.float32)
+STD = np.array(synth.IMAGENET_STD, np.float32)
+
+
+def _station(N, H, W, C, with_d2h=True):
+    import torch
+    nbytes = trfn.tr_ts_slot_bytes(N, H, W, C)
+    slots = [torch.empty(nbytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    ts = trfn.TransferStation(torch.cuda.current_device(), slots, streams[0], streams[1],
+                              streams[2] if with_d2h else None)
+    return ts, streams
+
+
+@pytest.mark.parametrize("dt", [trfn.OUT_F16, trfn.OUT_F32])
+def test_every_batch_matches_the_oracle(dt):
+    import torch
+    N, H, W, C = 8, 32, 48, 3
+    K = 7
+    ts, _ = _station(N, H, W, C)
+    tdt = torch.float16 if dt == trfn.OUT_F16 else torch.float32
+    srcs = [synth.pixels_gaussian(300 + k, N, H, W, C) for k in range(K)]
+    recs = [oracle.sample_aug_params(400 + k, 0, N, H, W)[0] for k in range(K)]
+    h_src = [torch.from_numpy(x).pin_memory() for x in srcs]
+    h_par = [torch.from_numpy(r).pin_memory() for r in recs]
+    d_out = [torch.empty((N, H, W, C), dtype=tdt, device="cuda") for _ in range(K)]
+    h_out = [torch.zeros((N, H, W, C), dtype=tdt).pin_memory() for _ in range(K)]
+    for k in range(K):
+        assert ts.submit(h_src[k], d_out[k], MEAN, STD, h_params=h_par[k], h_dst=h_out[k], out_dtype=dt) == k
+    assert ts.sync(30000)
+    for k in range(K):
+        ref = oracle.fused_norm(srcs[k], MEAN, STD, recs[k], out_dtype=dt)
+        for got in (d_out[k].cpu(), h_out[k]):
+            arr = got.view(torch.int16).numpy().view(np.uint16) if dt == trfn.OUT_F16 else got.numpy()
+            assert_parity(arr, ref, dt, "batch %d" % k)
+    ts.close()
+
+
+def test_two_device_outputs_reused_across_batches():
+    """d_dst alternating between two buffers while results are copied back:
+    batch k's kernel waits for batch k-2's copy to the host."""
+    import torch
+    N, H, W, C = 4, 16, 32, 3
+    K = 9
+    ts, _ = _station(N, H, W, C)
+    srcs = [synth.pixels_uniform(500 + k, N, H, W, C) for k in range(K)]
+    h_src = [torch.from_numpy(x).pin_memory() for x in srcs]
+    d_out = [torch.empty((N, H, W, C), dtype=torch.float16, device="cuda") for _ in range(2)]
+    h_out = [torch.zeros((N, H, W, C), dtype=torch.float16).pin_memory() for _ in range(K)]
+    for k in range(K):
+        ts.submit(h_src[k], d_out[k % 2], MEAN, STD, h_dst=h_out[k])
+    assert ts.sync(30000)
+    for k in range(K):
+        ref = oracle.fused_norm(srcs[k], MEAN, STD, None, out_dtype=trfn.OUT_F16)
+        assert_parity(h_out[k].view(torch.int16).numpy().view(np.uint16), ref, trfn.OUT_F16, "batch %d" % k)
+    ts.close()
+
+
+def test_sync_times_out_then_completes():
+    """A copy stream held busy by a bounded sleep kernel: a short sync gives up
+    with a timeout, a later unbounded sync sees the batch complete."""
+    import torch
+    N, H, W, C = 2, 8, 16, 3
+    ts, (s_copy, s_comp, s_d2h) = _station(N, H, W, C)
+    src = synth.pixels_uniform(7, N, H, W, C)
+    h_src = torch.from_numpy(src).pin_memory()
+    d_out = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    with torch.cuda.stream(s_copy):
+        torch.cuda._sleep(400_000_000)   # a few hundred milliseconds of spinning, bounded
+    ts.submit(h_src, d_out, MEAN, STD)
+    assert ts.sync(5) is False
+    assert ts.sync(-1) is True
+    ref = oracle.fused_norm(src, MEAN, STD, None, out_dtype=trfn.OUT_F16)
+    assert_parity(d_out.cpu().view(torch.int16).numpy().view(np.uint16), ref, trfn.OUT_F16)
+    ts.close()
+
+
+def test_submit_rejects_bad_arguments():
+    import torch
+    N, H, W, C = 2, 8, 16, 3
+    ts, _ = _station(N, H, W, C, with_d2h=False)
+    h_src = torch.zeros((N, H, W, C), dtype=torch.uint8).pin_memory()
+    d_out = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    h_out = torch.zeros((N, H, W, C), dtype=torch.float16).pin_memory()
+    with pytest.raises(trfn.TrError):
+        ts.submit(h_src, d_out, MEAN, STD, h_dst=h_out)   # no result stream was given
+    big = torch.zeros((N + 5, H, W, C), dtype=torch.uint8).pin_memory()
+    with pytest.raises(trfn.TrError):
+        ts.submit(big, d_out, MEAN, STD)                   # does not fit a slot
+    ts.close()

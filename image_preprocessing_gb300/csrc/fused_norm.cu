@@ -247,8 +247,9 @@ struct TiledParams {
     uint32_t plane_bytes;  // NCHW: bytes per plane of one band in the output stage (R*W*ob)
     int stages;
     unsigned int* ws;      // scheduling workspace (ticket counters, finished CTAs), or null
-    int hints;             // bit 0: loads evict-first in L2; bit 1: stores evict-first;
-                           // bit 2: stores evict-last; bit 3: early dependent launch
+    int hints;             // tr_tune_tiled flags: bit 0 normal-priority loads, bit 1
+                           // normal-priority stores, bit 2 evict-last stores (default:
+                           // both evict-first); bit 3 early dependent launch
     float scale[4];
     float bias[4];
 };
@@ -275,10 +276,12 @@ __device__ __forceinline__ Band band_of(const TiledParams& p, int u) {
     return b;
 }
 
+// Source bytes are read exactly once: by default they enter L2 with
+// evict-first priority.
 __device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, const void* src, uint32_t bytes,
                                            uint32_t bar) {
-    if (p.hints & 1) bulk_g2s_hint(dst, src, bytes, bar, policy_evict_first());
-    else bulk_g2s(dst, src, bytes, bar);
+    if (p.hints & 1) bulk_g2s(dst, src, bytes, bar);
+    else bulk_g2s_hint(dst, src, bytes, bar, policy_evict_first());
 }
 
 // Fills stage s with unit u: records the unit for the consumers, arrives on
@@ -464,10 +467,14 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
                                            const UnitRec& rec) {
     constexpr int OB = OUT_F16 ? 2 : 4;
     const uint32_t src = smem_u32(sout);
-    const uint64_t pol = (p.hints & 2) ? policy_evict_first() : policy_evict_last();
+    // Output lines go to L2 evict-first by default (a streamed result); a
+    // caller whose next kernel reads the output from L2 can ask for normal
+    // or evict-last priority.
+    const bool plain = (p.hints & 6) == 2;
+    const uint64_t pol = (p.hints & 4) ? policy_evict_last() : policy_evict_first();
     auto put = [&](void* g, uint32_t from, uint32_t bytes) {
-        if (p.hints & 6) bulk_s2g_hint(g, from, bytes, pol);
-        else bulk_s2g(g, from, bytes);
+        if (plain) bulk_s2g(g, from, bytes);
+        else bulk_s2g_hint(g, from, bytes, pol);
     };
     if (LAYOUT == TR_LAYOUT_NCHW) {
         const uint32_t bytes = (uint32_t)rec.rows * p.W * OB;

@@ -274,10 +274,12 @@ int tr_device_status(int* flags, int clear);
  *   stages           shared-memory input stages, 2..8 (default 3 for bands
  *                    above 8 KB of source, else 4),
  *   max_ctas_per_sm  cap on resident CTAs per SM (default: occupancy limit),
- *   flags            L2 policies: bit 0 source loads evict-first, bit 1 output
- *                    stores evict-first, bit 2 output stores evict-last; bit 3
- *                    lets the next kernel in the stream launch as soon as this
- *                    one has started (default: once its loads are issued).
+ *   flags            L2 policies (default: source loads and output stores
+ *                    both evict-first): bit 0 normal-priority loads, bit 1
+ *                    normal-priority stores, bit 2 evict-last stores (for a
+ *                    consumer that reads the output from L2); bit 3 lets the
+ *                    next kernel in the stream launch as soon as this one has
+ *                    started (default: once its loads are issued).
  * Results do not depend on the geometry.  Errors: TR_ERR_INVALID_ARGUMENT
  * for negative values or stages of 1 or above 8.                            */
 int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags);

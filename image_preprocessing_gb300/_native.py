@@ -56,6 +56,8 @@ _SIGNATURES = {
     "tr_ts_create": (_i, [_i, ctypes.POINTER(_vp), ctypes.c_size_t, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
     "tr_ts_submit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _fp, _fp, _i, _i,
                           ctypes.POINTER(ctypes.c_longlong)]),
+    "tr_ts_submit_partial": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _fp, _fp, _i, _i,
+                                  ctypes.POINTER(ctypes.c_longlong)]),
     "tr_ts_sync": (_i, [_vp, _i]),
     "tr_ts_destroy": (_i, [_vp]),
     "tr_device_status": (_i, [ctypes.POINTER(_i), _i]),

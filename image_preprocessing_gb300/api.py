@@ -173,6 +173,20 @@ class TransferStation:
                                  _code(layout, _LAYOUTS), ctypes.byref(k)), "tr_ts_submit")
         return k.value
 
+    def submit_partial(self, h_src, n_batch, d_dst, mean, std, h_params=None, h_dst=None, out_dtype=OUT_F16,
+                       layout=LAYOUT_NHWC):
+        """A short batch: h_src holds n_valid < n_batch images; the rest of the
+        batch repeats the station's filler (first image of its first batch)."""
+        n_valid, H, W, C = h_src.shape
+        k = ctypes.c_longlong(-1)
+        check(lib().tr_ts_submit_partial(self._h, h_src.data_ptr(),
+                                         None if h_params is None else h_params.data_ptr(), n_valid,
+                                         d_dst.data_ptr(), None if h_dst is None else h_dst.data_ptr(),
+                                         n_batch, H, W, C, float_array(mean), float_array(std),
+                                         _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS), ctypes.byref(k)),
+              "tr_ts_submit_partial")
+        return k.value
+
     def sync(self, timeout_ms=-1):
         """True when all submitted work has finished; False on timeout."""
         rc = lib().tr_ts_sync(self._h, int(timeout_ms))

@@ -18,8 +18,10 @@
 //
 // so the copy of batch k+1 overlaps the kernel of batch k.  The host never
 // blocks except in tr_ts_sync(), which polls the events against a deadline.
-// Slot layout: [images][pad to 256][records], after the article's
-// [labels][padding][image] zones aligned to 256 bytes (§四).
+// Slot layout: [images][records][filler image][filler record], each zone on a
+// 256-byte boundary, after the article's [labels][padding][image] zones (§四).
+// A short batch is padded to full size with the filler, the first image of the
+// first batch (the article's incomplete-batch filling, §四.1).
 
 #include <cuda_runtime.h>
 
@@ -40,6 +42,7 @@ struct tr_transfer_station {
     cudaEvent_t d2h_done[2] = {nullptr, nullptr};
     bool done_used[2] = {false, false};
     bool d2h_used[2] = {false, false};
+    bool filler_saved = false;   // the first batch's first image and record are in both slots
     long long next_batch = 0;
     std::mutex mu;
 };
@@ -47,6 +50,24 @@ struct tr_transfer_station {
 namespace {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Slot layout: [N images][pad][N records][pad][filler image][pad][filler record].
+// The filler is the first image (and record) of the first batch, kept for
+// padding short batches (the article's incomplete-batch filling, §四.1).
+struct SlotLayout {
+    size_t img, images, records, filler, filler_rec, total;
+};
+
+SlotLayout slot_layout(int N, int H, int W, int C) {
+    SlotLayout l;
+    l.img = (size_t)H * W * C;
+    l.images = 0;
+    l.records = align256((size_t)N * l.img);
+    l.filler = l.records + align256((size_t)N * sizeof(tr_aug_param));
+    l.filler_rec = l.filler + align256(l.img);
+    l.total = l.filler_rec + align256(sizeof(tr_aug_param));
+    return l;
+}
 
 bool ok(cudaError_t e, const char* what) {
     if (e == cudaSuccess) return true;
@@ -114,7 +135,7 @@ extern "C" {
 
 size_t tr_ts_slot_bytes(int N, int H, int W, int C) {
     if (N < 0 || H < 1 || W < 1 || C < 1) return 0;
-    return align256((size_t)N * H * W * C) + (size_t)N * sizeof(tr_aug_param);
+    return slot_layout(N, H, W, C).total;
 }
 
 int tr_ts_create(int device, void* const d_slot[2], size_t slot_bytes, void* copy_stream,
@@ -146,20 +167,27 @@ int tr_ts_create(int device, void* const d_slot[2], size_t slot_bytes, void* cop
     return TR_OK;
 }
 
-int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params,
-                 void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean,
-                 const float* std, int out_dtype, int out_layout, long long* batch_index) {
-    if (ts == nullptr || h_src == nullptr || d_dst == nullptr || N < 1 || H < 1 || W < 1 || C < 1 ||
-        C > 4 || mean == nullptr || std == nullptr)
-        return TR_ERR_INVALID_ARGUMENT;
-    if (out_dtype != TR_OUT_F32 && out_dtype != TR_OUT_F16) return TR_ERR_INVALID_ARGUMENT;
-    if (out_layout != TR_LAYOUT_NHWC && out_layout != TR_LAYOUT_NCHW && out_layout != TR_LAYOUT_NHWC4)
+}  // extern "C"
+
+namespace {
+
+// Batch k of N images, of which the first n_valid come from the host and the
+// rest repeat the filler; see tr_ts_submit and tr_ts_submit_partial.
+int submit_impl(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params, int n_valid,
+                void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean, const float* std,
+                int out_dtype, int out_layout, long long* batch_index) {
+    if (ts == nullptr || h_src == nullptr || d_dst == nullptr || N < 1 || n_valid < 1 || n_valid > N)
         return TR_ERR_INVALID_ARGUMENT;
     if (h_dst != nullptr && ts->d2h == nullptr) return TR_ERR_INVALID_ARGUMENT;
-    const size_t in_bytes = (size_t)N * H * W * C;
-    const size_t rec_off = align256(in_bytes);
-    const size_t need = rec_off + (h_params ? (size_t)N * sizeof(tr_aug_param) : 0);
-    if (need > ts->slot_bytes) return TR_ERR_INVALID_ARGUMENT;
+    // the kernel's own argument checks (shape, type, layout, mean/std), with
+    // nothing launched, before any copy is queued
+    int rc = tr_fused_norm(nullptr, nullptr, 0, H, W, C, mean, std, nullptr, out_dtype, out_layout, nullptr);
+    if (rc != TR_OK) return rc;
+    const SlotLayout l = slot_layout(N, H, W, C);
+    const bool room_for_filler = l.total <= ts->slot_bytes;
+    if (l.filler > ts->slot_bytes && (h_params != nullptr || n_valid < N)) return TR_ERR_INVALID_ARGUMENT;
+    if (l.records > ts->slot_bytes) return TR_ERR_INVALID_ARGUMENT;
+    if (n_valid < N && !room_for_filler) return TR_ERR_INVALID_ARGUMENT;
     const size_t out_bytes = (size_t)N * H * W * (out_layout == TR_LAYOUT_NHWC4 ? 4 : C) *
                              (out_dtype == TR_OUT_F16 ? 2 : 4);
 
@@ -169,24 +197,50 @@ int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_par
     const int s = (int)(k & 1);
     uint8_t* slot = ts->slot[s];
     const tr_aug_param* d_params =
-        h_params ? reinterpret_cast<const tr_aug_param*>(slot + rec_off) : nullptr;
+        h_params ? reinterpret_cast<const tr_aug_param*>(slot + l.records) : nullptr;
+    const size_t rec = sizeof(tr_aug_param);
 
     if (ts->done_used[s] && !ok(cudaStreamWaitEvent(ts->copy, ts->done[s], 0), "cudaStreamWaitEvent"))
         return TR_ERR_CUDA;
-    if (!ok(cudaMemcpyAsync(slot, h_src, in_bytes, cudaMemcpyHostToDevice, ts->copy), "cudaMemcpyAsync"))
+    if (!ok(cudaMemcpyAsync(slot, h_src, (size_t)n_valid * l.img, cudaMemcpyHostToDevice, ts->copy),
+            "cudaMemcpyAsync"))
         return TR_ERR_CUDA;
-    if (h_params && !ok(cudaMemcpyAsync(slot + rec_off, h_params, (size_t)N * sizeof(tr_aug_param),
+    if (h_params && !ok(cudaMemcpyAsync(slot + l.records, h_params, (size_t)n_valid * rec,
                                         cudaMemcpyHostToDevice, ts->copy),
                         "cudaMemcpyAsync"))
         return TR_ERR_CUDA;
+    if (!ts->filler_saved && room_for_filler) {
+        // the first batch's first image and record become the filler, in
+        // both slots (the other slot is not in use before batch 1)
+        for (int t = 0; t < 2; ++t) {
+            if (!ok(cudaMemcpyAsync(ts->slot[t] + l.filler, slot, l.img, cudaMemcpyDeviceToDevice, ts->copy),
+                    "cudaMemcpyAsync"))
+                return TR_ERR_CUDA;
+            const cudaError_t e =
+                h_params ? cudaMemcpyAsync(ts->slot[t] + l.filler_rec, slot + l.records, rec,
+                                           cudaMemcpyDeviceToDevice, ts->copy)
+                         : cudaMemsetAsync(ts->slot[t] + l.filler_rec, 0, rec, ts->copy);
+            if (!ok(e, "filler record")) return TR_ERR_CUDA;
+        }
+        ts->filler_saved = true;
+    }
+    for (int i = n_valid; i < N; ++i) {
+        if (!ok(cudaMemcpyAsync(slot + (size_t)i * l.img, slot + l.filler, l.img, cudaMemcpyDeviceToDevice,
+                                ts->copy),
+                "cudaMemcpyAsync"))
+            return TR_ERR_CUDA;
+        if (h_params && !ok(cudaMemcpyAsync(slot + l.records + (size_t)i * rec, slot + l.filler_rec, rec,
+                                            cudaMemcpyDeviceToDevice, ts->copy),
+                            "cudaMemcpyAsync"))
+            return TR_ERR_CUDA;
+    }
     if (!ok(cudaEventRecord(ts->copied[s], ts->copy), "cudaEventRecord")) return TR_ERR_CUDA;
 
     if (!ok(cudaStreamWaitEvent(ts->compute, ts->copied[s], 0), "cudaStreamWaitEvent")) return TR_ERR_CUDA;
     if (ts->d2h_used[s] &&
         !ok(cudaStreamWaitEvent(ts->compute, ts->d2h_done[s], 0), "cudaStreamWaitEvent"))
         return TR_ERR_CUDA;
-    const int rc = tr_fused_norm(slot, d_dst, N, H, W, C, mean, std, d_params, out_dtype, out_layout,
-                                 ts->compute);
+    rc = tr_fused_norm(slot, d_dst, N, H, W, C, mean, std, d_params, out_dtype, out_layout, ts->compute);
     if (rc != TR_OK) return rc;
     if (!ok(cudaEventRecord(ts->done[s], ts->compute), "cudaEventRecord")) return TR_ERR_CUDA;
     ts->done_used[s] = true;
@@ -202,6 +256,25 @@ int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_par
     ts->next_batch = k + 1;
     if (batch_index) *batch_index = k;
     return TR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params,
+                 void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean,
+                 const float* std, int out_dtype, int out_layout, long long* batch_index) {
+    return submit_impl(ts, h_src, h_params, N, d_dst, h_dst, N, H, W, C, mean, std, out_dtype, out_layout,
+                       batch_index);
+}
+
+int tr_ts_submit_partial(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params,
+                         int n_valid, void* d_dst, void* h_dst, int N, int H, int W, int C,
+                         const float* mean, const float* std, int out_dtype, int out_layout,
+                         long long* batch_index) {
+    return submit_impl(ts, h_src, h_params, n_valid, d_dst, h_dst, N, H, W, C, mean, std, out_dtype,
+                       out_layout, batch_index);
 }
 
 int tr_ts_sync(tr_transfer_station* ts, int timeout_ms) {

@@ -220,8 +220,9 @@ int tr_validate_aug_params(const tr_aug_param* host_params, int N, int H, int W,
  */
 typedef struct tr_transfer_station tr_transfer_station;
 
-/* Bytes one device slot needs for a batch: the image bytes rounded up to 256,
- * then N records (the slot layout [images][pad to 256][records]).           */
+/* Bytes one device slot needs for a batch of N images: the slot layout is
+ * [N images][N records][filler image][filler record], each zone starting on a
+ * 256-byte boundary (the article's [labels][padding][image] zones, §四).     */
 size_t tr_ts_slot_bytes(int N, int H, int W, int C);
 
 /*   device        CUDA device ordinal the slots and streams belong to.
@@ -249,6 +250,21 @@ int tr_ts_submit(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_par
                  void* d_dst, void* h_dst, int N, int H, int W, int C,
                  const float* mean, const float* std, int out_dtype, int out_layout,
                  long long* batch_index);
+
+/* tr_ts_submit for a short batch: h_src holds n_valid images (1 <= n_valid
+ * <= N) and h_params, when not NULL, n_valid records; images n_valid..N-1 of
+ * the batch repeat the filler, so that every batch has N images (the
+ * article's incomplete-batch filling, TransferStation §四.1: the engine sees
+ * one batch size and one captured graph).  The filler is the first image and
+ * record of the first batch this station received (its record is "no flip,
+ * no erase" if that batch had none); both are kept in the slots' filler zones
+ * and copied into place on the copy stream.  Errors as tr_ts_submit, and
+ * TR_ERR_INVALID_ARGUMENT for n_valid outside 1..N or slots without room for
+ * the filler zones (tr_ts_slot_bytes).                                       */
+int tr_ts_submit_partial(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params,
+                         int n_valid, void* d_dst, void* h_dst, int N, int H, int W, int C,
+                         const float* mean, const float* std, int out_dtype, int out_layout,
+                         long long* batch_index);
 
 /* Wait until everything submitted so far has finished, polling events; gives
  * up after timeout_ms milliseconds with TR_ERR_TIMEOUT (the work stays

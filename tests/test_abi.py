@@ -171,9 +171,10 @@ def test_validate_aug_params():
 
 
 def test_slot_bytes_layout():
-    # images rounded up to 256 bytes, then the 20-byte records
-    assert trfn.tr_ts_slot_bytes(256, 224, 224, 3) == 256 * 224 * 224 * 3 + 256 * 20
-    assert trfn.tr_ts_slot_bytes(3, 5, 7, 3) == 512 + 60
+    # [images][records][filler image][filler record], each zone on a 256-byte boundary
+    img = 224 * 224 * 3
+    assert trfn.tr_ts_slot_bytes(256, 224, 224, 3) == 256 * img + 5120 + img + 256
+    assert trfn.tr_ts_slot_bytes(3, 5, 7, 3) == 512 + 256 + 256 + 256
     assert trfn.tr_ts_slot_bytes(-1, 5, 7, 3) == 0
 
 

@@ -106,3 +106,48 @@ def test_submit_rejects_bad_arguments():
     with pytest.raises(trfn.TrError):
         ts.submit(big, d_out, MEAN, STD)                   # does not fit a slot
     ts.close()
+
+
+def _f16(t):
+    import torch
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_short_batch_is_padded_with_the_first_batchs_first_image():
+    """TransferStation §四.1: a short last batch is filled up with the first
+    sample of the first batch, so every batch keeps one size."""
+    import torch
+    N, H, W, C = 6, 16, 32, 3
+    ts, _ = _station(N, H, W, C)
+    full = synth.pixels_uniform(61, N, H, W, C)
+    short = synth.pixels_uniform(62, 2, H, W, C)
+    r_full = oracle.sample_aug_params(63, 0, N, H, W)[0]
+    r_short = oracle.sample_aug_params(64, 0, 2, H, W)[0]
+    d0 = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    d1 = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    ts.submit(torch.from_numpy(full).pin_memory(), d0, MEAN, STD, h_params=torch.from_numpy(r_full).pin_memory())
+    ts.submit_partial(torch.from_numpy(short).pin_memory(), N, d1, MEAN, STD,
+                      h_params=torch.from_numpy(r_short).pin_memory())
+    assert ts.sync(30000)
+    want_src = np.concatenate([short, np.repeat(full[:1], N - 2, axis=0)])
+    want_rec = np.concatenate([r_short, np.repeat(r_full[:1], N - 2, axis=0)])
+    ref = oracle.fused_norm(want_src, MEAN, STD, want_rec, out_dtype=trfn.OUT_F16)
+    assert_parity(_f16(d1), ref, trfn.OUT_F16, "padded batch")
+    ref0 = oracle.fused_norm(full, MEAN, STD, r_full, out_dtype=trfn.OUT_F16)
+    assert_parity(_f16(d0), ref0, trfn.OUT_F16, "first batch")
+    ts.close()
+
+
+def test_first_batch_short_pads_with_its_own_first_image():
+    import torch
+    N, H, W, C = 4, 8, 16, 3
+    ts, _ = _station(N, H, W, C)
+    short = synth.pixels_uniform(71, 1, H, W, C)
+    d = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    ts.submit_partial(torch.from_numpy(short).pin_memory(), N, d, MEAN, STD)
+    assert ts.sync(30000)
+    ref = oracle.fused_norm(np.repeat(short, N, axis=0), MEAN, STD, None, out_dtype=trfn.OUT_F16)
+    assert_parity(_f16(d), ref, trfn.OUT_F16)
+    with pytest.raises(trfn.TrError):
+        ts.submit_partial(torch.from_numpy(np.repeat(short, N + 1, axis=0)).pin_memory(), N, d, MEAN, STD)
+    ts.close()

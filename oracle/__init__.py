@@ -50,6 +50,11 @@ def lib():
                                         ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int]
         L.oracle_fused_norm.restype = ctypes.c_int
+        L.oracle_fused_norm_crop.argtypes = [u8p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                             i32p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int]
+        L.oracle_fused_norm_crop.restype = ctypes.c_int
         L.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
         L.oracle_uniform01.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         L.oracle_uniform01.restype = ctypes.c_float
@@ -117,6 +122,38 @@ def fused_norm(src, mean, std, aug=None, out_dtype=OUT_F32, layout=LAYOUT_NHWC, 
     rc = lib().oracle_fused_norm(_ptr(src, ctypes.c_uint8), dst.ctypes.data_as(ctypes.c_void_p), N, H, W, C,
                                  _ptr(mean, ctypes.c_float), _ptr(std, ctypes.c_float), augp,
                                  int(out_dtype), int(layout), a, b)
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dst
+
+
+def fused_norm_crop(src_bytes, image_stride, row_stride, src_H, src_W, N, H, W, C, mean, std, crop=None,
+                    aug=None, out_dtype=OUT_F32, layout=LAYOUT_NHWC):
+    """Oracle output for H x W windows of a strided uint8 source.
+
+    src_bytes: 1-D uint8 array holding N images, image n's byte (sy, sx, c) at
+    n*image_stride + sy*row_stride + sx*C + c; crop: int32 (N, 2) {top, left}."""
+    src_bytes = np.ascontiguousarray(src_bytes, dtype=np.uint8).reshape(-1)
+    mean = np.ascontiguousarray(mean, dtype=np.float32)
+    std = np.ascontiguousarray(std, dtype=np.float32)
+    if layout == LAYOUT_NCHW:
+        shape = (N, C, H, W)
+    elif layout == LAYOUT_NHWC4:
+        shape = (N, H, W, 4)
+    else:
+        shape = (N, H, W, C)
+    dst = np.zeros(shape, dtype=np.float32 if out_dtype == OUT_F32 else np.uint16)
+    cp = None
+    if crop is not None:
+        crop = np.ascontiguousarray(crop, dtype=np.int32).reshape(N, 2)
+        cp = _ptr(crop, ctypes.c_int32)
+    ap = None
+    if aug is not None:
+        aug = np.ascontiguousarray(aug, dtype=np.int32).reshape(N, 5)
+        ap = _ptr(aug, ctypes.c_int32)
+    rc = lib().oracle_fused_norm_crop(_ptr(src_bytes, ctypes.c_uint8), image_stride, row_stride, src_H, src_W, cp,
+                                      dst.ctypes.data_as(ctypes.c_void_p), N, H, W, C, _ptr(mean, ctypes.c_float),
+                                      _ptr(std, ctypes.c_float), ap, int(out_dtype), int(layout), 0, N)
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dst

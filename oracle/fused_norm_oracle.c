@@ -208,6 +208,69 @@ int oracle_fused_norm(const uint8_t* src, void* dst, int N, int H, int W, int C,
     return 0;
 }
 
+/* The same step on windows of a larger, possibly strided, source: output
+ * pixel (n, y, x) reads source pixel (n, cy_n + y, cx_n + x') with x' the
+ * (possibly mirrored) column inside the H x W window, i.e. a crop followed by
+ * the fused step (the article's execute() takes an input stride, §五; the
+ * crop is the one upstream of it, §一).  Source byte (n, sy, sx, c) is at
+ * src[n*image_stride + sy*row_stride + sx*C + c].  crop: N pairs {cy, cx}
+ * (NULL = all zero); a window must lie inside the src_H x src_W image.
+ * Returns -1 for windows outside the source or bad strides.                */
+int oracle_fused_norm_crop(const uint8_t* src, size_t image_stride, size_t row_stride, int src_H, int src_W,
+                           const int32_t* crop, void* dst, int N, int H, int W, int C,
+                           const float* mean, const float* stdv, const int32_t* aug,
+                           int out_dtype, int out_layout, int n_begin, int n_end) {
+    if (N < 0 || H < 1 || W < 1 || C < 1 || C > 4 || src_H < H || src_W < W) return -1;
+    if (row_stride < (size_t)src_W * C || image_stride < (size_t)(src_H - 1) * row_stride + (size_t)src_W * C)
+        return -1;
+    if (out_dtype != ORACLE_OUT_F32 && out_dtype != ORACLE_OUT_F16) return -1;
+    if (out_layout != ORACLE_LAYOUT_NHWC && out_layout != ORACLE_LAYOUT_NCHW &&
+        out_layout != ORACLE_LAYOUT_NHWC4) return -1;
+    if (n_begin < 0) n_begin = 0;
+    if (n_end > N) n_end = N;
+    float* d32 = (float*)dst;
+    uint16_t* d16 = (uint16_t*)dst;
+    const int out_ch = (out_layout == ORACLE_LAYOUT_NHWC4) ? 4 : C;
+    for (int n = n_begin; n < n_end; ++n) {
+        const long long cy = crop ? crop[2 * (size_t)n] : 0;
+        const long long cx = crop ? crop[2 * (size_t)n + 1] : 0;
+        if (cy < 0 || cx < 0 || cy + H > src_H || cx + W > src_W) return -1;
+        int flip = 0;
+        long long ey0 = 0, ex0 = 0, eh = 0, ew = 0;
+        if (aug != NULL) {
+            const int32_t* a = aug + (size_t)n * 5;
+            flip = (a[0] != 0);
+            ey0 = a[1]; ex0 = a[2]; eh = a[3]; ew = a[4];
+        }
+        const int has_erase = (eh > 0 && ew > 0);
+        for (int y = 0; y < H; ++y) {
+            for (int x = 0; x < W; ++x) {
+                const int erased = has_erase && y >= ey0 && y < ey0 + eh && x >= ex0 && x < ex0 + ew;
+                const int xs = flip ? (W - 1 - x) : x;
+                for (int c = 0; c < out_ch; ++c) {
+                    float v32;
+                    if (c >= C || erased) {
+                        v32 = 0.0f;
+                    } else {
+                        const uint8_t u = src[(size_t)n * image_stride + (size_t)(cy + y) * row_stride +
+                                              (size_t)(cx + xs) * C + c];
+                        double r = ((double)u / 255.0 - (double)mean[c]) / (double)stdv[c];
+                        v32 = (float)r;
+                    }
+                    size_t o;
+                    if (out_layout == ORACLE_LAYOUT_NCHW)
+                        o = (((size_t)n * C + c) * H + y) * W + x;
+                    else
+                        o = (((size_t)n * H + y) * W + x) * out_ch + c;
+                    if (out_dtype == ORACLE_OUT_F32) d32[o] = v32;
+                    else d16[o] = oracle_f32_to_f16(v32);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
  * easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies with the

@@ -370,3 +370,44 @@ def test_sampler_moments_at_224():
     # erased pixel fraction per image ~ 0.5 * 0.175
     frac = (a[:, 3] * a[:, 4]).sum() / (N * 224.0 * 224.0)
     assert 0.08 < frac < 0.095
+
+
+# ------------------------------------------------------------- crop -------
+
+def _strided(src, row_pad, image_pad):
+    """Lay a compact (N, SH, SW, C) batch out with padded rows and images."""
+    N, SH, SW, C = src.shape
+    row_stride = SW * C + row_pad
+    image_stride = SH * row_stride + image_pad
+    buf = np.full(N * image_stride, 0xEE, np.uint8)
+    for n in range(N):
+        for y in range(SH):
+            o = n * image_stride + y * row_stride
+            buf[o:o + SW * C] = src[n, y].reshape(-1)
+    return buf, image_stride, row_stride
+
+
+@pytest.mark.parametrize("pads", [(0, 0), (16, 0), (5, 96), (48, 7)])
+def test_crop_equals_slicing_then_the_plain_step(pads):
+    """A window of a strided source equals numpy slicing followed by the
+    compact oracle: the crop only moves indices."""
+    mean, std, _ = oracle.norm_preset("IMAGENET")
+    N, SH, SW, C, H, W = 4, 12, 20, 3, 7, 9
+    src = synth.pixels_uniform(21, N, SH, SW, C)
+    buf, istr, rstr = _strided(src, *pads)
+    crop = np.array([[0, 0], [5, 11], [2, 3], [SH - H, SW - W]], np.int32)
+    aug = np.array([[1, 1, 2, 3, 4], [0, 0, 0, 0, 0], [1, 6, 8, 1, 1], [0, 2, 0, 5, 9]], np.int32)
+    for dt in (oracle.OUT_F32, oracle.OUT_F16):
+        for lay in (oracle.LAYOUT_NHWC, oracle.LAYOUT_NCHW, oracle.LAYOUT_NHWC4):
+            got = oracle.fused_norm_crop(buf, istr, rstr, SH, SW, N, H, W, C, mean, std, crop, aug, dt, lay)
+            windows = np.stack([src[n, cy:cy + H, cx:cx + W] for n, (cy, cx) in enumerate(crop)])
+            assert np.array_equal(got, oracle.fused_norm(windows, mean, std, aug, out_dtype=dt, layout=lay))
+
+
+def test_crop_rejects_windows_outside_the_source():
+    mean, std, _ = oracle.norm_preset("IMAGENET")
+    src = synth.pixels_uniform(1, 1, 8, 8, 3)
+    with pytest.raises(ValueError):
+        oracle.fused_norm_crop(src.reshape(-1), 192, 24, 8, 8, 1, 4, 4, 3, mean, std, np.array([[5, 0]]))
+    with pytest.raises(ValueError):
+        oracle.fused_norm_crop(src.reshape(-1), 192, 24, 8, 8, 1, 4, 4, 3, mean, std, np.array([[0, -1]]))

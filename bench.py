@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4])
     ap.add_argument("--layout", default=None, help="override the config's output layout (nhwc/nchw/nhwc4)")
     ap.add_argument("--batch", type=int, default=None, help="override the config's batch size N")
+    ap.add_argument("--crop", type=int, default=0,
+                    help="read each image as a window of an SxS source (random origins when the workload "
+                         "flips/erases, else the centre): tr_fused_norm_crop")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
     ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
     ap.add_argument("--e2e-steps", type=int, default=64)
@@ -203,6 +206,9 @@ def workload(args):
     if args.batch:
         name = name.replace("n%d_" % cfg["N"], "n%d_" % args.batch, 1)
         cfg["N"] = args.batch
+    cfg["crop"] = getattr(args, "crop", 0)
+    if cfg["crop"]:
+        name += "_crop_from_%dx%d" % (cfg["crop"], cfg["crop"])
     cfg["workload"] = name
     return cfg
 
@@ -257,13 +263,22 @@ def run_ours(args, rank, local, world, pg):
 
     # distinct buffer sets whose total footprint is at least 4x L2
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = N * H * W * C + int(np.prod(out_shape)) * (2 if dt == trfn.OUT_F16 else 4)
+    S = cfg["crop"]
+    src_img = (S * S * C) if S else (H * W * C)
+    set_bytes = N * src_img + int(np.prod(out_shape)) * (2 if dt == trfn.OUT_F16 else 4)
     nsets = max(2, int(np.ceil(4 * l2 / set_bytes)))
-    srcs, dsts, augs, recs_all = [], [], [], []
+    srcs, dsts, augs, recs_all, crops = [], [], [], [], []
     offset = rank * 10 ** 9
     for j in range(nsets):
-        hb = host_batch(cfg, 1000 + args.config + 100 * j + 7919 * rank)
+        hb = host_batch(dict(cfg, H=S, W=S) if S else cfg, 1000 + args.config + 100 * j + 7919 * rank)
         srcs.append(torch.from_numpy(hb).to(dev))
+        if S:
+            g = np.random.default_rng(3000 + j)
+            if cfg["flip"] or cfg["erase"]:
+                c = np.stack([g.integers(0, S - H + 1, N), g.integers(0, S - W + 1, N)], axis=1)
+            else:
+                c = np.tile([(S - H) // 2, (S - W) // 2], (N, 1))
+            crops.append(torch.from_numpy(c.astype(np.int32)).to(dev))
         dsts.append(torch.empty(out_shape, dtype=tdt, device=dev))
         recs, offset = sample_records(cfg, 2000 + args.config, offset, trfn.tr_sample_aug_params)
         recs_all.append(recs)
@@ -276,8 +291,13 @@ def run_ours(args, rank, local, world, pg):
     ws = None if args.static else torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
 
     def launch(j):
-        trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout, stream=stream,
-                           variant=args.variant, workspace=ws)
+        if S:
+            trfn.tr_fused_norm_crop(srcs[j], S, S, S * C, S * S * C, dsts[j], N, H, W, C, mean, std, crop=crops[j],
+                                    aug=augs[j], out_dtype=dt, layout=layout, stream=stream, variant=args.variant,
+                                    workspace=ws)
+        else:
+            trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout, stream=stream,
+                               variant=args.variant, workspace=ws)
 
     # warm the library's per-kernel caches, then capture graphs of launches
     with torch.cuda.stream(stream):
@@ -341,7 +361,7 @@ def run_ours(args, rank, local, world, pg):
     peak, peak_kind = measured_peaks()
 
     # sampled parity of the last outputs against the oracle (bench's own launch configuration)
-    parity = parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets)
+    parity = parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets, crops)
 
     e2e = None
     if not args.no_e2e:
@@ -369,6 +389,7 @@ def run_ours(args, rank, local, world, pg):
                 nsets, nsets * set_bytes / 1e6, l2 / 1e6),
             "launch": "CUDA graph of %d launches replayed; variant %d" % (G, args.variant),
             "schedule": "static (tr_fused_norm)" if args.static else "dynamic bands (tr_fused_norm_ws)",
+            "source": ("%dx%d windows of %dx%d images (tr_fused_norm_crop)" % (H, W, S, S)) if S else "compact",
             "parallelism": "replicas" if world > 1 else "single",
         },
         "hbm_gbs": achieved_gbs,
@@ -390,7 +411,7 @@ def run_ours(args, rank, local, world, pg):
     return res
 
 
-def parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets):
+def parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets, crops=None):
     """A few images of the last written buffer set against the oracle."""
     import oracle
     import torch
@@ -400,7 +421,12 @@ def parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets):
     recs = recs_all[j][idx] if recs_all[j] is not None else None
     got = dsts[j][idx].cpu()
     got = got.view(torch.int16).numpy().view(np.uint16) if dt == 1 else got.numpy()
-    ref = oracle.fused_norm(src, mean, std, recs, out_dtype=dt, layout=layout)
+    if crops:
+        S, H, W, C = cfg["crop"], cfg["H"], cfg["W"], cfg["C"]
+        ref = oracle.fused_norm_crop(src.reshape(-1), S * S * C, S * C, S, S, len(idx), H, W, C, mean, std,
+                                     crops[j][idx].cpu().numpy(), recs, dt, layout)
+    else:
+        ref = oracle.fused_norm(src, mean, std, recs, out_dtype=dt, layout=layout)
     if dt == 1:
         def ordered(b):
             b = b.astype(np.int32)

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "tr_fused_norm_variant": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i]),
     "tr_fused_norm_ws": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i, _vp]),
     "tr_workspace_bytes": (ctypes.c_size_t, []),
+    "tr_fused_norm_crop": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
+                                _vp, _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp]),
     "tr_fused_norm_plan": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]),
     "tr_norm_preset": (_i, [_i, _fp, _fp, ctypes.POINTER(_i)]),

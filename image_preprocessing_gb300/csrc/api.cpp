@@ -40,9 +40,17 @@ int check_shape(int N, int H, int W, int C, int out_dtype, int out_layout) {
     return TR_OK;
 }
 
+// A strided source read through per-image windows (tr_fused_norm_crop).
+struct CropSource {
+    bool on = false;
+    const int32_t* crop = nullptr;
+    int src_H = 0, src_W = 0;
+    size_t row_stride = 0, image_stride = 0;
+};
+
 int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,
                     const float* stdv, const tr_aug_param* aug, int out_dtype, int out_layout,
-                    void* stream, int variant, void* workspace) {
+                    void* stream, int variant, void* workspace, const CropSource& cs = CropSource()) {
     int rc = check_shape(N, H, W, C, out_dtype, out_layout);
     if (rc != TR_OK) return rc;
     if (variant != TR_VARIANT_AUTO && variant != TR_VARIANT_TILED && variant != TR_VARIANT_GENERIC)
@@ -68,12 +76,24 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     if (aug != nullptr && ((uintptr_t)aug % 4u) != 0) return TR_ERR_INVALID_ARGUMENT;
     if (workspace != nullptr && ((uintptr_t)workspace % 16u) != 0) return TR_ERR_INVALID_ARGUMENT;
     const int out_ch = (out_layout == TR_LAYOUT_NHWC4) ? 4 : C;
-    const unsigned long long in_bytes = (unsigned long long)N * H * W * C;
+    if (cs.on) {
+        if (cs.src_H < H || cs.src_W < W) return TR_ERR_INVALID_ARGUMENT;
+        if (cs.row_stride < (size_t)cs.src_W * C ||
+            cs.image_stride < (size_t)(cs.src_H - 1) * cs.row_stride + (size_t)cs.src_W * C)
+            return TR_ERR_INVALID_ARGUMENT;
+        if (cs.crop != nullptr && ((uintptr_t)cs.crop % 4u) != 0) return TR_ERR_INVALID_ARGUMENT;
+    }
+    const unsigned long long in_bytes =
+        cs.on ? (unsigned long long)(N - 1) * cs.image_stride + (unsigned long long)(cs.src_H - 1) * cs.row_stride +
+                    (unsigned long long)cs.src_W * C
+              : (unsigned long long)N * H * W * C;
     const unsigned long long out_bytes = (unsigned long long)N * H * W * out_ch * ob;
     const uintptr_t s0 = (uintptr_t)src, d0 = (uintptr_t)dst;
     if (s0 < d0 + out_bytes && d0 < s0 + in_bytes) return TR_ERR_INVALID_ARGUMENT;   // overlap
 
-    const bool tiled_ok = tiled_supported(src, dst, N, H, W, C, out_dtype, out_layout);
+    const bool tiled_ok = cs.on ? tiled_crop_supported(src, dst, N, H, W, C, out_dtype, out_layout, cs.src_H,
+                                                       cs.src_W, cs.row_stride, cs.image_stride)
+                                : tiled_supported(src, dst, N, H, W, C, out_dtype, out_layout);
     const bool forced = (variant != TR_VARIANT_AUTO);
     if (variant == TR_VARIANT_TILED && !tiled_ok) return TR_ERR_NOT_SUPPORTED;
     if (variant == TR_VARIANT_AUTO) variant = tiled_ok ? TR_VARIANT_TILED : TR_VARIANT_GENERIC;
@@ -86,6 +106,12 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     a.out_layout = out_layout;
     a.stream = stream;
     a.workspace = workspace;
+    a.crop_src = cs.on;
+    a.crop = cs.crop;
+    a.src_H = cs.src_H;
+    a.src_W = cs.src_W;
+    a.src_row_stride = cs.row_stride;
+    a.src_image_stride = cs.image_stride;
     rc = launch(a, variant);
     if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {
         // the tiled geometry does not fit this device's shared memory (rows
@@ -124,6 +150,22 @@ int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
 }
 
 size_t tr_workspace_bytes(void) { return kWorkspaceBytes; }
+
+int tr_fused_norm_crop(const uint8_t* src_u8, int src_H, int src_W, size_t src_row_stride,
+                       size_t src_image_stride, const int32_t* crop_yx, void* dst, int N, int H, int W, int C,
+                       const float* mean, const float* std, const tr_aug_param* aug_params, int out_dtype,
+                       int out_layout, void* stream, int variant, void* workspace) {
+    if (src_H < 1 || src_W < 1) return TR_ERR_INVALID_ARGUMENT;
+    CropSource cs;
+    cs.on = true;
+    cs.crop = crop_yx;
+    cs.src_H = src_H;
+    cs.src_W = src_W;
+    cs.row_stride = src_row_stride;
+    cs.image_stride = src_image_stride;
+    return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout, stream,
+                           variant, workspace, cs);
+}
 
 int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,
                        int out_dtype, int out_layout, int* variant) {

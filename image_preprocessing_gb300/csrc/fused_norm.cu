@@ -19,7 +19,12 @@
 //    same PRMT, one exact FADD removes 2^23, one FFMA applies scale and bias.
 //    Results go to a double-buffered shared-memory output tile that one TMA
 //    bulk store per band (per plane for NCHW) writes to global memory.
-//  * GENERIC: one thread per output element, any shape and alignment.
+//    With a crop source (tr_fused_norm_crop) the bands come from windows of a
+//    strided source through a TMA tensor copy (cp.async.bulk.tensor): the
+//    source is described as {16-byte chunk, chunk, row, image}, so a window
+//    may start at any byte; consumers realign the first chunk's offset with
+//    funnel shifts.
+//  * GENERIC: one thread per output element, any shape, stride and alignment.
 //
 // Both kernels compute each value as fma(float(x), scale_c, bias_c) with the
 // same binary32 operands, so they agree bit for bit.
@@ -28,6 +33,8 @@
 // within about a second sets bit 0 of the device status word, the CTA drains
 // what it has in flight (again bounded) and returns.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -159,6 +166,16 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return pol;
 }
 
+// TMA tensor copy of one box of a 4-d tensor map into shared memory.
+__device__ __forceinline__ void tensor_g2s_4d(uint32_t dst_smem, const void* tmap, int c0, int c1, int c2, int c3,
+                                              uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst_smem),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // TMA bulk copy shared -> global in the current bulk group.
 __device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
@@ -233,6 +250,10 @@ __device__ __forceinline__ void convert_group(const uint32_t (&w)[Group<C>::kWor
 // ---------------------------------------------------------------- tiled ---
 
 struct TiledParams {
+    CUtensorMap tmap;      // crop sources: {16-byte chunk, chunk, row, image} of the source
+    const int32_t* crop;   // crop sources: per-image window origin {top, left}, or null
+    int src_H, src_W;      // crop sources: source image size
+    uint32_t in_pitch;     // bytes per row of an input stage (W*C; chunks*16 for crop sources)
     const uint8_t* src;
     uint8_t* dst;
     const tr_aug_param* aug;
@@ -256,7 +277,8 @@ struct TiledParams {
 
 // Per-stage record of the unit held in that stage.
 struct UnitRec {
-    int n, y_begin, rows, flip;
+    int n, y_begin, rows;
+    int flags;             // bit 0: flip; bits 8..11: byte offset of the window in its first chunk
     int erow_lo, erow_hi;  // erased output rows [lo, hi), clipped to the image
     int ecol_lo, ecol_hi;  // erased output columns [lo, hi), clipped
 };
@@ -288,7 +310,7 @@ __device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, c
 // full[s] with the byte count and issues the band's copies, skipping the
 // 16-byte chunks that lie wholly inside the erased source span of the erased
 // rows.
-template <int C>
+template <int C, bool CROP>
 __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem,
                                            const tr_aug_param& a) {
     const Band b = band_of(p, u);
@@ -305,8 +327,25 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
         }
     }
     UnitRec* rec = reinterpret_cast<UnitRec*>(smem + kRecOffset) + s;
-    rec->n = b.n; rec->y_begin = y_begin; rec->rows = rows; rec->flip = flip;
+    rec->n = b.n; rec->y_begin = y_begin; rec->rows = rows; rec->flags = flip;
     rec->erow_lo = erow_lo; rec->erow_hi = erow_hi; rec->ecol_lo = ecol_lo; rec->ecol_hi = ecol_hi;
+
+    if (CROP) {
+        // The window's rows, from its 16-byte chunk on, as one box of R rows
+        // (rows past the source image arrive as zeros and are not used).
+        int cy = 0, cx = 0;
+        if (p.crop != nullptr) {
+            cy = min(max(p.crop[2 * (size_t)b.n], 0), p.src_H - p.H);
+            cx = min(max(p.crop[2 * (size_t)b.n + 1], 0), p.src_W - p.W);
+        }
+        const int xb = cx * C;
+        rec->flags = flip | ((xb & 15) << 8);
+        const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
+        mbar_arrive_expect_tx(bar, (uint32_t)p.R * p.in_pitch);
+        tensor_g2s_4d(smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage, &p.tmap, 0, xb >> 4,
+                      cy + y_begin, b.n, bar, (p.hints & 1) ? policy_evict_last() : policy_evict_first());
+        return;
+    }
 
     const uint32_t L = (uint32_t)p.W * C;
     const uint8_t* g = p.src + ((size_t)b.n * p.H + y_begin) * L;
@@ -413,7 +452,7 @@ __device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout,
     }
 }
 
-template <int C, int OUT_F16, int LAYOUT>
+template <int C, int OUT_F16, int LAYOUT, bool CROP>
 __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
                                              uint8_t* sout, const UnitRec& rec, int tid, int nthr) {
     constexpr int P = Group<C>::P;
@@ -434,10 +473,20 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
 #pragma unroll
             for (int k = 0; k < GB; ++k) v[k] = 0.0f;
         } else {
-            const int sgx = rec.flip ? (p.gpr - 1 - gx) : gx;
+            const int sgx = (rec.flags & 1) ? (p.gpr - 1 - gx) : gx;
             const uint8_t* s = sin + (size_t)r * L + (size_t)sgx * GB;
             uint32_t w[Group<C>::kWords];
-            if (GB == 16) {
+            if (CROP) {
+                // the group starts at any byte: aligned words, then funnel shifts
+                const uint32_t at = (uint32_t)r * p.in_pitch + (uint32_t)(rec.flags >> 8) + (uint32_t)sgx * GB;
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(sin + (at & ~3u));
+                const uint32_t sh = (at & 3u) * 8u;
+                uint32_t raw[Group<C>::kWords + 1];
+#pragma unroll
+                for (int q = 0; q <= Group<C>::kWords; ++q) raw[q] = wp[q];
+#pragma unroll
+                for (int q = 0; q < Group<C>::kWords; ++q) w[q] = __funnelshift_r(raw[q], raw[q + 1], sh);
+            } else if (GB == 16) {
                 const uint4 t = *reinterpret_cast<const uint4*>(s);
                 w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
             } else {
@@ -448,7 +497,7 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
                     w[2 * q + 1] = t.y;
                 }
             }
-            if (rec.flip) convert_group<C, true>(w, p.scale, p.bias, v);
+            if (rec.flags & 1) convert_group<C, true>(w, p.scale, p.bias, v);
             else convert_group<C, false>(w, p.scale, p.bias, v);
             if (lo < hi) {
 #pragma unroll
@@ -510,7 +559,7 @@ constexpr int kDoneWord = kTicketGroups * kTicketStride;
 // Warps 1.. are consumers: they wait for full[s], convert the band into the
 // output tile i % 2, meet on named barrier 1, and one of them releases the
 // stage and issues the TMA store of the tile.
-template <int C, int OUT_F16, int LAYOUT>
+template <int C, int OUT_F16, int LAYOUT, bool CROP>
 __global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ TiledParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
@@ -556,7 +605,7 @@ __global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ Tile
                     mbar_arrive(full0 + 8u * s);
                     break;
                 }
-                issue_unit<C>(p, u, s, smem, a);
+                issue_unit<C, CROP>(p, u, s, smem, a);
                 // the next unit and its record: requested now, used after the
                 // next empty wait
                 if (p.ws == nullptr || j + 1 < S) {
@@ -602,7 +651,7 @@ __global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ Tile
         const bool ok = mbar_wait_bounded(full0 + 8u * s, (uint32_t)(i / S) & 1u);
         const UnitRec rec = recs[s];
         uint8_t* ob = sout + (size_t)(i & 1) * p.out_stage;
-        if (ok) compute_unit<C, OUT_F16, LAYOUT>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
+        if (ok) compute_unit<C, OUT_F16, LAYOUT, CROP>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
         fence_proxy_async_smem();
         // The store issued last iteration reads the other output tile, which
         // the next iteration overwrites: it must be done reading first.
@@ -626,8 +675,11 @@ struct GenericParams {
     const uint8_t* src;
     uint8_t* dst;
     const tr_aug_param* aug;
+    const int32_t* crop;   // per-image window origin {top, left}, or null
     long long total;       // output elements
+    long long image_stride, row_stride;   // source strides in bytes
     int H, W, C;
+    int src_H, src_W;      // source image size (H, W for compact sources)
     float scale[4];
     float bias[4];
 };
@@ -665,8 +717,14 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
                          x >= a.x0 && x < (long long)a.x0 + a.w;
             }
             if (!erased) {
+                long long cy = 0, cx = 0;
+                if (p.crop != nullptr) {
+                    cy = min(max((long long)p.crop[2 * n], 0ll), (long long)(p.src_H - p.H));
+                    cx = min(max((long long)p.crop[2 * n + 1], 0ll), (long long)(p.src_W - p.W));
+                }
                 const long long xs = flip ? (W - 1 - x) : x;
-                const uint8_t b = __ldg(p.src + ((n * H + y) * W + xs) * C + c);
+                const uint8_t b =
+                    __ldg(p.src + n * p.image_stride + (cy + y) * p.row_stride + (cx + xs) * C + c);
                 v = __fmaf_rn((float)b, p.scale[c], p.bias[c]);
             }
         }
@@ -697,27 +755,32 @@ DeviceInfo device_info(int dev) {
 using TiledFn = void (*)(TiledParams);
 using GenericFn = void (*)(GenericParams);
 
-template <int C, int F16>
+template <int C, int F16, bool CROP>
 TiledFn pick_tiled_layout(int layout) {
     switch (layout) {
-    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC>;
-    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW>;
-    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4>;
+    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC, CROP>;
+    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW, CROP>;
+    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4, CROP>;
     }
 }
 
-template <int C>
+template <int C, bool CROP>
 TiledFn pick_tiled_dtype(int f16, int layout) {
-    return f16 ? pick_tiled_layout<C, 1>(layout) : pick_tiled_layout<C, 0>(layout);
+    return f16 ? pick_tiled_layout<C, 1, CROP>(layout) : pick_tiled_layout<C, 0, CROP>(layout);
 }
 
-TiledFn pick_tiled(int C, int f16, int layout) {
+template <bool CROP>
+TiledFn pick_tiled_c(int C, int f16, int layout) {
     switch (C) {
-    case 1: return pick_tiled_dtype<1>(f16, layout);
-    case 2: return pick_tiled_dtype<2>(f16, layout);
-    case 3: return pick_tiled_dtype<3>(f16, layout);
-    default: return pick_tiled_dtype<4>(f16, layout);
+    case 1: return pick_tiled_dtype<1, CROP>(f16, layout);
+    case 2: return pick_tiled_dtype<2, CROP>(f16, layout);
+    case 3: return pick_tiled_dtype<3, CROP>(f16, layout);
+    default: return pick_tiled_dtype<4, CROP>(f16, layout);
     }
+}
+
+TiledFn pick_tiled(int C, int f16, int layout, bool crop) {
+    return crop ? pick_tiled_c<true>(C, f16, layout) : pick_tiled_c<false>(C, f16, layout);
 }
 
 GenericFn pick_generic(int f16, int layout) {
@@ -746,7 +809,10 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Geometry knobs (tr_tune_tiled); 0 keeps the default.
 std::atomic<int> g_band_bytes{0}, g_stages{0}, g_ctas_per_sm{0}, g_flags{0};
 
-TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit) {
+// pitch: bytes of one staged source row (W*C, or the crop box's chunks*16);
+// slack: extra bytes after a stage's rows (crop consumers read one word past).
+TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch = 0,
+                     size_t slack = 0) {
     TiledPlan pl;
     const int ob = f16 ? 2 : 4;
     const int P = group_pixels(C);
@@ -768,11 +834,12 @@ TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit) {
     const int sknob = g_stages.load(std::memory_order_relaxed);
     const int stages0 = std::min(sknob >= 2 ? sknob : ((size_t)R * L > 8192 ? 3 : 4), kMaxStages);
     int stages = stages0;
+    if (pitch == 0) pitch = L;
     for (;;) {
-        const size_t in_stage = round_up((size_t)R * L, 128);
+        const size_t in_stage = round_up((size_t)R * pitch + slack, 128);
         const size_t out_stage = round_up((size_t)R * out_row, 128);
         const size_t smem = kHeaderBytes + stages * in_stage + 2 * out_stage;
-        if (in_stage < (1u << 20) && smem <= (size_t)smem_limit) {
+        if (in_stage < (1u << 20) && smem <= (size_t)smem_limit && R <= 256) {
             pl.ok = true;
             pl.R = R;
             pl.bands = (H + R - 1) / R;
@@ -817,6 +884,38 @@ bool check_cuda(cudaError_t e, const char* what) {
     return false;
 }
 
+// The source of a crop launch as a 4-d tensor {16-byte chunk, chunk, row,
+// image} for TMA tensor copies; the box is {16, nch, R, 1}.  Reads outside the
+// tensor (rows past an image, chunks past a row) arrive as zeros.
+int encode_crop_map(CUtensorMap* map, const LaunchArgs& a, uint32_t nch, uint32_t R) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (encode == nullptr) {
+        set_last_error("cuTensorMapEncodeTiled unavailable", (int)cudaErrorNotSupported);
+        return TR_ERR_CUDA;
+    }
+    const cuuint64_t dims[4] = {16, (cuuint64_t)a.src_W * a.C / 16, (cuuint64_t)a.src_H, (cuuint64_t)a.N};
+    const cuuint64_t strides[3] = {16, (cuuint64_t)a.src_row_stride, (cuuint64_t)a.src_image_stride};
+    const cuuint32_t box[4] = {16, nch, R, 1};
+    const cuuint32_t elem[4] = {1, 1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(a.src), dims, strides,
+                              box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_last_error("cuTensorMapEncodeTiled", (int)cudaErrorInvalidValue);
+        return TR_ERR_CUDA;
+    }
+    return TR_OK;
+}
+
 int launch_tiled(const LaunchArgs& a) {
     int dev = 0;
     if (!check_cuda(cudaGetDevice(&dev), "cudaGetDevice")) return TR_ERR_CUDA;
@@ -826,10 +925,25 @@ int launch_tiled(const LaunchArgs& a) {
         return TR_ERR_CUDA;
     }
     const int f16 = (a.out_dtype == TR_OUT_F16);
-    const TiledPlan pl = plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin);
+    const bool crop = a.crop_src;
+    const size_t L = (size_t)a.W * a.C;
+    // crop sources: a box of R rows of `nch` 16-byte chunks covers a window
+    // that starts anywhere in its first chunk
+    const size_t nch = crop ? (L + 15 + 15) / 16 : 0;
+    if (crop && nch > 256) return TR_ERR_NOT_SUPPORTED;
+    const TiledPlan pl = plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, crop ? nch * 16 : 0,
+                                    crop ? 16 : 0);
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 
     TiledParams p;
+    p.crop = a.crop;
+    p.src_H = crop ? a.src_H : a.H;
+    p.src_W = crop ? a.src_W : a.W;
+    p.in_pitch = (uint32_t)(crop ? nch * 16 : L);
+    if (crop) {
+        const int rc = encode_crop_map(&p.tmap, a, (uint32_t)nch, (uint32_t)pl.R);
+        if (rc != TR_OK) return rc;
+    }
     p.src = a.src;
     p.dst = static_cast<uint8_t*>(a.dst);
     p.aug = a.aug;
@@ -847,14 +961,14 @@ int launch_tiled(const LaunchArgs& a) {
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 
-    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout);
+    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop);
     // Per-kernel opt-in to the device's largest dynamic shared memory (once),
     // and the occupancy of each (threads, shared memory) geometry.
     struct Cached { const void* fn; int dev; size_t smem; int threads; int blocks; };
     static std::mutex mu;
     static Cached cache[256];
     static int ncache = 0;
-    static const void* opted[64][32];
+    static const void* opted[64][64];
     static int nopted[64];
     int blocks_per_sm = 0;
     {
@@ -867,7 +981,7 @@ int launch_tiled(const LaunchArgs& a) {
                                                  di.smem_optin),
                             "cudaFuncSetAttribute"))
                 return TR_ERR_CUDA;
-            if (nopted[dev] < 32) opted[dev][nopted[dev]++] = (const void*)fn;
+            if (nopted[dev] < 64) opted[dev][nopted[dev]++] = (const void*)fn;
         }
         for (int k = 0; k < ncache; ++k) {
             if (cache[k].fn == (const void*)fn && cache[k].dev == dev && cache[k].smem == pl.smem &&
@@ -916,6 +1030,11 @@ int launch_generic(const LaunchArgs& a) {
     p.aug = a.aug;
     p.total = (long long)a.N * a.H * a.W * out_ch;
     p.H = a.H; p.W = a.W; p.C = a.C;
+    p.crop = a.crop_src ? a.crop : nullptr;
+    p.src_H = a.crop_src ? a.src_H : a.H;
+    p.src_W = a.crop_src ? a.src_W : a.W;
+    p.row_stride = a.crop_src ? (long long)a.src_row_stride : (long long)a.W * a.C;
+    p.image_stride = a.crop_src ? (long long)a.src_image_stride : (long long)a.H * a.W * a.C;
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
     const int threads = 256;
     long long grid = (p.total + threads - 1) / threads;
@@ -941,6 +1060,16 @@ bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, i
     if (((long long)W * C) % 16 != 0) return false;
     if (out_layout == TR_LAYOUT_NCHW && ((long long)W * ob) % 16 != 0) return false;
     if ((long long)N * H > (1LL << 31) - 1) return false;   // unit indices are int
+    return true;
+}
+
+bool tiled_crop_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C, int out_dtype,
+                          int out_layout, int src_H, int src_W, size_t row_stride, size_t image_stride) {
+    if (!tiled_supported(src, dst, N, H, W, C, out_dtype, out_layout)) return false;
+    if (((size_t)src_W * C) % 16 != 0 || row_stride % 16 != 0 || image_stride % 16 != 0) return false;
+    if (image_stride < (size_t)src_H * row_stride) return false;
+    if (((size_t)W * C + 30) / 16 > 256) return false;
+    if ((size_t)src_W * C / 16 > 0xFFFFFFFFull || (long long)src_H > 0xFFFFFFFFll) return false;
     return true;
 }
 

@@ -21,6 +21,12 @@ struct LaunchArgs {
     int out_layout;
     void* stream;
     void* workspace;  // scheduling workspace (tr_workspace_bytes(), zeroed), or null
+    // windows of a strided source (tr_fused_norm_crop); otherwise a compact
+    // NHWC source of H x W images
+    bool crop_src = false;
+    const int32_t* crop = nullptr;
+    int src_H = 0, src_W = 0;
+    size_t src_row_stride = 0, src_image_stride = 0;
 };
 
 constexpr size_t kWorkspaceBytes = 2048;
@@ -28,6 +34,11 @@ constexpr size_t kWorkspaceBytes = 2048;
 // Whether the tiled kernel's preconditions hold for these arguments.
 bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C,
                      int out_dtype, int out_layout);
+
+// Whether the tiled kernel can read crop windows of this strided source
+// through TMA tensor copies.
+bool tiled_crop_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C, int out_dtype,
+                          int out_layout, int src_H, int src_W, size_t row_stride, size_t image_stride);
 
 // Launches the chosen kernel (TR_VARIANT_TILED or TR_VARIANT_GENERIC) on
 // a.stream.  Returns a tr_status.

@@ -140,6 +140,33 @@ int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
                      const float* mean, const float* std, const tr_aug_param* aug_params,
                      int out_dtype, int out_layout, void* stream, int variant, void* workspace);
 
+/* tr_fused_norm_crop — the fused step on H x W windows of a larger, strided
+ * source: the crop just upstream of the step fused into its load (the
+ * article's execute() takes an input stride, §五; DALI's crop_mirror_normalize,
+ * cited as prior art in §二.2, also fuses the crop).
+ *   src_u8       device; image n's byte (sy, sx, c) is at
+ *                src_u8[n*src_image_stride + sy*src_row_stride + sx*C + c],
+ *                0 <= sy < src_H, 0 <= sx < src_W.
+ *   crop_yx      device int32 [N][2]: the window's top row and left column in
+ *                its source image (4-byte aligned), or NULL for (0, 0) for all.
+ *                Windows are clamped into the source image, so an origin out
+ *                of range cannot read out of bounds.
+ *   N,H,W,C, dst, mean, std, aug_params (in window coordinates), out_dtype,
+ *   out_layout, stream, variant, workspace: as tr_fused_norm_ws.
+ * Output pixel (n, y, x) takes source pixel (n, cy + y, cx + x') with x' the
+ * column of the window, mirrored when flipping.  The TILED kernel reads the
+ * windows with TMA tensor copies when src is 16-byte aligned, src_W*C,
+ * src_row_stride and src_image_stride are multiples of 16,
+ * src_image_stride >= src_H*src_row_stride and W*C <= 4064 (plus the TILED
+ * conditions of tr_fused_norm); otherwise GENERIC.
+ * Errors as tr_fused_norm, and TR_ERR_INVALID_ARGUMENT for src_H < H,
+ * src_W < W, a row stride below src_W*C or an image stride below
+ * (src_H-1)*src_row_stride + src_W*C.                                       */
+int tr_fused_norm_crop(const uint8_t* src_u8, int src_H, int src_W, size_t src_row_stride,
+                       size_t src_image_stride, const int32_t* crop_yx, void* dst, int N, int H, int W, int C,
+                       const float* mean, const float* std, const tr_aug_param* aug_params, int out_dtype,
+                       int out_layout, void* stream, int variant, void* workspace);
+
 /* Bytes of the scheduling workspace (2048). */
 size_t tr_workspace_bytes(void);
 

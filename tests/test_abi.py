@@ -206,3 +206,22 @@ def test_product_sources_never_reference_the_oracle():
             if fn.endswith((".py", ".cu", ".cpp", ".h")):
                 text = open(os.path.join(dirpath, fn), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text and "liboracle" not in text, fn
+
+
+def test_crop_arguments_rejected_before_launch():
+    L = _native.lib()
+    # src_H < H, row stride below a row, image stride below an image
+    assert L.tr_fused_norm_crop(0x1000, 10, 20, 60, 600, None, 0x100000, 1, 12, 16, 3, M3, S3, None, 0, 0,
+                                None, 0, None) == INVALID
+    assert L.tr_fused_norm_crop(0x1000, 20, 20, 50, 1200, None, 0x100000, 1, 12, 16, 3, M3, S3, None, 0, 0,
+                                None, 0, None) == INVALID
+    assert L.tr_fused_norm_crop(0x1000, 20, 20, 64, 600, None, 0x100000, 1, 12, 16, 3, M3, S3, None, 0, 0,
+                                None, 0, None) == INVALID
+    # crop origins off int32 alignment
+    assert L.tr_fused_norm_crop(0x1000, 20, 20, 64, 1280, 0x5002, 0x100000, 1, 12, 16, 3, M3, S3, None, 0, 0,
+                                None, 0, None) == INVALID
+    # forced TILED where the source strides are not 16-byte multiples
+    assert L.tr_fused_norm_crop(0x1000, 20, 20, 60, 1200, None, 0x100000, 1, 12, 16, 3, M3, S3, None, 0, 0,
+                                None, 1, None) == NOT_SUPPORTED
+    assert L.tr_fused_norm_crop(None, 20, 20, 64, 1280, None, None, 0, 12, 16, 3, M3, S3, None, 0, 0,
+                                None, 0, None) == OK

@@ -55,6 +55,9 @@ def lib():
                                              ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int]
         L.oracle_fused_norm_crop.restype = ctypes.c_int
+        L.oracle_exp_f32_array.argtypes = [f32p, f32p, ctypes.c_size_t]
+        L.oracle_sample_aug_params_blocked.argtypes = L.oracle_sample_aug_params.argtypes
+        L.oracle_sample_aug_params_blocked.restype = ctypes.c_int
         L.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
         L.oracle_uniform01.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
         L.oracle_uniform01.restype = ctypes.c_float
@@ -63,6 +66,8 @@ def lib():
                                                ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                                ctypes.c_float, ctypes.c_float, ctypes.c_float, i32p, u64p]
         L.oracle_sample_aug_params.restype = ctypes.c_int
+        L.oracle_sample_aug_params_blocked.argtypes = L.oracle_sample_aug_params.argtypes
+        L.oracle_sample_aug_params_blocked.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -179,6 +184,31 @@ def sample_aug_params(seed, offset, N, H, W, flip=True, flip_p=0.5, erase=True, 
     rc = lib().oracle_sample_aug_params(seed, offset, N, H, W, int(flip), flip_p, int(erase), erase_p,
                                         scale[0], scale[1], ratio[0], ratio[1],
                                         _ptr(out, ctypes.c_int32), ctypes.byref(nxt))
+    if rc != 0:
+        raise ValueError("oracle sampler rejected the arguments")
+    return out, nxt.value
+
+
+def exp_f32(x):
+    """The oracle's own binary32 exp (Cody-Waite reduction, degree-7 Taylor)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    lib().oracle_exp_f32_array(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_float), x.size)
+    return out
+
+
+DRAWS_PER_IMAGE = 24
+
+
+def sample_aug_params_blocked(seed, offset, N, H, W, flip=True, flip_p=0.5, erase=True, erase_p=0.5,
+                              scale=(0.02, 0.33), ratio=(0.3, 3.3)):
+    """Records with one counter block of 24 draws per image (image n uses
+    offsets offset + 24n + k); returns (int32 (N, 5), offset + 24N)."""
+    out = np.zeros((N, 5), np.int32)
+    nxt = ctypes.c_uint64(0)
+    rc = lib().oracle_sample_aug_params_blocked(seed, offset, N, H, W, int(flip), flip_p, int(erase), erase_p,
+                                                scale[0], scale[1], ratio[0], ratio[1],
+                                                _ptr(out, ctypes.c_int32), ctypes.byref(nxt))
     if rc != 0:
         raise ValueError("oracle sampler rejected the arguments")
     return out, nxt.value

@@ -385,3 +385,94 @@ int oracle_sample_aug_params(uint64_t seed, uint64_t offset, int N, int H, int W
     if (next_offset) *next_offset = g.offset;
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Record sampling with one counter block per image, the form a GPU thread
+ * per image can produce: image n's draws use offsets offset + 24n + k,
+ * k < 24 (a flip draw, a gate draw, ten attempts of two draws, two origin
+ * draws: at most 24).  The decisions are those of oracle_sample_aug_params;
+ * only the offset of each draw differs.
+ *
+ * exp of the log-aspect draw uses this file's own exp (below), written so that
+ * every step is a correctly rounded IEEE operation (multiply, add, fma, rint,
+ * exact scaling by 2^k): any implementation that takes the same steps gets
+ * the same bits, so the integer rectangle sizes cannot differ by a libm's
+ * last-place choice.                                                        */
+
+/* e^x for |x| < 80: Cody–Waite reduction x = k ln2 + r with ln2 split into a
+ * 24-bit head whose products with |k| < 2^9 are exact and a tail, |r| <= ln2/2,
+ * then the degree-7 Taylor polynomial of e^r (truncation below 5e-9 relative)
+ * in Horner form with fused multiply-adds, then multiplication by 2^k.     */
+float oracle_exp_f32(float x) {
+    const float inv_ln2 = 1.44269504088896341f;
+    const float ln2_hi = 0.693145751953125f;      /* 0x3f317200 */
+    const float ln2_lo = 1.42860682030941723212e-6f;
+    const float k = rintf(x * inv_ln2);
+    float r = fmaf(-k, ln2_hi, x);
+    r = fmaf(-k, ln2_lo, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    uint32_t bits = (uint32_t)((int)k + 127) << 23;   /* 2^k, a normal number for |k| < 126 */
+    float two_k;
+    memcpy(&two_k, &bits, sizeof two_k);
+    return p * two_k;
+}
+
+void oracle_exp_f32_array(const float* in, float* out, size_t n) {
+    for (size_t i = 0; i < n; ++i) out[i] = oracle_exp_f32(in[i]);
+}
+
+#define ORACLE_DRAWS_PER_IMAGE 24
+
+static float block_uniform(uint64_t seed, uint64_t base, int* k) {
+    float u = oracle_uniform01(seed, base + (uint64_t)(*k));
+    *k += 1;
+    return u;
+}
+
+int oracle_sample_aug_params_blocked(uint64_t seed, uint64_t offset, int N, int H, int W,
+                                     int flip_enabled, float flip_p,
+                                     int erase_enabled, float erase_p,
+                                     float scale_lo, float scale_hi,
+                                     float ratio_lo, float ratio_hi,
+                                     int32_t* out, uint64_t* next_offset) {
+    if (N < 0 || H < 1 || W < 1) return -1;
+    const float log_lo = logf(ratio_lo);
+    const float log_hi = logf(ratio_hi);
+    const float img_area = (float)H * (float)W;
+    for (int n = 0; n < N; ++n) {
+        const uint64_t base = offset + (uint64_t)n * ORACLE_DRAWS_PER_IMAGE;
+        int k = 0;
+        int32_t* a = out + (size_t)n * 5;
+        a[0] = 0; a[1] = 0; a[2] = 0; a[3] = 0; a[4] = 0;
+        if (flip_enabled) a[0] = (block_uniform(seed, base, &k) < flip_p) ? 1 : 0;
+        if (!erase_enabled || erase_p <= 0.0f) continue;
+        if (block_uniform(seed, base, &k) >= erase_p) continue;
+        for (int attempt = 0; attempt < 10; ++attempt) {
+            float ratio = scale_lo + block_uniform(seed, base, &k) * (scale_hi - scale_lo);
+            float area = ratio * img_area;
+            float log_ar = log_lo + block_uniform(seed, base, &k) * (log_hi - log_lo);
+            float ar = oracle_exp_f32(log_ar);
+            int eh = (int)roundf(sqrtf(area * ar));
+            int ew = (int)roundf(sqrtf(area / ar));
+            if (eh > 0 && ew > 0 && eh < H && ew < W) {
+                /* integer draw in [lo, hi]: lo + floor(u * (hi - lo + 1)), exact */
+                uint32_t ky = philox_bits24(seed, base + (uint64_t)k); k += 1;
+                uint32_t kx = philox_bits24(seed, base + (uint64_t)k); k += 1;
+                a[1] = (int32_t)(((uint64_t)ky * (uint64_t)(H - eh + 1)) >> 24);
+                a[2] = (int32_t)(((uint64_t)kx * (uint64_t)(W - ew + 1)) >> 24);
+                a[3] = eh;
+                a[4] = ew;
+                break;
+            }
+        }
+    }
+    if (next_offset) *next_offset = offset + (uint64_t)N * ORACLE_DRAWS_PER_IMAGE;
+    return 0;
+}

@@ -411,3 +411,50 @@ def test_crop_rejects_windows_outside_the_source():
         oracle.fused_norm_crop(src.reshape(-1), 192, 24, 8, 8, 1, 4, 4, 3, mean, std, np.array([[5, 0]]))
     with pytest.raises(ValueError):
         oracle.fused_norm_crop(src.reshape(-1), 192, 24, 8, 8, 1, 4, 4, 3, mean, std, np.array([[0, -1]]))
+
+
+# ------------------------------------------ per-image counter blocks ------
+
+def test_own_exp_is_within_two_ulp_of_the_exact_exp():
+    x = np.linspace(-20.0, 20.0, 400001, dtype=np.float32)
+    x = np.concatenate([x, np.log(np.float32([0.3, 3.3])), np.float32([0.0, -1e-8, 1e-8, 0.34657359])])
+    got = oracle.exp_f32(x).astype(np.float64)
+    exact = np.exp(x.astype(np.float64))
+    ulp = np.spacing(exact.astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(got - exact) / ulp) <= 2.0
+    assert oracle.exp_f32(np.float32([0.0]))[0] == 1.0
+
+
+def test_blocked_sampler_is_per_image():
+    """Image n's record depends only on (seed, offset + 24n): sampling a
+    suffix from its block offset gives the same records."""
+    a, nxt = oracle.sample_aug_params_blocked(5, 1000, 64, 224, 224, erase_p=0.7)
+    assert nxt == 1000 + 24 * 64
+    b, _ = oracle.sample_aug_params_blocked(5, 1000 + 24 * 40, 24, 224, 224, erase_p=0.7)
+    assert np.array_equal(a[40:], b)
+    c, _ = oracle.sample_aug_params_blocked(5, 1000, 64, 224, 224, erase_p=0.7)
+    assert np.array_equal(a, c)
+
+
+def test_blocked_sampler_distribution():
+    N = 20000
+    a, _ = oracle.sample_aug_params_blocked(2003, 0, N, 224, 224)
+    sigma = np.sqrt(0.25 / N)
+    assert abs(a[:, 0].mean() - 0.5) < 4 * sigma
+    erased = a[:, 3] > 0
+    assert abs(erased.mean() - 0.5) < 4 * sigma
+    area = (a[erased, 3] * a[erased, 4]) / (224.0 * 224.0)
+    assert 0.16 < area.mean() < 0.19
+    e = a[erased]
+    assert np.all(e[:, 1] + e[:, 3] <= 224) and np.all(e[:, 2] + e[:, 4] <= 224)
+    assert np.all(e[:, 3] < 224) and np.all(e[:, 4] < 224) and np.all(e[:, 1:3] >= 0)
+    ar = a[erased, 3] / a[erased, 4]
+    assert 0.8 < np.median(ar) < 1.25
+
+
+def test_blocked_and_sequential_samplers_agree_on_the_first_image():
+    # image 0 draws from offset, offset+1, ... in both forms
+    a, _ = oracle.sample_aug_params(9, 77, 1, 224, 224, erase_p=1.0)
+    b, _ = oracle.sample_aug_params_blocked(9, 77, 1, 224, 224, erase_p=1.0)
+    # the rectangle sizes may differ only through exp's last place; the flip and the gate agree
+    assert a[0, 0] == b[0, 0] and (a[0, 3] > 0) == (b[0, 3] > 0)

@@ -58,6 +58,8 @@ def parse():
                          "flips/erases, else the centre): tr_fused_norm_crop")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
     ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
+    ap.add_argument("--device-sampling", action="store_true",
+                    help="each step samples its records on the GPU (tr_sample_aug_params_device) before the kernel")
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -283,6 +285,11 @@ def run_ours(args, rank, local, world, pg):
         recs, offset = sample_records(cfg, 2000 + args.config, offset, trfn.tr_sample_aug_params)
         recs_all.append(recs)
         augs.append(torch.from_numpy(recs).to(dev) if recs is not None else None)
+    if args.device_sampling and (cfg["flip"] or cfg["erase"]):
+        # the records each step samples on the GPU (same seeds as launch(j) below)
+        import oracle
+        recs_all = [oracle.sample_aug_params_blocked(4000 + j, 0, N, H, W, flip=cfg["flip"], erase=cfg["erase"],
+                                                     erase_p=cfg["erase_p"])[0] for j in range(nsets)]
     alg_bytes = [algorithmic_bytes(cfg, r) for r in recs_all]
 
     stream = torch.cuda.Stream(device=dev)
@@ -290,7 +297,12 @@ def run_ours(args, rank, local, world, pg):
     # after another); --static measures the workspace-free schedule
     ws = None if args.static else torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
 
+    dev_sampling = args.device_sampling and (cfg["flip"] or cfg["erase"])
+
     def launch(j):
+        if dev_sampling:
+            trfn.tr_sample_aug_params_device(4000 + j, 0, N, H, W, augs[j], flip=cfg["flip"], erase=cfg["erase"],
+                                             erase_p=cfg["erase_p"], stream=stream)
         if S:
             trfn.tr_fused_norm_crop(srcs[j], S, S, S * C, S * S * C, dsts[j], N, H, W, C, mean, std, crop=crops[j],
                                     aug=augs[j], out_dtype=dt, layout=layout, stream=stream, variant=args.variant,
@@ -390,6 +402,8 @@ def run_ours(args, rank, local, world, pg):
             "launch": "CUDA graph of %d launches replayed; variant %d" % (G, args.variant),
             "schedule": "static (tr_fused_norm)" if args.static else "dynamic bands (tr_fused_norm_ws)",
             "source": ("%dx%d windows of %dx%d images (tr_fused_norm_crop)" % (H, W, S, S)) if S else "compact",
+            "records": "sampled on the GPU every step (tr_sample_aug_params_device)" if dev_sampling
+                       else "sampled on the host (tr_sample_aug_params), uploaded once",
             "parallelism": "replicas" if world > 1 else "single",
         },
         "hbm_gbs": achieved_gbs,
@@ -400,7 +414,7 @@ def run_ours(args, rank, local, world, pg):
             "algorithmic_bytes_per_launch": avg_bytes,
             "traffic": profiled_traffic(cfg["workload"]),
         },
-        "gpu_launches": K,
+        "gpu_launches": K * (2 if dev_sampling else 1),
         "captured_launches": int(captured),
         "parity_sample": parity,
     }

@@ -53,6 +53,8 @@ _SIGNATURES = {
     "tr_norm_preset": (_i, [_i, _fp, _fp, ctypes.POINTER(_i)]),
     "tr_sample_aug_params": (_i, [_u64, _u64, _i, _i, _i, _i, _f, _i, _f, _f, _f, _f, _f, _vp,
                                   ctypes.POINTER(_u64)]),
+    "tr_sample_aug_params_device": (_i, [_u64, _u64, _i, _i, _i, _i, _f, _i, _f, _f, _f, _f, _f, _vp,
+                                         ctypes.POINTER(_u64), _vp]),
     "tr_validate_aug_params": (_i, [_vp, _i, _i, _i, ctypes.POINTER(_i)]),
     "tr_ts_slot_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
     "tr_ts_create": (_i, [_i, ctypes.POINTER(_vp), ctypes.c_size_t, _vp, _vp, _vp, ctypes.POINTER(_vp)]),

@@ -132,6 +132,18 @@ def tr_sample_aug_params(seed, offset, N, H, W, flip=True, flip_p=0.5, erase=Tru
     return out, nxt.value
 
 
+def tr_sample_aug_params_device(seed, offset, N, H, W, out, flip=True, flip_p=0.5, erase=True, erase_p=0.5,
+                                scale=(0.02, 0.33), ratio=(0.3, 3.3), stream=None):
+    """Sample N records on the GPU into `out` (CUDA int32 (N, 5) tensor or a
+    device address); returns the next offset (offset + 24 N)."""
+    nxt = ctypes.c_uint64(0)
+    check(lib().tr_sample_aug_params_device(seed, offset, N, H, W, int(bool(flip)), flip_p, int(bool(erase)),
+                                            erase_p, scale[0], scale[1], ratio[0], ratio[1],
+                                            _dev_ptr(out, "out"), ctypes.byref(nxt), _stream_handle(stream)),
+          "tr_sample_aug_params_device")
+    return nxt.value
+
+
 def tr_validate_aug_params(records, H, W):
     """Returns -1 when every record is valid, else the first bad index."""
     rec = np.ascontiguousarray(records, dtype=np.int32).reshape(-1, 5)

@@ -229,6 +229,22 @@ int tr_sample_aug_params(uint64_t seed, uint64_t offset, int N, int H, int W,
                          float scale_lo, float scale_hi, float ratio_lo, float ratio_hi,
                          tr_aug_param* out_host, uint64_t* next_offset);
 
+/* tr_sample_aug_params_device — the same decisions made on the GPU, one
+ * thread per image, written to d_out (device, N records, 4-byte aligned) on
+ * `stream` in stream order.  Image n draws from its own counter block,
+ * offsets offset + 24n + k (24 = the most draws one image can take), so the
+ * batch needs no sequential pass; *next_offset (may be NULL) receives
+ * offset + 24N.  exp of the log-aspect draw is evaluated by fixed steps
+ * (Cody–Waite reduction, degree-7 Taylor polynomial, correctly rounded
+ * operations), so a CPU that takes the same steps reproduces the records bit
+ * for bit; the records differ from tr_sample_aug_params' (which draws
+ * sequentially) but follow the same distribution.  Errors as
+ * tr_sample_aug_params, TR_ERR_CUDA on a launch failure.                     */
+int tr_sample_aug_params_device(uint64_t seed, uint64_t offset, int N, int H, int W,
+                                int flip_enabled, float flip_p, int erase_enabled, float erase_p,
+                                float scale_lo, float scale_hi, float ratio_lo, float ratio_hi,
+                                tr_aug_param* d_out, uint64_t* next_offset, void* stream);
+
 /* Host check of N records: TR_OK when every rectangle is either "no erase"
  * (h <= 0 or w <= 0) or lies inside the H x W image; else
  * TR_ERR_INVALID_ARGUMENT with the first bad index in *bad_index (may be

@@ -270,7 +270,8 @@ struct TiledParams {
     unsigned int* ws;      // scheduling workspace (ticket counters, finished CTAs), or null
     int hints;             // tr_tune_tiled flags: bit 0 normal-priority loads, bit 1
                            // normal-priority stores, bit 2 evict-last stores (default:
-                           // both evict-first); bit 3 early dependent launch
+                           // both evict-first); bit 3 early dependent launch; bit 6 test
+                           // hook: unit 0's stage expects 16 bytes that never arrive
     float scale[4];
     float bias[4];
 };
@@ -360,13 +361,15 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     const int xs_hi = flip ? p.W - ecol_lo : ecol_hi;
     const uint32_t a_lo = ((uint32_t)xs_lo * C + 15u) & ~15u;
     const uint32_t a_hi = ((uint32_t)xs_hi * C) & ~15u;
+    // test hook for the bounded waits: unit 0's stage then never completes
+    const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;
     if (r_lo >= r_hi || a_hi <= a_lo) {
-        mbar_arrive_expect_tx(bar, total);
+        mbar_arrive_expect_tx(bar, total + missing);
         load_bytes(p, sdst, g, total, bar);
         return;
     }
     const uint32_t skipped = (uint32_t)(r_hi - r_lo) * (a_hi - a_lo);
-    mbar_arrive_expect_tx(bar, total - skipped);
+    mbar_arrive_expect_tx(bar, total - skipped + missing);
     uint32_t pos = 0;
     for (int r = r_lo; r < r_hi; ++r) {
         const uint32_t seg_end = (uint32_t)r * L + a_lo;
@@ -957,7 +960,7 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
-    p.hints = g_flags.load(std::memory_order_relaxed) & 15;
+    p.hints = g_flags.load(std::memory_order_relaxed) & 127;
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 

@@ -338,7 +338,11 @@ int tr_device_status(int* flags, int clear);
  *                    normal-priority stores, bit 2 evict-last stores (for a
  *                    consumer that reads the output from L2); bit 3 lets the
  *                    next kernel in the stream launch as soon as this one has
- *                    started (default: once its loads are issued).
+ *                    started (default: once its loads are issued); bit 6 is a
+ *                    test hook for the kernels' bounded waits: the first band
+ *                    of a batch waits for 16 bytes that never arrive, its waits
+ *                    run out after about a second, the launch returns with bit 0
+ *                    of the device status word set and its output incomplete.
  * Results do not depend on the geometry.  Errors: TR_ERR_INVALID_ARGUMENT
  * for negative values or stages of 1 or above 8.                            */
 int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags);

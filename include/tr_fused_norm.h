@@ -84,8 +84,9 @@ typedef struct tr_aug_param {
 
 /* Kernel selection, for tests and benchmarks.  AUTO picks TILED whenever its
  * preconditions hold (16-byte aligned src/dst, W*C a multiple of 16, and for
- * NCHW W*sizeof(out) a multiple of 16), else GENERIC.  Forcing TILED where
- * its preconditions fail returns TR_ERR_NOT_SUPPORTED.                      */
+ * NCHW W*sizeof(out) a multiple of 16) and the batch has at least 2^18 output
+ * elements (below that the per-element kernel finishes first), else GENERIC.
+ * Forcing TILED where its preconditions fail returns TR_ERR_NOT_SUPPORTED.  */
 typedef enum tr_variant {
     TR_VARIANT_AUTO = 0,
     TR_VARIANT_TILED = 1,     /* persistent CTAs, TMA bulk row-band staging, TMA bulk stores */

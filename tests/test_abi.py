@@ -100,10 +100,11 @@ def test_forced_tiled_on_unsupported_shape_is_not_supported():
 @pytest.mark.parametrize("shape,dt,lay,src,dst,want", [
     ((256, 224, 224, 3), 1, 0, 0x1000, 0x10000000, 1),
     ((256, 224, 224, 3), 0, 1, 0x1000, 0x10000000, 1),
-    ((16, 32, 32, 3), 0, 0, 0x1000, 0x10000000, 1),
+    ((16, 32, 32, 3), 0, 0, 0x1000, 0x10000000, 2),   # small batch: the per-element kernel
+    ((86, 32, 32, 3), 0, 0, 0x1000, 0x10000000, 1),   # 264,192 output elements
     ((200, 28, 28, 1), 0, 0, 0x1000, 0x10000000, 2),  # W*C = 28
-    ((4, 8, 12, 4), 1, 1, 0x1000, 0x10000000, 2),     # NCHW fp16 row of 24 bytes
-    ((4, 8, 12, 4), 0, 1, 0x1000, 0x10000000, 1),
+    ((128, 64, 12, 4), 1, 1, 0x1000, 0x10000000, 2),  # NCHW fp16 row of 24 bytes
+    ((128, 64, 12, 4), 0, 1, 0x1000, 0x10000000, 1),
     ((4, 8, 16, 3), 1, 0, 0x1008, 0x10000000, 2),     # src not 16-byte aligned
     ((4, 8, 16, 3), 1, 0, 0x1000, 0x10000004, 2),     # dst not 16-byte aligned
 ])

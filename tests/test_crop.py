@@ -73,9 +73,14 @@ def test_crop_windows_match_the_oracle(case, dt, layout):
     crop[0] = (0, 0)
     crop[-1] = (SH - H, SW - W)
     aug = synth.random_records(7 + N, N, H, W, allow_outside=True)
-    got = _run(buf, istr, rstr, SH, SW, N, H, W, C, crop, aug, dt, layout)
     ref = oracle.fused_norm_crop(buf, istr, rstr, SH, SW, N, H, W, C, MEAN[:C], STD[:C], crop, aug, dt, layout)
+    got = _run(buf, istr, rstr, SH, SW, N, H, W, C, crop, aug, dt, layout)
     assert_parity(got, ref, dt, str(case))
+    tma = (rp % 16 == 0 and ip % 16 == 0 and (SW * C) % 16 == 0 and (W * C) % 16 == 0 and
+           not (layout == NCHW and (W * (2 if dt == F16 else 4)) % 16))
+    if tma:   # the TMA tensor path, whatever AUTO picks for a batch this size
+        got = _run(buf, istr, rstr, SH, SW, N, H, W, C, crop, aug, dt, layout, trfn.VARIANT_TILED)
+        assert_parity(got, ref, dt, str(case) + " tiled")
 
 
 @pytest.mark.parametrize("case", CASES[:5])

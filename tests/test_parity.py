@@ -75,6 +75,10 @@ def test_shapes_with_coordinate_images(shape, dt, layout):
     std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
     aug = synth.random_records(31 + N * H + W, N, H, W, allow_outside=True)
     check_case(src, mean, std, aug, dt, layout)
+    # the same shapes through the tiled kernel wherever it applies (AUTO sends
+    # batches this small to the per-element kernel)
+    if trfn.tr_fused_norm_plan(0x1000, 0x100000, N, 4096, W, C, dt, layout) == TILED:
+        check_case(src, mean, std, aug, dt, layout, variant=TILED)
 
 
 @pytest.mark.parametrize("shape", SHAPES_TILED)
@@ -107,8 +111,9 @@ def test_erase_edge_cases():
     ], np.int32)
     for dt in (F32, F16):
         for layout in (NHWC, NCHW, NHWC4):
-            gpu, ref = check_case(src, IMNET[0], IMNET[1], aug, dt, layout)
-            assert np.array_equal(zero_mask(gpu, layout, dt), zero_mask(ref, layout, dt))
+            for variant in (TILED, GENERIC):
+                gpu, ref = check_case(src, IMNET[0], IMNET[1], aug, dt, layout, variant=variant)
+                assert np.array_equal(zero_mask(gpu, layout, dt), zero_mask(ref, layout, dt))
 
 
 def test_flip_positions_exact():
@@ -117,7 +122,7 @@ def test_flip_positions_exact():
     aug = np.zeros((N, 5), np.int32)
     aug[::2, 0] = 1
     mean, std = np.zeros(3, np.float32), np.full(3, 1 / 255, np.float32)  # value ~ byte
-    gpu, _ = check_case(src, mean, std, aug, F32, NHWC)
+    gpu, _ = check_case(src, mean, std, aug, F32, NHWC, variant=TILED)
     x = np.rint(gpu[..., 0]).astype(int)
     assert np.array_equal(x[0], np.broadcast_to(W - 1 - np.arange(W), (H, W)))
     assert np.array_equal(x[1], np.broadcast_to(np.arange(W), (H, W)))
@@ -156,6 +161,7 @@ def test_all_presets_full_domain():
                 assert np.max(np.abs(gpu.astype(np.float64) - ref)) <= tol
                 continue
             check_case(src, mean, std, None, dt, NHWC)
+            check_case(src, mean, std, None, dt, NHWC, variant=TILED)
 
 
 def test_device_status_is_clear():
@@ -197,7 +203,9 @@ def test_dynamic_schedule_on_small_shapes(shape):
     aug = synth.random_records(3 + N, N, H, W, allow_outside=True)
     ws = _workspace()
     for layout in (NHWC, NCHW, NHWC4):
-        check_case(src, mean, std, aug, F16, layout, workspace=ws.data_ptr())
+        if trfn.tr_fused_norm_plan(0x1000, 0x100000, N, 4096, W, C, F16, layout) != TILED:
+            continue   # e.g. NCHW rows of 24 bytes
+        check_case(src, mean, std, aug, F16, layout, variant=TILED, workspace=ws.data_ptr())
         assert int(ws.count_nonzero()) == 0
 
 

@@ -253,7 +253,8 @@ struct TiledParams {
     CUtensorMap tmap;      // crop sources: {16-byte chunk, chunk, row, image} of the source
     const int32_t* crop;   // crop sources: per-image window origin {top, left}, or null
     int src_H, src_W;      // crop sources: source image size
-    uint32_t in_pitch;     // bytes per row of an input stage (W*C; chunks*16 for crop sources)
+    uint32_t in_pitch;     // bytes per row of an input stage (W*C; chunks*chunk bytes for crop sources)
+    int chunk_shift;       // crop sources: log2 of the tensor's innermost chunk (4 or 5: 16 or 32 bytes)
     const uint8_t* src;
     uint8_t* dst;
     const tr_aug_param* aug;
@@ -340,10 +341,10 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
             cx = min(max(p.crop[2 * (size_t)b.n + 1], 0), p.src_W - p.W);
         }
         const int xb = cx * C;
-        rec->flags = flip | ((xb & 15) << 8);
+        rec->flags = flip | ((xb & ((1 << p.chunk_shift) - 1)) << 8);
         const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
         mbar_arrive_expect_tx(bar, (uint32_t)p.R * p.in_pitch);
-        tensor_g2s_4d(smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage, &p.tmap, 0, xb >> 4,
+        tensor_g2s_4d(smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage, &p.tmap, 0, xb >> p.chunk_shift,
                       cy + y_begin, b.n, bar, (p.hints & 1) ? policy_evict_last() : policy_evict_first());
         return;
     }
@@ -887,10 +888,14 @@ bool check_cuda(cudaError_t e, const char* what) {
     return false;
 }
 
-// The source of a crop launch as a 4-d tensor {16-byte chunk, chunk, row,
-// image} for TMA tensor copies; the box is {16, nch, R, 1}.  Reads outside the
-// tensor (rows past an image, chunks past a row) arrive as zeros.
-int encode_crop_map(CUtensorMap* map, const LaunchArgs& a, uint32_t nch, uint32_t R) {
+// The source of a crop launch as a 4-d tensor {chunk, chunk index, row,
+// image} for TMA tensor copies; the box is {chunk, nch, R, 1}.  Reads outside
+// the tensor (rows past an image, chunks past a row) arrive as zeros.  With
+// 32-byte chunks every request covers whole L2 sectors; without L2 promotion
+// DRAM is read in sectors, so a window row costs at most one partial sector
+// at each end.
+int encode_crop_map(CUtensorMap* map, const LaunchArgs& a, uint32_t chunk, uint32_t nch, uint32_t R,
+                    bool promote) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -905,13 +910,14 @@ int encode_crop_map(CUtensorMap* map, const LaunchArgs& a, uint32_t nch, uint32_
         set_last_error("cuTensorMapEncodeTiled unavailable", (int)cudaErrorNotSupported);
         return TR_ERR_CUDA;
     }
-    const cuuint64_t dims[4] = {16, (cuuint64_t)a.src_W * a.C / 16, (cuuint64_t)a.src_H, (cuuint64_t)a.N};
-    const cuuint64_t strides[3] = {16, (cuuint64_t)a.src_row_stride, (cuuint64_t)a.src_image_stride};
-    const cuuint32_t box[4] = {16, nch, R, 1};
+    const cuuint64_t dims[4] = {chunk, (cuuint64_t)a.src_W * a.C / chunk, (cuuint64_t)a.src_H, (cuuint64_t)a.N};
+    const cuuint64_t strides[3] = {chunk, (cuuint64_t)a.src_row_stride, (cuuint64_t)a.src_image_stride};
+    const cuuint32_t box[4] = {chunk, nch, R, 1};
     const cuuint32_t elem[4] = {1, 1, 1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(a.src), dims, strides,
                               box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              promote ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         set_last_error("cuTensorMapEncodeTiled", (int)cudaErrorInvalidValue);
         return TR_ERR_CUDA;
@@ -930,11 +936,15 @@ int launch_tiled(const LaunchArgs& a) {
     const int f16 = (a.out_dtype == TR_OUT_F16);
     const bool crop = a.crop_src;
     const size_t L = (size_t)a.W * a.C;
-    // crop sources: a box of R rows of `nch` 16-byte chunks covers a window
-    // that starts anywhere in its first chunk
-    const size_t nch = crop ? (L + 15 + 15) / 16 : 0;
+    // crop sources: a box of R rows of `nch` chunks covers a window that
+    // starts anywhere in its first chunk; 32-byte chunks when the source rows
+    // allow (tr_tune_tiled flags bit 8 forces 16, bit 9 asks for L2 promotion)
+    const int tflags = g_flags.load(std::memory_order_relaxed);
+    const int chunk_shift = (crop && ((size_t)a.src_W * a.C) % 32 == 0 && !(tflags & 256)) ? 5 : 4;
+    const size_t chunk = (size_t)1 << chunk_shift;
+    const size_t nch = crop ? (L + 2 * (chunk - 1)) / chunk : 0;
     if (crop && nch > 256) return TR_ERR_NOT_SUPPORTED;
-    const TiledPlan pl = plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, crop ? nch * 16 : 0,
+    const TiledPlan pl = plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, crop ? nch * chunk : 0,
                                     crop ? 16 : 0);
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 
@@ -942,9 +952,11 @@ int launch_tiled(const LaunchArgs& a) {
     p.crop = a.crop;
     p.src_H = crop ? a.src_H : a.H;
     p.src_W = crop ? a.src_W : a.W;
-    p.in_pitch = (uint32_t)(crop ? nch * 16 : L);
+    p.in_pitch = (uint32_t)(crop ? nch * chunk : L);
+    p.chunk_shift = chunk_shift;
     if (crop) {
-        const int rc = encode_crop_map(&p.tmap, a, (uint32_t)nch, (uint32_t)pl.R);
+        const int rc = encode_crop_map(&p.tmap, a, (uint32_t)chunk, (uint32_t)nch, (uint32_t)pl.R,
+                                       (tflags & 512) != 0);
         if (rc != TR_OK) return rc;
     }
     p.src = a.src;

@@ -343,7 +343,9 @@ int tr_device_status(int* flags, int clear);
  *                    test hook for the kernels' bounded waits: the first band
  *                    of a batch waits for 16 bytes that never arrive, its waits
  *                    run out after about a second, the launch returns with bit 0
- *                    of the device status word set and its output incomplete.
+ *                    of the device status word set and its output incomplete;
+ *                    crop sources: bit 8 reads 16-byte chunks even where 32-byte
+ *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion.
  * Results do not depend on the geometry.  Errors: TR_ERR_INVALID_ARGUMENT
  * for negative values or stages of 1 or above 8.                            */
 int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags);

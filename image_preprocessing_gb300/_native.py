@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(_HERE, "libtrfn.so")
 
 TR_OK = 0
 STATUS_NAMES = {0: "TR_OK", 1: "TR_ERR_INVALID_ARGUMENT", 2: "TR_ERR_NOT_SUPPORTED", 3: "TR_ERR_CUDA",
-                4: "TR_ERR_TIMEOUT", 5: "TR_ERR_DEVICE"}
+                4: "TR_ERR_TIMEOUT", 5: "TR_ERR_DEVICE", 6: "TR_END_OF_DATA"}
 
 
 class TrError(RuntimeError):
@@ -31,6 +31,16 @@ class TrError(RuntimeError):
 class AugParam(ctypes.Structure):
     _fields_ = [("flip", ctypes.c_int32), ("y0", ctypes.c_int32), ("x0", ctypes.c_int32),
                 ("h", ctypes.c_int32), ("w", ctypes.c_int32)]
+
+
+class StageSlot(ctypes.Structure):
+    _fields_ = [("image", ctypes.c_void_p), ("record", ctypes.c_void_p), ("sample", ctypes.c_longlong),
+                ("batch", ctypes.c_longlong), ("index", ctypes.c_int), ("zone", ctypes.c_int)]
+
+
+class StageBatch(ctypes.Structure):
+    _fields_ = [("images", ctypes.c_void_p), ("records", ctypes.c_void_p), ("batch", ctypes.c_longlong),
+                ("count", ctypes.c_int), ("zone", ctypes.c_int)]
 
 
 _lib = None
@@ -62,6 +72,16 @@ _SIGNATURES = {
                           ctypes.POINTER(ctypes.c_longlong)]),
     "tr_ts_submit_partial": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _fp, _fp, _i, _i,
                                   ctypes.POINTER(ctypes.c_longlong)]),
+    "tr_ts_submit_staged": (_i, [_vp, _vp, ctypes.POINTER(StageBatch), _i, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
+                                 _i, _i, ctypes.POINTER(ctypes.c_longlong)]),
+    "tr_stage_zone_bytes": (ctypes.c_size_t, [_i, _i, _i, _i]),
+    "tr_stage_create": (_i, [ctypes.POINTER(_vp), ctypes.c_size_t, _i, _i, _i, _i, _i, ctypes.POINTER(_vp)]),
+    "tr_stage_acquire": (_i, [_vp, ctypes.c_longlong, _i, ctypes.POINTER(StageSlot)]),
+    "tr_stage_commit": (_i, [_vp, ctypes.POINTER(StageSlot)]),
+    "tr_stage_close": (_i, [_vp, ctypes.c_longlong]),
+    "tr_stage_wait_readable": (_i, [_vp, _i, ctypes.POINTER(StageBatch)]),
+    "tr_stage_release": (_i, [_vp, ctypes.c_longlong]),
+    "tr_stage_destroy": (_i, [_vp]),
     "tr_ts_sync": (_i, [_vp, _i]),
     "tr_ts_destroy": (_i, [_vp]),
     "tr_device_status": (_i, [ctypes.POINTER(_i), _i]),

@@ -9,7 +9,7 @@ import ctypes
 import numpy as np
 
 from . import _native
-from ._native import AugParam, TrError, check, float_array, lib
+from ._native import AugParam, StageBatch, StageSlot, TrError, check, float_array, lib
 
 OUT_F32, OUT_F16 = 0, 1
 LAYOUT_NHWC, LAYOUT_NCHW, LAYOUT_NHWC4 = 0, 1, 2
@@ -215,6 +215,20 @@ class TransferStation:
               "tr_ts_submit_partial")
         return k.value
 
+    def submit_staged(self, staging, batch, d_dst, mean, std, n_batch=None, with_records=True, h_dst=None,
+                      out_dtype=OUT_F16, layout=LAYOUT_NHWC):
+        """Upload a batch handed out by staging.wait_readable() (a StageBatch),
+        padded to n_batch images, run the kernel, and give the host zone back
+        once its copies have finished."""
+        N = staging.N if n_batch is None else n_batch
+        _, H, W, C = staging.shape
+        k = ctypes.c_longlong(-1)
+        check(lib().tr_ts_submit_staged(self._h, staging._h, ctypes.byref(batch), int(bool(with_records)),
+                                        d_dst.data_ptr(), None if h_dst is None else h_dst.data_ptr(), N, H, W, C,
+                                        float_array(mean), float_array(std), _code(out_dtype, _DTYPES),
+                                        _code(layout, _LAYOUTS), ctypes.byref(k)), "tr_ts_submit_staged")
+        return k.value
+
     def sync(self, timeout_ms=-1):
         """True when all submitted work has finished; False on timeout."""
         rc = lib().tr_ts_sync(self._h, int(timeout_ms))
@@ -237,5 +251,103 @@ class TransferStation:
     def __del__(self):
         try:
             self.close()
+        except Exception:
+            pass
+
+
+STAGE_FAST, STAGE_REPRODUCIBLE = 0, 1
+END_OF_DATA = 6
+_STAGE_MODES = {"fast": STAGE_FAST, "reproducible": STAGE_REPRODUCIBLE}
+
+
+def tr_stage_zone_bytes(N, H, W, C):
+    return int(lib().tr_stage_zone_bytes(N, H, W, C))
+
+
+class Staging:
+    """tr_stage_* wrapper: two host zones that producer threads fill sample by
+    sample while the station uploads the other zone.
+
+    zones: two uint8 CPU tensors (pinned for asynchronous uploads) or numpy
+    arrays of tr_stage_zone_bytes(N,H,W,C) bytes each.  acquire() returns a
+    StageSlot (or None at the end of the data); image_view()/record_view()
+    give numpy views of the slot's place."""
+
+    def __init__(self, zones, N, H, W, C, mode=STAGE_FAST):
+        self._zones = zones  # keep the memory alive
+        ptrs = [z.data_ptr() if hasattr(z, "data_ptr") else z.ctypes.data for z in zones]
+        nbytes = min(z.numel() if hasattr(z, "numel") else z.nbytes for z in zones)
+        self._base = ptrs
+        self.N, self.shape = N, (N, H, W, C)
+        self.img_bytes = H * W * C
+        handle = ctypes.c_void_p(0)
+        check(lib().tr_stage_create((ctypes.c_void_p * 2)(*ptrs), nbytes, N, H, W, C,
+                                    _code(mode, _STAGE_MODES), ctypes.byref(handle)), "tr_stage_create")
+        self._h = handle
+
+    def acquire(self, sample=-1, timeout_ms=-1):
+        """A claimed StageSlot; None at the end of the data; raises TrError
+        (status TR_ERR_TIMEOUT) when the deadline passes."""
+        slot = StageSlot()
+        rc = lib().tr_stage_acquire(self._h, int(sample), int(timeout_ms), ctypes.byref(slot))
+        if rc == END_OF_DATA:
+            return None
+        check(rc, "tr_stage_acquire")
+        return slot
+
+    def commit(self, slot):
+        check(lib().tr_stage_commit(self._h, ctypes.byref(slot)), "tr_stage_commit")
+
+    def close(self, total_samples=-1):
+        check(lib().tr_stage_close(self._h, int(total_samples)), "tr_stage_close")
+
+    def wait_readable(self, timeout_ms=-1):
+        """The next StageBatch in order; None after the last batch of closed data."""
+        b = StageBatch()
+        rc = lib().tr_stage_wait_readable(self._h, int(timeout_ms), ctypes.byref(b))
+        if rc == END_OF_DATA:
+            return None
+        check(rc, "tr_stage_wait_readable")
+        return b
+
+    def release(self, batch):
+        check(lib().tr_stage_release(self._h, int(batch)), "tr_stage_release")
+
+    def _zone_offset(self, ptr, zone):
+        return int(ptr) - int(self._base[zone])
+
+    def image_view(self, slot_or_batch, count=1):
+        """numpy uint8 view of `count` images starting at a slot's (or batch's) place."""
+        zone = slot_or_batch.zone
+        ptr = slot_or_batch.image if isinstance(slot_or_batch, StageSlot) else slot_or_batch.images
+        z = self._zones[zone]
+        arr = z.numpy() if hasattr(z, "numpy") else z
+        off = self._zone_offset(ptr, zone)
+        _, H, W, C = self.shape
+        return arr[off:off + count * self.img_bytes].reshape(count, H, W, C)
+
+    def record_view(self, slot_or_batch, count=1):
+        """numpy int32 (count, 5) view of the records at a slot's (or batch's) place."""
+        zone = slot_or_batch.zone
+        ptr = slot_or_batch.record if isinstance(slot_or_batch, StageSlot) else slot_or_batch.records
+        z = self._zones[zone]
+        arr = z.numpy() if hasattr(z, "numpy") else z
+        off = self._zone_offset(ptr, zone)
+        return arr[off:off + count * 20].view(np.int32).reshape(count, 5)
+
+    def destroy(self):
+        if self._h:
+            h, self._h = self._h, None
+            check(lib().tr_stage_destroy(h), "tr_stage_destroy")
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+    def __del__(self):
+        try:
+            self.destroy()
         except Exception:
             pass

@@ -248,6 +248,7 @@ const char* tr_status_string(int status) {
     case TR_ERR_CUDA: return "CUDA error";
     case TR_ERR_TIMEOUT: return "timed out";
     case TR_ERR_DEVICE: return "device reported an error";
+    case TR_END_OF_DATA: return "end of data";
     default: return "unknown status";
     }
 }

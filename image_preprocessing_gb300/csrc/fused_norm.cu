@@ -742,6 +742,8 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
 struct DeviceInfo {
     int sm_count = 0;
     int smem_optin = 0;
+    int smem_per_sm = 0;      // shared memory of one SM
+    int smem_reserved = 0;    // shared memory the system reserves per resident CTA
 };
 
 DeviceInfo device_info(int dev) {
@@ -752,6 +754,8 @@ DeviceInfo device_info(int dev) {
     if (cache[dev].sm_count == 0) {
         cudaDeviceGetAttribute(&cache[dev].sm_count, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&cache[dev].smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&cache[dev].smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     }
     return cache[dev];
 }
@@ -813,10 +817,42 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Geometry knobs (tr_tune_tiled); 0 keeps the default.
 std::atomic<int> g_band_bytes{0}, g_stages{0}, g_ctas_per_sm{0}, g_flags{0};
 
-// pitch: bytes of one staged source row (W*C, or the crop box's chunks*16);
+// pitch: bytes of one staged source row (W*C, or the crop box's chunks*chunk);
 // slack: extra bytes after a stage's rows (crop consumers read one word past).
+TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch, size_t slack,
+                       int R_force);
+
 TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch = 0,
                      size_t slack = 0) {
+    return plan_tiled_r(H, W, C, f16, layout, smem_limit, pitch, slack, 0);
+}
+
+// CTAs of a plan that fit one SM's shared memory.
+int smem_residency(const TiledPlan& pl, int smem_per_sm, int reserved) {
+    return pl.ok ? (int)((size_t)smem_per_sm / (pl.smem + (size_t)reserved)) : 0;
+}
+
+// A crop box stages wider rows than the window (whole chunks), which can cost
+// one resident CTA per SM against the compact geometry; then take the largest
+// lower band height (down to half, divisors of H first) that restores it.
+TiledPlan plan_tiled_crop(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm,
+                          int reserved, size_t pitch, size_t slack) {
+    const TiledPlan pl = plan_tiled(H, W, C, f16, layout, smem_limit, pitch, slack);
+    if (!pl.ok || smem_per_sm <= 0 || g_band_bytes.load(std::memory_order_relaxed) > 0) return pl;
+    const int want = smem_residency(plan_tiled(H, W, C, f16, layout, smem_limit), smem_per_sm, reserved);
+    if (smem_residency(pl, smem_per_sm, reserved) >= want) return pl;
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int r = pl.R - 1; r >= (pl.R + 1) / 2 && r >= 1; --r) {
+            if (pass == 0 && H % r != 0) continue;
+            const TiledPlan q = plan_tiled_r(H, W, C, f16, layout, smem_limit, pitch, slack, r);
+            if (q.ok && q.stages == pl.stages && smem_residency(q, smem_per_sm, reserved) >= want) return q;
+        }
+    }
+    return pl;
+}
+
+TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch, size_t slack,
+                       int R_force) {
     TiledPlan pl;
     const int ob = f16 ? 2 : 4;
     const int P = group_pixels(C);
@@ -833,6 +869,7 @@ TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit, s
     for (int r = R; r >= (R + 1) / 2; --r) {
         if (H % r == 0) { R = r; break; }
     }
+    if (R_force > 0) R = std::min(R_force, H);
     while (R > 1 && (size_t)R * gpr >= 65536) --R;
     if ((size_t)R * gpr >= 65536) return pl;
     const int sknob = g_stages.load(std::memory_order_relaxed);
@@ -944,8 +981,9 @@ int launch_tiled(const LaunchArgs& a) {
     const size_t chunk = (size_t)1 << chunk_shift;
     const size_t nch = crop ? (L + 2 * (chunk - 1)) / chunk : 0;
     if (crop && nch > 256) return TR_ERR_NOT_SUPPORTED;
-    const TiledPlan pl = plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, crop ? nch * chunk : 0,
-                                    crop ? 16 : 0);
+    const TiledPlan pl = crop ? plan_tiled_crop(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm,
+                                                di.smem_reserved, nch * chunk, 16)
+                              : plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin);
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 
     TiledParams p;

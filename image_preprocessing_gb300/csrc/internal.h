@@ -58,4 +58,11 @@ void tune_tiled(int band_bytes, int stages, int ctas_per_sm, int flags);
 void count_launch();
 uint64_t launch_count();
 
+// Staging-area hooks for the station (staging.cpp): checks that b is a batch
+// of st handed out for N images of H*W*C bytes; counts a release queued on a
+// stream; and performs it (from a stream host function: no CUDA call).
+int stage_batch_ok(const tr_staging* st, const tr_stage_batch* b, int N, int H, int W, int C);
+void stage_release_queued(tr_staging* st);
+void stage_release_from_stream(tr_staging* st, long long batch);
+
 }  // namespace trfn

@@ -49,6 +49,22 @@ struct tr_transfer_station {
 
 namespace {
 
+// A staged zone to give back once its upload has finished (one per slot:
+// a slot holds at most one batch in flight).
+struct StagedRelease {
+    tr_staging* st = nullptr;
+    long long batch = 0;
+};
+void CUDART_CB release_staged(void* arg) {
+    StagedRelease* r = static_cast<StagedRelease*>(arg);
+    trfn::stage_release_from_stream(r->st, r->batch);
+    delete r;
+}
+
+}  // namespace
+
+namespace {
+
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // Slot layout: [N images][pad][N records][pad][filler image][pad][filler record].
@@ -175,7 +191,8 @@ namespace {
 // rest repeat the filler; see tr_ts_submit and tr_ts_submit_partial.
 int submit_impl(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_param* h_params, int n_valid,
                 void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean, const float* std,
-                int out_dtype, int out_layout, long long* batch_index) {
+                int out_dtype, int out_layout, long long* batch_index, tr_staging* stage = nullptr,
+                long long stage_batch = 0) {
     if (ts == nullptr || h_src == nullptr || d_dst == nullptr || N < 1 || n_valid < 1 || n_valid > N)
         return TR_ERR_INVALID_ARGUMENT;
     if (h_dst != nullptr && ts->d2h == nullptr) return TR_ERR_INVALID_ARGUMENT;
@@ -209,6 +226,21 @@ int submit_impl(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_para
                                         cudaMemcpyHostToDevice, ts->copy),
                         "cudaMemcpyAsync"))
         return TR_ERR_CUDA;
+    if (stage != nullptr) {
+        // the host zone is free again once the copies above have finished
+        StagedRelease* r = new (std::nothrow) StagedRelease{stage, stage_batch};
+        if (r == nullptr) return TR_ERR_INVALID_ARGUMENT;
+        trfn::stage_release_queued(stage);
+        const cudaError_t e = cudaLaunchHostFunc(ts->copy, release_staged, r);
+        if (e != cudaSuccess) {
+            // not queued: release now (the copies may still be reading the
+            // zone, so wait for them first)
+            cudaStreamSynchronize(ts->copy);
+            release_staged(r);
+            trfn::set_last_error("cudaLaunchHostFunc", (int)e);
+            return TR_ERR_CUDA;
+        }
+    }
     if (!ts->filler_saved && room_for_filler) {
         // the first batch's first image and record become the filler, in
         // both slots (the other slot is not in use before batch 1)
@@ -275,6 +307,16 @@ int tr_ts_submit_partial(tr_transfer_station* ts, const uint8_t* h_src, const tr
                          long long* batch_index) {
     return submit_impl(ts, h_src, h_params, n_valid, d_dst, h_dst, N, H, W, C, mean, std, out_dtype,
                        out_layout, batch_index);
+}
+
+int tr_ts_submit_staged(tr_transfer_station* ts, tr_staging* st, const tr_stage_batch* b, int with_records,
+                        void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean,
+                        const float* std, int out_dtype, int out_layout, long long* batch_index) {
+    if (ts == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    const int rc = trfn::stage_batch_ok(st, b, N, H, W, C);
+    if (rc != TR_OK) return rc;
+    return submit_impl(ts, b->images, with_records ? b->records : nullptr, b->count, d_dst, h_dst, N, H, W, C,
+                       mean, std, out_dtype, out_layout, batch_index, st, b->batch);
 }
 
 int tr_ts_sync(tr_transfer_station* ts, int timeout_ms) {

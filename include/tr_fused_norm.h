@@ -39,7 +39,8 @@ typedef enum tr_status {
     TR_ERR_NOT_SUPPORTED = 2,
     TR_ERR_CUDA = 3,          /* a CUDA runtime call failed; see tr_last_error_message() */
     TR_ERR_TIMEOUT = 4,       /* a bounded wait ran out (host event wait or device pipeline wait) */
-    TR_ERR_DEVICE = 5         /* a kernel reported an error through the device status word */
+    TR_ERR_DEVICE = 5,        /* a kernel reported an error through the device status word */
+    TR_END_OF_DATA = 6        /* staging: the data set was closed and has no further sample/batch */
 } tr_status;
 
 /* Output element type (article §六 "FP32 and FP16 output"). */
@@ -317,6 +318,109 @@ int tr_ts_sync(tr_transfer_station* ts, int timeout_ms);
 
 /* Waits (without limit) for submitted work, then destroys the events. */
 int tr_ts_destroy(tr_transfer_station* ts);
+
+/* ------------------------------------------------------------------------
+ * tr_staging — the host side of the station: preprocessing workers (host
+ * threads) write samples into two caller-owned host zones A/B, one batch per
+ * zone, while the station uploads the other zone (the TransferStation of
+ * "(10) Multi-threaded preprocessing, NUMA awareness, asynchronous double
+ * buffering", tech-renaissance.cn/blog/?p=481, §四: a buffer that holds a
+ * whole batch, or the last samples once the data has run out, becomes
+ * readable, and the workers switch to the other buffer; §四.2: two ways of
+ * placing samples).  Batch b lives in zone b % 2; a zone takes samples of one
+ * batch at a time and is given back (released) once that batch's upload has
+ * finished.  Every wait has a deadline.  Pure host code: no CUDA call except
+ * in tr_ts_submit_staged.  All functions are thread-safe; any number of
+ * producer threads and one consumer thread.
+ */
+typedef struct tr_staging tr_staging;
+
+typedef enum tr_stage_mode {
+    TR_STAGE_FAST = 0,         /* a shared counter hands out the next free place (§四.2) */
+    TR_STAGE_REPRODUCIBLE = 1  /* sample s goes to batch s / N, place s % N, so every run
+                                  lays batches out identically (§四.2)                     */
+} tr_stage_mode;
+
+/* A place claimed by a producer. */
+typedef struct tr_stage_slot {
+    uint8_t* image;            /* H*W*C bytes to write the sample's uint8 NHWC image to */
+    tr_aug_param* record;      /* its record (read by the station when asked to)        */
+    long long sample;          /* sample number = batch * N + index                     */
+    long long batch;
+    int index;                 /* place within the batch, 0..N-1                        */
+    int zone;                  /* 0 = A, 1 = B                                          */
+} tr_stage_slot;
+
+/* A readable batch handed to the consumer: places 0..count-1 of one zone. */
+typedef struct tr_stage_batch {
+    uint8_t* images;           /* count images of H*W*C bytes, back to back             */
+    tr_aug_param* records;     /* count records                                         */
+    long long batch;
+    int count;                 /* N, or 1..N for the last batch of closed data          */
+    int zone;
+} tr_stage_batch;
+
+/* Bytes one zone needs: [N images][pad][N records], the record array on a
+ * 256-byte boundary (the article's aligned zones, §四); 0 for a bad shape.   */
+size_t tr_stage_zone_bytes(int N, int H, int W, int C);
+
+/* zone: two non-overlapping host buffers of zone_bytes each (pinned memory,
+ * e.g. cudaHostAlloc, for asynchronous uploads; any host memory works, the
+ * upload is then synchronous), aligned to 4 bytes.  The staging area never
+ * reads or writes the zones itself.  Errors: TR_ERR_INVALID_ARGUMENT.       */
+int tr_stage_create(void* const zone[2], size_t zone_bytes, int N, int H, int W, int C, int mode,
+                    tr_staging** out);
+
+/* Producer: claim a place.  FAST mode ignores `sample` and takes the next
+ * sample number; REPRODUCIBLE mode claims sample `sample` (>= 0).  Waits
+ * until the zone of the sample's batch takes that batch (the consumer has
+ * released the batch two before it): TR_ERR_TIMEOUT after timeout_ms
+ * milliseconds (nothing claimed; timeout_ms < 0 waits without limit).
+ * TR_END_OF_DATA once the data is closed and the sample lies beyond it.
+ * TR_ERR_INVALID_ARGUMENT for a REPRODUCIBLE sample already claimed or whose
+ * batch was already consumed.                                                */
+int tr_stage_acquire(tr_staging* st, long long sample, int timeout_ms, tr_stage_slot* slot);
+
+/* Producer: the sample in `slot` is written.  The batch turns readable when
+ * its last place is committed.  TR_ERR_INVALID_ARGUMENT for a slot not
+ * claimed, or committed twice.                                               */
+int tr_stage_commit(tr_staging* st, const tr_stage_slot* slot);
+
+/* End of the data ("every worker reports that samples ran out", §四): the
+ * data set has total_samples samples, or, with -1, the ones claimed so far
+ * (FAST: handed out; REPRODUCIBLE: up to the highest claimed sample).  Places
+ * beyond it are refused (TR_END_OF_DATA); a short last batch becomes readable
+ * once its places are committed.  TR_ERR_INVALID_ARGUMENT if already closed
+ * or if total_samples is below a sample already claimed (FAST: differs from
+ * the number handed out).                                                    */
+int tr_stage_close(tr_staging* st, long long total_samples);
+
+/* Consumer: the next batch in order, once readable; TR_ERR_TIMEOUT after
+ * timeout_ms milliseconds (< 0: no limit); TR_END_OF_DATA after the last
+ * batch of closed data.  The zone stays the consumer's until released.      */
+int tr_stage_wait_readable(tr_staging* st, int timeout_ms, tr_stage_batch* batch);
+
+/* Consumer: give the zone of `batch` back to the producers (for batch + 2).
+ * TR_ERR_INVALID_ARGUMENT if that batch is not handed out.                   */
+int tr_stage_release(tr_staging* st, long long batch);
+
+/* Waits (without limit) for releases queued by tr_ts_submit_staged, then
+ * frees the staging area.                                                    */
+int tr_stage_destroy(tr_staging* st);
+
+/* tr_ts_submit of a staged batch: uploads b->count images (and, when
+ * with_records != 0, their records; else no flip and no erase) from the zone,
+ * pads a short batch to N with the station's filler (tr_ts_submit_partial),
+ * and releases the zone on the copy stream as soon as its host-to-device
+ * copies have finished (a host function queued on the copy stream; it takes
+ * the staging area's lock and makes no CUDA call).  Other arguments and
+ * errors as tr_ts_submit; TR_ERR_INVALID_ARGUMENT when b is not a batch of
+ * st handed out for N images of H*W*C bytes.  After a failed call the zone
+ * may still be handed out: tr_ts_sync, then tr_stage_release (which answers
+ * TR_ERR_INVALID_ARGUMENT if the queued release already gave it back).      */
+int tr_ts_submit_staged(tr_transfer_station* ts, tr_staging* st, const tr_stage_batch* b, int with_records,
+                        void* d_dst, void* h_dst, int N, int H, int W, int C, const float* mean,
+                        const float* std, int out_dtype, int out_layout, long long* batch_index);
 
 /* ------------------------------------------------------------------------
  * Diagnostics.

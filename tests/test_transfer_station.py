@@ -151,3 +151,94 @@ def test_first_batch_short_pads_with_its_own_first_image():
     with pytest.raises(trfn.TrError):
         ts.submit_partial(torch.from_numpy(np.repeat(short, N + 1, axis=0)).pin_memory(), N, d, MEAN, STD)
     ts.close()
+
+
+def _staged_pipeline(mode, N, H, W, C, T, producers, dt=trfn.OUT_F16):
+    """Producer threads write samples into pinned host zones (tr_stage_*); the
+    consumer submits each readable batch to the station, which gives the zone
+    back once its upload has finished.  Returns per batch (place -> sample,
+    count, device output)."""
+    import threading
+    import torch
+    data = synth.pixels_uniform(900, T, H, W, C)
+    recs = oracle.sample_aug_params(901, 0, T, H, W)[0]
+    nb = trfn.tr_stage_zone_bytes(N, H, W, C)
+    zones = [torch.zeros(nb, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    st = trfn.Staging(zones, N, H, W, C, mode=mode)
+    ts, _ = _station(N, H, W, C)
+    lock = threading.Lock()
+    source = iter(range(T))
+    placed = {}            # sample number (place) -> data item
+    errors = []
+
+    def producer(w):
+        try:
+            mine = iter(range(w, T, producers))
+            while True:
+                if mode == trfn.STAGE_FAST:
+                    with lock:
+                        item = next(source, None)
+                    if item is None:
+                        return
+                    slot = st.acquire(timeout_ms=30000)
+                else:
+                    item = next(mine, None)
+                    if item is None:
+                        return
+                    slot = st.acquire(item, timeout_ms=30000)
+                st.image_view(slot)[0] = data[item]
+                st.record_view(slot)[0] = recs[item]
+                with lock:
+                    placed[slot.sample] = item
+                st.commit(slot)
+        except Exception as e:  # pragma: no cover
+            errors.append(e)
+
+    threads = [threading.Thread(target=producer, args=(w,)) for w in range(producers)]
+    for t in threads:
+        t.start()
+    tdt = torch.float16 if dt == trfn.OUT_F16 else torch.float32
+    outs = []
+    closed = False
+    while True:
+        if not closed and not any(t.is_alive() for t in threads):
+            st.close()
+            closed = True
+        try:
+            b = st.wait_readable(timeout_ms=50)
+        except trfn.TrError as e:
+            assert e.status == 4
+            continue
+        if b is None:
+            break
+        d = torch.empty((N, H, W, C), dtype=tdt, device="cuda")
+        assert ts.submit_staged(st, b, d, MEAN, STD, out_dtype=dt) == b.batch
+        outs.append((b.batch, b.count, d))
+    assert ts.sync(30000)
+    for t in threads:
+        t.join(10)
+    assert not errors, errors
+    ts.close()
+    st.destroy()
+    return data, recs, placed, outs
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_staged_batches_match_the_oracle(mode):
+    """Every place of every batch, including the short last batch's filler
+    images (the first image and record of the first batch), equals the
+    oracle on the sample the producers put there."""
+    N, H, W, C = 8, 32, 48, 3
+    T = 5 * N + 3
+    data, recs, placed, outs = _staged_pipeline(mode, N, H, W, C, T, producers=4)
+    assert [o[0] for o in outs] == list(range(6))
+    assert [o[1] for o in outs] == [N] * 5 + [3]
+    assert sorted(placed) == list(range(T)) and sorted(placed.values()) == list(range(T))
+    if mode == 1:
+        assert all(placed[s] == s for s in placed)             # reproducible: sample s at place s
+    filler = placed[0]
+    for b, count, d in outs:
+        items = [placed[b * N + i] if i < count else filler for i in range(N)]
+        ref = oracle.fused_norm(data[items], MEAN, STD, recs[items], out_dtype=trfn.OUT_F16)
+        got = d.cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+        assert_parity(got, ref, trfn.OUT_F16, "staged batch %d" % b)

@@ -54,6 +54,16 @@ def _dev_ptr(t, what):
     return t.data_ptr()
 
 
+def _workspace_ptr(ws, where):
+    """Device address of a scheduling workspace; a tensor must hold at least
+    tr_workspace_bytes() bytes (the C ABI takes the pointer alone)."""
+    if ws is None or isinstance(ws, int):
+        return ws
+    if ws.numel() * ws.element_size() < tr_workspace_bytes():
+        raise TrError(1, where, "workspace must hold at least %d bytes" % tr_workspace_bytes())
+    return _dev_ptr(ws, where)
+
+
 def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOUT_NHWC, stream=None,
                   variant=VARIANT_AUTO, shape=None, workspace=None):
     """Enqueue the fused step: src uint8 (N,H,W,C) CUDA tensor -> dst.
@@ -80,7 +90,7 @@ def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOU
     m, s = float_array(mean), float_array(std)
     rc = lib().tr_fused_norm_ws(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
                                 _dev_ptr(aug, "aug"), dt, lay, _stream_handle(stream), int(variant),
-                                _dev_ptr(workspace, "workspace"))
+                                _workspace_ptr(workspace, "tr_fused_norm"))
     check(rc, "tr_fused_norm")
 
 
@@ -96,7 +106,7 @@ def tr_fused_norm_crop(src, src_H, src_W, row_stride, image_stride, dst, N, H, W
     rc = lib().tr_fused_norm_crop(_dev_ptr(src, "src"), src_H, src_W, row_stride, image_stride,
                                   _dev_ptr(crop, "crop"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
                                   _dev_ptr(aug, "aug"), _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS),
-                                  _stream_handle(stream), int(variant), _dev_ptr(workspace, "workspace"))
+                                  _stream_handle(stream), int(variant), _workspace_ptr(workspace, "tr_fused_norm_crop"))
     check(rc, "tr_fused_norm_crop")
 
 

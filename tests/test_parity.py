@@ -252,3 +252,16 @@ def test_launches_complete_quickly_and_leave_no_status():
         torch.cuda.synchronize()
         assert (time.perf_counter() - t0) / 20 < 0.05
     assert trfn.tr_device_status() == 0
+
+
+def test_binding_rejects_short_workspace_tensor():
+    """The C ABI takes the workspace as a bare pointer; the binding checks a
+    tensor's size before handing it over, so nothing is launched."""
+    import torch
+    src = torch.zeros((4, 16, 16, 3), dtype=torch.uint8, device="cuda")
+    dst = torch.empty((4, 16, 16, 3), dtype=torch.float16, device="cuda")
+    before = trfn.tr_launch_count()
+    with pytest.raises(trfn.TrError):
+        trfn.tr_fused_norm(src, dst, [0.5] * 3, [0.25] * 3, workspace=torch.zeros(256, dtype=torch.uint8,
+                                                                                   device="cuda"))
+    assert trfn.tr_launch_count() == before

@@ -432,9 +432,11 @@ int tr_device_status(int* flags, int clear);
 
 /* Geometry of the TILED kernel, for tuning on a given device (process-wide;
  * 0 keeps the default for that knob):
- *   band_bytes       source bytes per row band (default: about 32 KB of source
- *                    plus output per band; the band height is the largest
- *                    divisor of H near the target, else the target),
+ *   band_bytes       source bytes per row band (default: about 32 KB of
+ *                    output per band; the band height is the largest divisor
+ *                    of H near the target, else the target; crop sources may
+ *                    lower it so that as many CTAs fit an SM as for a compact
+ *                    source),
  *   stages           shared-memory input stages, 2..8 (default 3 for bands
  *                    above 8 KB of source, else 4),
  *   max_ctas_per_sm  cap on resident CTAs per SM (default: occupancy limit),
@@ -443,7 +445,10 @@ int tr_device_status(int* flags, int clear);
  *                    normal-priority stores, bit 2 evict-last stores (for a
  *                    consumer that reads the output from L2); bit 3 lets the
  *                    next kernel in the stream launch as soon as this one has
- *                    started (default: once its loads are issued); bit 6 is a
+ *                    started (default: once its loads are issued); bit 4
+ *                    lets a CTA exit once its last store has read shared
+ *                    memory instead of once the store has completed (the
+ *                    grid's completion still covers the writes); bit 6 is a
  *                    test hook for the kernels' bounded waits: the first band
  *                    of a batch waits for 16 bytes that never arrive, its waits
  *                    run out after about a second, the launch returns with bit 0

@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-pipeline", action="store_true",
+                    help="skip the 64-batch pinned-host stream (reported under 'pipeline')")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     return ap.parse_args()
@@ -378,6 +380,9 @@ def run_ours(args, rank, local, world, pg):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg)
+    pipeline = None
+    if not args.no_pipeline and args.config == 3 and not S and not args.batch and not args.layout:
+        pipeline = run_pipeline(dev, rank, pg)
 
     value = aggregate_images_per_s(world, N, K, ms_max)
     res = {
@@ -422,6 +427,8 @@ def run_ours(args, rank, local, world, pg):
         res["clocks"] = clk
     if e2e is not None:
         res["e2e"] = e2e
+    if pipeline is not None:
+        res["pipeline"] = pipeline
     return res
 
 
@@ -501,6 +508,105 @@ def run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg):
             "path": "tr_ts_submit: pinned host u8 + records -> device slot A/B (copy stream) -> kernel "
                     "(compute stream) -> pinned host output (d2h stream)",
             "link_gbs": (h2d + d2h) * K / sec / 1e9}
+
+
+def run_pipeline(dev, rank, pg):
+    """The 64-batch stream: 64 distinct pinned host batches of 256x224x224x3
+    uint8 (and their records, flip 0.5, erase 0.5, Philox offsets running on
+    across batches) go through the transfer station to fp16 NHWC on the
+    device; the copy of batch k+1 (copy stream) overlaps the kernel on batch
+    k (compute stream).  Outputs stay on the device (two alternating output
+    buffers).  Reports images/s from the first copy to the last kernel (CUDA
+    events), a lone 38.5 MB pinned copy, the kernel alone, and the overlap
+    efficiency (T_copy + T_kernel) / T_pipelined over the 64 batches."""
+    import torch
+    import image_preprocessing_gb300 as trfn
+    from image_preprocessing_gb300 import synth
+    cfg = synth.CONFIGS[5]
+    B, N, H, W, C = cfg["batches"], cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    # uniform pixels (seed 5000 + b): the copy and the kernel do not depend on
+    # pixel values, and 64 Gaussian batches take minutes to draw on the host
+    h_src = [torch.from_numpy(synth.pixels_uniform(5000 + b + 7919 * rank, N, H, W, C)).pin_memory()
+             for b in range(B)]
+    h_par, offset = [], 0
+    for b in range(B):
+        recs, offset = trfn.tr_sample_aug_params(2005, offset, N, H, W, flip=True, erase=True,
+                                                 erase_p=cfg["erase_p"])
+        h_par.append(torch.from_numpy(recs).pin_memory())
+    slot_bytes = trfn.tr_ts_slot_bytes(N, H, W, C)
+    slots = [torch.empty(slot_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_out = [torch.empty((N, H, W, C), dtype=torch.float16, device=dev) for _ in range(2)]
+    s_copy, s_comp = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def events():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    # every host batch is copied once before anything is timed: the first
+    # device access to freshly pinned pages costs several times a later one,
+    # and a running pipeline reuses its pinned buffers
+    img_bytes = N * H * W * C
+    with torch.cuda.stream(s_copy):
+        for b in range(B):
+            slots[b & 1][:img_bytes].copy_(h_src[b].view(-1), non_blocking=True)
+    torch.cuda.synchronize()
+    # a lone pinned host-to-device copy of one batch (8 batches, averaged)
+    e0, e1 = events()
+    with torch.cuda.stream(s_copy):
+        e0.record(s_copy)
+        for b in range(8):
+            slots[b & 1][:img_bytes].copy_(h_src[b].view(-1), non_blocking=True)
+        e1.record(s_copy)
+    e1.synchronize()
+    t_copy = e0.elapsed_time(e1) / 8 / 1e3
+    # the kernel alone on a slot, dynamically scheduled as in the station (16
+    # launches, averaged)
+    d_par = h_par[0].to(dev)
+    src0 = slots[0][:img_bytes].view(N, H, W, C)
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
+    e0, e1 = events()
+    with torch.cuda.stream(s_comp):
+        trfn.tr_fused_norm(src0, d_out[0], mean, std, d_par, out_dtype=trfn.OUT_F16, stream=s_comp, workspace=ws)
+        e0.record(s_comp)
+        for k in range(16):
+            trfn.tr_fused_norm(src0, d_out[k & 1], mean, std, d_par, out_dtype=trfn.OUT_F16, stream=s_comp,
+                               workspace=ws)
+        e1.record(s_comp)
+    e1.synchronize()
+    t_kernel = e0.elapsed_time(e1) / 16 / 1e3
+    # the pipelined stream
+    ts = trfn.TransferStation(dev.index, slots, s_copy, s_comp, None)
+    for b in range(2):   # warm-up: the station's first batch also saves its filler
+        ts.submit(h_src[b], d_out[b & 1], mean, std, h_params=h_par[b], out_dtype=trfn.OUT_F16)
+    assert ts.sync(60000)
+    barrier(pg)
+    torch.cuda.synchronize()
+    e0, e1 = events()
+    e0.record(s_copy)
+    launches = trfn.tr_launch_count()
+    for b in range(B):
+        ts.submit(h_src[b], d_out[b & 1], mean, std, h_params=h_par[b], out_dtype=trfn.OUT_F16)
+    e1.record(s_comp)
+    launches = trfn.tr_launch_count() - launches
+    e1.synchronize()
+    assert ts.sync(60000)
+    ts.close()
+    t_pipe = max_over_ranks(pg, e0.elapsed_time(e1) / 1e3, dev)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    h2d = img_bytes + N * 20
+    return {
+        "workload": cfg["name"], "batches": B, "images_per_s": world * B * N / t_pipe,
+        "ms_pipelined": t_pipe * 1e3, "h2d_gbs_lone_copy": img_bytes / t_copy / 1e9,
+        "us_copy_per_batch": t_copy * 1e6, "us_kernel_per_batch": t_kernel * 1e6,
+        "overlap_efficiency": B * (t_copy + t_kernel) / t_pipe,
+        "overlap_efficiency_bound": (t_copy + t_kernel) / max(t_copy, t_kernel),
+        "h2d_gbs_pipelined": B * h2d / t_pipe / 1e9,
+        "h2d_bytes_per_batch": h2d, "gpu_launches": int(launches),
+        "path": "tr_ts_submit: pinned host u8 + records -> device slot A/B (copy stream) -> kernel "
+                "(compute stream); outputs stay on the device",
+        "pixels": "uniform (seed 5000 + b)",
+    }
 
 
 # ------------------------------------------------------------- oracle -----

@@ -67,11 +67,14 @@ namespace {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Slot layout: [N images][pad][N records][pad][filler image][pad][filler record].
-// The filler is the first image (and record) of the first batch, kept for
-// padding short batches (the article's incomplete-batch filling, §四.1).
+// Slot layout: [N images][pad][N records][pad][filler image][pad][filler
+// record][pad][scheduling workspace].  The filler is the first image (and
+// record) of the first batch, kept for padding short batches (the article's
+// incomplete-batch filling, §四.1).  The workspace (tr_workspace_bytes) lets
+// the station's kernels hand out bands dynamically; the kernels run one after
+// another on the compute stream, so slot A's workspace serves them all.
 struct SlotLayout {
-    size_t img, images, records, filler, filler_rec, total;
+    size_t img, images, records, filler, filler_rec, ws, total;
 };
 
 SlotLayout slot_layout(int N, int H, int W, int C) {
@@ -81,7 +84,8 @@ SlotLayout slot_layout(int N, int H, int W, int C) {
     l.records = align256((size_t)N * l.img);
     l.filler = l.records + align256((size_t)N * sizeof(tr_aug_param));
     l.filler_rec = l.filler + align256(l.img);
-    l.total = l.filler_rec + align256(sizeof(tr_aug_param));
+    l.ws = l.filler_rec + align256(sizeof(tr_aug_param));
+    l.total = l.ws + align256(tr_workspace_bytes());
     return l;
 }
 
@@ -201,7 +205,8 @@ int submit_impl(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_para
     int rc = tr_fused_norm(nullptr, nullptr, 0, H, W, C, mean, std, nullptr, out_dtype, out_layout, nullptr);
     if (rc != TR_OK) return rc;
     const SlotLayout l = slot_layout(N, H, W, C);
-    const bool room_for_filler = l.total <= ts->slot_bytes;
+    const bool room_for_filler = l.ws <= ts->slot_bytes;
+    const bool room_for_ws = l.total <= ts->slot_bytes;
     if (l.filler > ts->slot_bytes && (h_params != nullptr || n_valid < N)) return TR_ERR_INVALID_ARGUMENT;
     if (l.records > ts->slot_bytes) return TR_ERR_INVALID_ARGUMENT;
     if (n_valid < N && !room_for_filler) return TR_ERR_INVALID_ARGUMENT;
@@ -272,7 +277,15 @@ int submit_impl(tr_transfer_station* ts, const uint8_t* h_src, const tr_aug_para
     if (ts->d2h_used[s] &&
         !ok(cudaStreamWaitEvent(ts->compute, ts->d2h_done[s], 0), "cudaStreamWaitEvent"))
         return TR_ERR_CUDA;
-    rc = tr_fused_norm(slot, d_dst, N, H, W, C, mean, std, d_params, out_dtype, out_layout, ts->compute);
+    void* ws = nullptr;
+    if (room_for_ws) {
+        // cleared before every kernel: a kernel leaves it zero, except one
+        // whose bounded waits ran out, and a batch costs far more than 2 KB
+        ws = ts->slot[0] + l.ws;
+        if (!ok(cudaMemsetAsync(ws, 0, tr_workspace_bytes(), ts->compute), "cudaMemsetAsync")) return TR_ERR_CUDA;
+    }
+    rc = tr_fused_norm_ws(slot, d_dst, N, H, W, C, mean, std, d_params, out_dtype, out_layout, ts->compute,
+                          TR_VARIANT_AUTO, ws);
     if (rc != TR_OK) return rc;
     if (!ok(cudaEventRecord(ts->done[s], ts->compute), "cudaEventRecord")) return TR_ERR_CUDA;
     ts->done_used[s] = true;

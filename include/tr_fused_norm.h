@@ -266,8 +266,11 @@ int tr_validate_aug_params(const tr_aug_param* host_params, int N, int H, int W,
 typedef struct tr_transfer_station tr_transfer_station;
 
 /* Bytes one device slot needs for a batch of N images: the slot layout is
- * [N images][N records][filler image][filler record], each zone starting on a
- * 256-byte boundary (the article's [labels][padding][image] zones, §四).     */
+ * [N images][N records][filler image][filler record][scheduling workspace],
+ * each zone starting on a 256-byte boundary (the article's
+ * [labels][padding][image] zones, §四).  Slots without room for the filler
+ * zones cannot take short batches or records; slots without room for the
+ * workspace run the statically scheduled kernel.                          */
 size_t tr_ts_slot_bytes(int N, int H, int W, int C);
 
 /*   device        CUDA device ordinal the slots and streams belong to.

@@ -172,10 +172,10 @@ def test_validate_aug_params():
 
 
 def test_slot_bytes_layout():
-    # [images][records][filler image][filler record], each zone on a 256-byte boundary
+    # [images][records][filler image][filler record][workspace], each zone on a 256-byte boundary
     img = 224 * 224 * 3
-    assert trfn.tr_ts_slot_bytes(256, 224, 224, 3) == 256 * img + 5120 + img + 256
-    assert trfn.tr_ts_slot_bytes(3, 5, 7, 3) == 512 + 256 + 256 + 256
+    assert trfn.tr_ts_slot_bytes(256, 224, 224, 3) == 256 * img + 5120 + img + 256 + 2048
+    assert trfn.tr_ts_slot_bytes(3, 5, 7, 3) == 512 + 256 + 256 + 256 + 2048
     assert trfn.tr_ts_slot_bytes(-1, 5, 7, 3) == 0
 
 

@@ -102,7 +102,8 @@ def test_submit_rejects_bad_arguments():
     h_out = torch.zeros((N, H, W, C), dtype=torch.float16).pin_memory()
     with pytest.raises(trfn.TrError):
         ts.submit(h_src, d_out, MEAN, STD, h_dst=h_out)   # no result stream was given
-    big = torch.zeros((N + 5, H, W, C), dtype=torch.uint8).pin_memory()
+    big = torch.zeros((10 * N, H, W, C), dtype=torch.uint8).pin_memory()
+    assert 10 * N * H * W * C > trfn.tr_ts_slot_bytes(N, H, W, C)
     with pytest.raises(trfn.TrError):
         ts.submit(big, d_out, MEAN, STD)                   # does not fit a slot
     ts.close()

@@ -611,6 +611,24 @@ def run_pipeline(dev, rank, pg):
 
 # ------------------------------------------------------------- oracle -----
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (model name, else the Arm part)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return "unknown"
+    arm_parts = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd0c": "Neoverse N1"}
+    for line in info.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    for line in info.splitlines():
+        if line.lower().startswith("cpu part"):
+            part = line.split(":", 1)[1].strip().lower()
+            return "Arm part %s (%s)" % (part, arm_parts.get(part, "unlisted"))
+    return "unknown"
+
+
 def oracle_images_per_s(cfg, seconds, threads=None):
     """The oracle as it stands on a bounded sample of the workload, split by
     image over host threads (ctypes releases the GIL).  Returns
@@ -704,8 +722,10 @@ def main():
         if not args.no_cpu:
             cfg = workload(args)
             v, threads, sample = oracle_images_per_s(cfg, args.cpu_seconds)
+            v1, _, sample1 = oracle_images_per_s(cfg, max(1.0, args.cpu_seconds / 4), threads=1)
             res["cpu_baseline"] = {"value": v, "unit": "images/s", "cores": threads, "kind": "oracle",
-                                   "sample": sample}
+                                   "sample": sample, "single_core": {"value": v1, "sample": sample1},
+                                   "cpu_model": cpu_model()}
         print(json.dumps(res), flush=True)
     if pg is not None:
         pg.destroy_process_group()

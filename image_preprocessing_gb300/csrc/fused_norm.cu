@@ -84,6 +84,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -380,6 +384,43 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     if (total > pos) load_bytes(p, sdst + pos, g + pos, total - pos, bar);
 }
 
+// Early form of issue_unit for a CTA's first unit (compact sources): the
+// whole band is requested before the unit's record has arrived; only the
+// expected byte count is posted, so the stage cannot complete before
+// publish_unit has written the record and arrived.
+template <int C>
+__device__ __forceinline__ void issue_unit_uncut(const TiledParams& p, int u, int s, uint8_t* smem) {
+    const Band b = band_of(p, u);
+    const uint32_t L = (uint32_t)p.W * C;
+    const uint32_t total = (uint32_t)b.rows * L;
+    const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
+    const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;   // bounded-wait test hook
+    mbar_expect_tx(bar, total + missing);
+    load_bytes(p, smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage,
+               p.src + ((size_t)b.n * p.H + b.y_begin) * L, total, bar);
+}
+
+// Writes unit u's record (flip, clipped erase rectangle) for stage s and
+// arrives on full[s] (release: consumers that see the phase see the record).
+__device__ __forceinline__ void publish_unit(const TiledParams& p, int u, int s, uint8_t* smem,
+                                             const tr_aug_param& a) {
+    const Band b = band_of(p, u);
+    int erow_lo = 0, erow_hi = 0, ecol_lo = 0, ecol_hi = 0;
+    if (a.h > 0 && a.w > 0) {
+        const long long y0 = a.y0, x0 = a.x0;
+        const long long ylo = max(y0, 0ll), yhi = min(y0 + a.h, (long long)p.H);
+        const long long xlo = max(x0, 0ll), xhi = min(x0 + a.w, (long long)p.W);
+        if (ylo < yhi && xlo < xhi) {
+            erow_lo = (int)ylo; erow_hi = (int)yhi;
+            ecol_lo = (int)xlo; ecol_hi = (int)xhi;
+        }
+    }
+    UnitRec* rec = reinterpret_cast<UnitRec*>(smem + kRecOffset) + s;
+    rec->n = b.n; rec->y_begin = b.y_begin; rec->rows = b.rows; rec->flags = (a.flip != 0);
+    rec->erow_lo = erow_lo; rec->erow_hi = erow_hi; rec->ecol_lo = ecol_lo; rec->ecol_hi = ecol_hi;
+    mbar_arrive(smem_u32(smem) + 8u * (uint32_t)s);
+}
+
 template <int C, int OUT_F16, int LAYOUT>
 __device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout, int r, int gx,
                                             const float (&v)[Group<C>::kBytes]) {
@@ -594,7 +635,11 @@ __global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ Tile
             const int n_dyn = max(0, p.num_units - S * G);   // units handed out by tickets
             int u = blockIdx.x;
             tr_aug_param a = {0, 0, 0, 0, 0};
-            if (p.aug != nullptr) a = p.aug[u / p.bands];
+            // the first unit's band is requested before its record has
+            // arrived (its erased span is then read too); measured 0.9 %
+            // faster at 256x224x224x3 than waiting for the record
+            const bool early0 = !CROP && !(p.hints & 32) && u < p.num_units;
+            if (p.aug != nullptr && !early0) a = p.aug[u / p.bands];
             int j = 0;
             bool ok = true;
             for (;; ++j) {
@@ -609,7 +654,13 @@ __global__ void __launch_bounds__(256) tiled_kernel(const __grid_constant__ Tile
                     mbar_arrive(full0 + 8u * s);
                     break;
                 }
-                issue_unit<C, CROP>(p, u, s, smem, a);
+                if (j == 0 && early0) {
+                    issue_unit_uncut<C>(p, u, s, smem);
+                    if (p.aug != nullptr) a = p.aug[u / p.bands];
+                    publish_unit(p, u, s, smem, a);
+                } else {
+                    issue_unit<C, CROP>(p, u, s, smem, a);
+                }
                 // the next unit and its record: requested now, used after the
                 // next empty wait
                 if (p.ws == nullptr || j + 1 < S) {

@@ -451,7 +451,10 @@ int tr_device_status(int* flags, int clear);
  *                    started (default: once its loads are issued); bit 4
  *                    lets a CTA exit once its last store has read shared
  *                    memory instead of once the store has completed (the
- *                    grid's completion still covers the writes); bit 6 is a
+ *                    grid's completion still covers the writes); bit 5 makes
+ *                    a CTA wait for its first band's record before requesting
+ *                    the band (default: the first band of a compact source is
+ *                    requested at once, erased span included); bit 6 is a
  *                    test hook for the kernels' bounded waits: the first band
  *                    of a batch waits for 16 bytes that never arrive, its waits
  *                    run out after about a second, the launch returns with bit 0

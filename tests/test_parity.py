@@ -265,3 +265,27 @@ def test_binding_rejects_short_workspace_tensor():
         trfn.tr_fused_norm(src, dst, [0.5] * 3, [0.25] * 3, workspace=torch.zeros(256, dtype=torch.uint8,
                                                                                    device="cuda"))
     assert trfn.tr_launch_count() == before
+
+
+@pytest.mark.parametrize("shape", SHAPES_TILED)
+def test_record_first_and_early_first_band_agree(shape):
+    """A CTA's first band is requested before its record arrives (default) or
+    after it (tr_tune_tiled flags bit 5): both match the oracle and each
+    other bit for bit, with the static and the dynamic schedule."""
+    N, H, W, C = shape
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(5 + N, N, H, W, allow_outside=True)
+    ws = _workspace()
+    outs = []
+    try:
+        for flags in (0, 32):
+            trfn.tr_tune_tiled(0, 0, 0, flags)
+            for w in (None, ws.data_ptr()):
+                got, _ = check_case(src, mean, std, aug, F16, NHWC, variant=TILED, workspace=w)
+                outs.append(got)
+    finally:
+        trfn.tr_tune_tiled(0, 0, 0, 0)
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)

@@ -58,6 +58,8 @@ def parse():
                          "flips/erases, else the centre): tr_fused_norm_crop")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
     ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
+    ap.add_argument("--fused-sampling", action="store_true",
+                    help="records drawn inside the fused kernel each step (tr_fused_norm_sampled)")
     ap.add_argument("--device-sampling", action="store_true",
                     help="each step samples its records on the GPU (tr_sample_aug_params_device) before the kernel")
     ap.add_argument("--e2e-steps", type=int, default=64)
@@ -287,7 +289,7 @@ def run_ours(args, rank, local, world, pg):
         recs, offset = sample_records(cfg, 2000 + args.config, offset, trfn.tr_sample_aug_params)
         recs_all.append(recs)
         augs.append(torch.from_numpy(recs).to(dev) if recs is not None else None)
-    if args.device_sampling and (cfg["flip"] or cfg["erase"]):
+    if (args.device_sampling or args.fused_sampling) and (cfg["flip"] or cfg["erase"]):
         # the records each step samples on the GPU (same seeds as launch(j) below)
         import oracle
         recs_all = [oracle.sample_aug_params_blocked(4000 + j, 0, N, H, W, flip=cfg["flip"], erase=cfg["erase"],
@@ -300,8 +302,14 @@ def run_ours(args, rank, local, world, pg):
     ws = None if args.static else torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
 
     dev_sampling = args.device_sampling and (cfg["flip"] or cfg["erase"])
+    fused_sampling = args.fused_sampling and (cfg["flip"] or cfg["erase"]) and not S
 
     def launch(j):
+        if fused_sampling:
+            trfn.tr_fused_norm_sampled(srcs[j], dsts[j], mean, std, 4000 + j, 0, augs[j], flip=cfg["flip"],
+                                       erase=cfg["erase"], erase_p=cfg["erase_p"], out_dtype=dt, layout=layout,
+                                       stream=stream, variant=args.variant, workspace=ws)
+            return
         if dev_sampling:
             trfn.tr_sample_aug_params_device(4000 + j, 0, N, H, W, augs[j], flip=cfg["flip"], erase=cfg["erase"],
                                              erase_p=cfg["erase_p"], stream=stream)
@@ -407,8 +415,9 @@ def run_ours(args, rank, local, world, pg):
             "launch": "CUDA graph of %d launches replayed; variant %d" % (G, args.variant),
             "schedule": "static (tr_fused_norm)" if args.static else "dynamic bands (tr_fused_norm_ws)",
             "source": ("%dx%d windows of %dx%d images (tr_fused_norm_crop)" % (H, W, S, S)) if S else "compact",
-            "records": "sampled on the GPU every step (tr_sample_aug_params_device)" if dev_sampling
-                       else "sampled on the host (tr_sample_aug_params), uploaded once",
+            "records": ("sampled inside the fused kernel every step (tr_fused_norm_sampled)" if fused_sampling
+                        else "sampled on the GPU every step (tr_sample_aug_params_device)" if dev_sampling
+                        else "sampled on the host (tr_sample_aug_params), uploaded once"),
             "parallelism": "replicas" if world > 1 else "single",
         },
         "hbm_gbs": achieved_gbs,

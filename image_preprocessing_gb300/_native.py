@@ -43,6 +43,12 @@ class StageBatch(ctypes.Structure):
                 ("count", ctypes.c_int), ("zone", ctypes.c_int)]
 
 
+class AugSampling(ctypes.Structure):
+    _fields_ = [("flip_enabled", ctypes.c_int), ("flip_p", ctypes.c_float), ("erase_enabled", ctypes.c_int),
+                ("erase_p", ctypes.c_float), ("scale_lo", ctypes.c_float), ("scale_hi", ctypes.c_float),
+                ("ratio_lo", ctypes.c_float), ("ratio_hi", ctypes.c_float)]
+
+
 _lib = None
 
 _vp = ctypes.c_void_p
@@ -56,6 +62,8 @@ _SIGNATURES = {
     "tr_fused_norm_variant": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i]),
     "tr_fused_norm_ws": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i, _vp]),
     "tr_workspace_bytes": (ctypes.c_size_t, []),
+    "tr_fused_norm_sampled": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _u64, _u64, ctypes.POINTER(AugSampling), _vp,
+                                   ctypes.POINTER(_u64), _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_crop": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
                                 _vp, _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp]),

@@ -9,7 +9,7 @@ import ctypes
 import numpy as np
 
 from . import _native
-from ._native import AugParam, StageBatch, StageSlot, TrError, check, float_array, lib
+from ._native import AugParam, AugSampling, StageBatch, StageSlot, TrError, check, float_array, lib
 
 OUT_F32, OUT_F16 = 0, 1
 LAYOUT_NHWC, LAYOUT_NCHW, LAYOUT_NHWC4 = 0, 1, 2
@@ -92,6 +92,35 @@ def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOU
                                 _dev_ptr(aug, "aug"), dt, lay, _stream_handle(stream), int(variant),
                                 _workspace_ptr(workspace, "tr_fused_norm"))
     check(rc, "tr_fused_norm")
+
+
+def tr_fused_norm_sampled(src, dst, mean, std, seed, offset, records, flip=True, flip_p=0.5, erase=True,
+                          erase_p=0.5, scale=(0.02, 0.33), ratio=(0.3, 3.3), out_dtype=OUT_F16, layout=LAYOUT_NHWC,
+                          stream=None, variant=VARIANT_AUTO, workspace=None):
+    """tr_fused_norm with the records drawn on the GPU in the same launch
+    (image n's record = tr_sample_aug_params_device's, counter block
+    offset + 24n); records: CUDA int32 (N, 5) tensor receiving them.
+    Returns the next free offset."""
+    import torch
+    if src.dtype != torch.uint8 or src.dim() != 4:
+        raise TrError(1, "tr_fused_norm_sampled", "src must be a uint8 (N,H,W,C) tensor")
+    N, H, W, C = src.shape
+    dt, lay = _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS)
+    want = torch.float16 if dt == OUT_F16 else torch.float32
+    if dst.dtype != want or dst.numel() != int(np.prod(out_shape(N, H, W, C, lay))):
+        raise TrError(1, "tr_fused_norm_sampled", "dst must be %s of the output shape" % want)
+    if records.dtype != torch.int32 or records.numel() != 5 * N:
+        raise TrError(1, "tr_fused_norm_sampled", "records must be int32 with N*5 elements")
+    sp = AugSampling(int(bool(flip)), float(flip_p), int(bool(erase)), float(erase_p), float(scale[0]),
+                     float(scale[1]), float(ratio[0]), float(ratio[1]))
+    nxt = ctypes.c_uint64(0)
+    check(lib().tr_fused_norm_sampled(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, float_array(mean),
+                                      float_array(std), int(seed), int(offset), ctypes.byref(sp),
+                                      _dev_ptr(records, "records"), ctypes.byref(nxt), dt, lay,
+                                      _stream_handle(stream), int(variant),
+                                      _workspace_ptr(workspace, "tr_fused_norm_sampled")),
+          "tr_fused_norm_sampled")
+    return nxt.value
 
 
 def tr_fused_norm_crop(src, src_H, src_W, row_stride, image_stride, dst, N, H, W, C, mean, std, crop=None,

@@ -58,9 +58,17 @@ struct CropSource {
     size_t row_stride = 0, image_stride = 0;
 };
 
+// Records drawn on the GPU as part of the launch (tr_fused_norm_sampled).
+struct Sampling {
+    bool on = false;
+    SampleSpec spec;
+    tr_aug_param* out = nullptr;   // device, N records
+};
+
 int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,
                     const float* stdv, const tr_aug_param* aug, int out_dtype, int out_layout,
-                    void* stream, int variant, void* workspace, const CropSource& cs = CropSource()) {
+                    void* stream, int variant, void* workspace, const CropSource& cs = CropSource(),
+                    const Sampling& smp = Sampling()) {
     int rc = check_shape(N, H, W, C, out_dtype, out_layout);
     if (rc != TR_OK) return rc;
     if (variant != TR_VARIANT_AUTO && variant != TR_VARIANT_TILED && variant != TR_VARIANT_GENERIC)
@@ -100,6 +108,14 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     const unsigned long long out_bytes = (unsigned long long)N * H * W * out_ch * ob;
     const uintptr_t s0 = (uintptr_t)src, d0 = (uintptr_t)dst;
     if (s0 < d0 + out_bytes && d0 < s0 + in_bytes) return TR_ERR_INVALID_ARGUMENT;   // overlap
+    if (smp.on) {
+        // the kernel writes the records while it reads src and writes dst
+        const uintptr_t r0 = (uintptr_t)smp.out;
+        const unsigned long long rec_bytes = (unsigned long long)N * sizeof(tr_aug_param);
+        if (smp.out == nullptr || (r0 % 4u) != 0 || aug != nullptr) return TR_ERR_INVALID_ARGUMENT;
+        if ((r0 < s0 + in_bytes && s0 < r0 + rec_bytes) || (r0 < d0 + out_bytes && d0 < r0 + rec_bytes))
+            return TR_ERR_INVALID_ARGUMENT;
+    }
 
     const bool tiled_ok = cs.on ? tiled_crop_supported(src, dst, N, H, W, C, out_dtype, out_layout, cs.src_H,
                                                        cs.src_W, cs.row_stride, cs.image_stride)
@@ -123,6 +139,13 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     a.src_W = cs.src_W;
     a.src_row_stride = cs.row_stride;
     a.src_image_stride = cs.image_stride;
+    if (smp.on) {
+        // the records first, into smp.out, then the kernel reads them in
+        // stream order (its prologue overlaps the sampler)
+        rc = launch_sampler(smp.spec, N, smp.out, stream);
+        if (rc != TR_OK) return rc;
+        a.aug = smp.out;
+    }
     rc = launch(a, variant);
     if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {
         // the tiled geometry does not fit this device's shared memory (rows
@@ -161,6 +184,25 @@ int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
 }
 
 size_t tr_workspace_bytes(void) { return kWorkspaceBytes; }
+
+int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,
+                          const float* std, uint64_t seed, uint64_t offset, const tr_aug_sampling* sampling,
+                          tr_aug_param* d_records, uint64_t* next_offset, int out_dtype, int out_layout,
+                          void* stream, int variant, void* workspace) {
+    if (sampling == nullptr || H < 1 || W < 1) return TR_ERR_INVALID_ARGUMENT;
+    Sampling smp;
+    smp.on = true;
+    smp.out = d_records;
+    int rc = make_sample_spec(seed, offset, H, W, sampling->flip_enabled, sampling->flip_p,
+                              sampling->erase_enabled, sampling->erase_p, sampling->scale_lo, sampling->scale_hi,
+                              sampling->ratio_lo, sampling->ratio_hi, &smp.spec);
+    if (rc != TR_OK) return rc;
+    if (N > 0 && d_records == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    rc = fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, nullptr, out_dtype, out_layout, stream, variant,
+                         workspace, CropSource(), smp);
+    if (rc == TR_OK && next_offset != nullptr) *next_offset = offset + (uint64_t)N * 24u;
+    return rc;
+}
 
 int tr_fused_norm_crop(const uint8_t* src_u8, int src_H, int src_W, size_t src_row_stride,
                        size_t src_image_stride, const int32_t* crop_yx, void* dst, int N, int H, int W, int C,

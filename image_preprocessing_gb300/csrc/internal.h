@@ -9,6 +9,16 @@
 
 namespace trfn {
 
+// Settings of the per-image record sampler (tr_sample_aug_params_device and
+// the sampled fused kernel); log_lo/log_hi are log(ratio_lo)/log(ratio_hi),
+// taken once on the host.
+struct SampleSpec {
+    uint64_t seed = 0, offset = 0;
+    int H = 0, W = 0;
+    int flip_enabled = 0, erase = 0;
+    float flip_p = 0.0f, erase_p = 0.0f, scale_lo = 0.0f, scale_hi = 0.0f, log_lo = 0.0f, log_hi = 0.0f;
+};
+
 // Arguments of one fused-normalisation launch after host validation.
 struct LaunchArgs {
     const uint8_t* src;
@@ -53,6 +63,14 @@ const char* last_error();
 
 // Tiled-kernel geometry knobs (0 = default).
 void tune_tiled(int band_bytes, int stages, int ctas_per_sm, int flags);
+
+// Record sampler (sampler_device.cu): validates the sampling settings into
+// a SampleSpec (TR_ERR_INVALID_ARGUMENT as tr_sample_aug_params), and
+// launches the one-thread-per-image sampler writing N records to d_out.
+int make_sample_spec(uint64_t seed, uint64_t offset, int H, int W, int flip_enabled, float flip_p,
+                     int erase_enabled, float erase_p, float scale_lo, float scale_hi, float ratio_lo,
+                     float ratio_hi, SampleSpec* sp);
+int launch_sampler(const SampleSpec& sp, int N, tr_aug_param* d_out, void* stream);
 
 // Count of kernels launched by this library.
 void count_launch();

@@ -231,8 +231,9 @@ int tr_sample_aug_params(uint64_t seed, uint64_t offset, int N, int H, int W,
                          float scale_lo, float scale_hi, float ratio_lo, float ratio_hi,
                          tr_aug_param* out_host, uint64_t* next_offset);
 
-/* tr_sample_aug_params_device — the same decisions made on the GPU, one
- * thread per image, written to d_out (device, N records, 4-byte aligned) on
+/* tr_sample_aug_params_device — the same decisions made on the GPU (a warp
+ * per image for batches up to 8 images per SM, else a thread per image),
+ * written to d_out (device, N records, 4-byte aligned) on
  * `stream` in stream order.  Image n draws from its own counter block,
  * offsets offset + 24n + k (24 = the most draws one image can take), so the
  * batch needs no sequential pass; *next_offset (may be NULL) receives
@@ -246,6 +247,34 @@ int tr_sample_aug_params_device(uint64_t seed, uint64_t offset, int N, int H, in
                                 int flip_enabled, float flip_p, int erase_enabled, float erase_p,
                                 float scale_lo, float scale_hi, float ratio_lo, float ratio_hi,
                                 tr_aug_param* d_out, uint64_t* next_offset, void* stream);
+
+/* Sampling settings of tr_fused_norm_sampled (meaning as the arguments of
+ * tr_sample_aug_params).                                                    */
+typedef struct tr_aug_sampling {
+    int flip_enabled;
+    float flip_p;
+    int erase_enabled;
+    float erase_p;
+    float scale_lo, scale_hi;   /* erased area as a fraction of the image */
+    float ratio_lo, ratio_hi;   /* erased aspect ratio h/w               */
+} tr_aug_sampling;
+
+/* tr_sample_aug_params_device(seed, offset, ...) into d_records, then
+ * tr_fused_norm_ws reading them, as one call: two launches in stream order
+ * (the kernel's prologue overlaps the sampler), no record crosses the host
+ * link.  d_records: device, N records, 4-byte aligned, not overlapping src or
+ * dst.  *next_offset (may be NULL) receives offset + 24N.  Errors as
+ * tr_fused_norm_ws and tr_sample_aug_params_device, all checked before
+ * either launch; TR_ERR_INVALID_ARGUMENT for a NULL sampling or d_records
+ * (N > 0).  There is no such call in the article (its execute() draws on
+ * the CPU, §五).  Sampling inside the fused kernel instead (the producer warp
+ * drawing each band's record) measured slower: 22.6 against 21.3 us for
+ * 256x224x224x3, as a record costs more to sample than to load and sits on
+ * the producer's path to its next copy.                                    */
+int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                          const float* mean, const float* std, uint64_t seed, uint64_t offset,
+                          const tr_aug_sampling* sampling, tr_aug_param* d_records, uint64_t* next_offset,
+                          int out_dtype, int out_layout, void* stream, int variant, void* workspace);
 
 /* Host check of N records: TR_OK when every rectangle is either "no erase"
  * (h <= 0 or w <= 0) or lies inside the H x W image; else

@@ -226,3 +226,26 @@ def test_crop_arguments_rejected_before_launch():
                                 None, 1, None) == NOT_SUPPORTED
     assert L.tr_fused_norm_crop(None, 20, 20, 64, 1280, None, None, 0, 12, 16, 3, M3, S3, None, 0, 0,
                                 None, 0, None) == OK
+
+
+def test_fused_sampled_host_checks():
+    """tr_fused_norm_sampled's checks run on the host: an empty batch is a
+    no-op that still reports the next offset; bad sampling settings, a
+    missing sampling struct or missing records are rejected."""
+    L = _native.lib()
+    m = _native.float_array([0.5, 0.5, 0.5])
+    s = _native.float_array([0.25, 0.25, 0.25])
+    good = _native.AugSampling(1, 0.5, 1, 0.5, 0.02, 0.33, 0.3, 3.3)
+    nxt = ctypes.c_uint64(7)
+    assert L.tr_fused_norm_sampled(None, None, 0, 8, 8, 3, m, s, 1, 40, ctypes.byref(good), None,
+                                   ctypes.byref(nxt), 1, 0, None, 0, None) == 0
+    assert nxt.value == 40
+    for bad in (_native.AugSampling(1, 0.5, 1, 0.5, 0.5, 0.1, 0.3, 3.3),        # scale bounds out of order
+                _native.AugSampling(1, 0.5, 1, 0.5, 0.02, 0.33, 0.0, 3.3),      # ratio_lo <= 0
+                _native.AugSampling(1, float("nan"), 0, 0.0, 0, 0, 0, 0)):      # non-finite p
+        assert L.tr_fused_norm_sampled(None, None, 0, 8, 8, 3, m, s, 1, 0, ctypes.byref(bad), None, None,
+                                       1, 0, None, 0, None) == 1
+    assert L.tr_fused_norm_sampled(None, None, 0, 8, 8, 3, m, s, 1, 0, None, None, None, 1, 0, None, 0, None) == 1
+    # N > 0 without a records buffer
+    assert L.tr_fused_norm_sampled(0x1000, 0x200000, 4, 8, 8, 3, m, s, 1, 0, ctypes.byref(good), None, None,
+                                   1, 0, None, 0, None) == 1

@@ -341,12 +341,16 @@ def run_ours(args, rank, local, world, pg):
     g_tail = capture(K % G) if K % G else None
     captured = trfn.tr_launch_count() - launches_before
 
-    def run_steps(steps, exact_tail=None):
+    def run_steps(steps, exact_tail=None, marks=None):
         # full graph replays, then the remainder as one tail graph (timed
         # region) or as eager launches (warm-up); all on `stream`, where the
-        # timing events are recorded (a replay goes to the current stream)
+        # timing events are recorded (a replay goes to the current stream).
+        # marks: (replay index, event) pairs recorded before that replay
+        marks = dict(marks or [])
         with torch.cuda.stream(stream):
-            for _ in range(steps // G):
+            for i in range(steps // G):
+                if i in marks:
+                    marks[i].record(stream)
                 g_full.replay()
             rem = steps % G
             if rem and exact_tail is not None:
@@ -366,8 +370,12 @@ def run_ours(args, rank, local, world, pg):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    # five trials inside the timed region: events between graph replays
+    replays = K // G
+    trial_at = [replays * t // 5 for t in range(1, 5)] if replays >= 5 else []
+    trial_ev = [torch.cuda.Event(enable_timing=True) for _ in trial_at]
     ev0.record(stream)
-    run_steps(K, g_tail)
+    run_steps(K, g_tail, marks=list(zip(trial_at, trial_ev)))
     ev1.record(stream)
     ev1.synchronize()
     torch.cuda.synchronize()
@@ -375,6 +383,13 @@ def run_ours(args, rank, local, world, pg):
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(pg, ms, dev)
+    trials = None
+    if trial_ev:
+        bounds = [ev0] + trial_ev + [ev1]
+        steps_in = [(b - a) * G for a, b in zip([0] + trial_at, trial_at + [replays])]
+        steps_in[-1] += K % G
+        per = [bounds[t].elapsed_time(bounds[t + 1]) / steps_in[t] for t in range(len(steps_in))]
+        trials = {"count": len(per), "ms_per_step": per, "median_ms_per_step": float(np.median(per))}
     per_launch_s = (ms / 1000.0) / K
     # average algorithmic bytes per launch over the rotation actually timed
     seq = [k % nsets for k in range(K)]
@@ -434,6 +449,8 @@ def run_ours(args, rank, local, world, pg):
     }
     if clk is not None:
         res["clocks"] = clk
+    if trials is not None:
+        res["trials"] = trials
     if e2e is not None:
         res["e2e"] = e2e
     if pipeline is not None:

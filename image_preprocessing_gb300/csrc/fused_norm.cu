@@ -12,8 +12,8 @@
 //  * TILED: a persistent kernel.  The batch is cut into units of R rows of one
 //    image ("row bands").  One thread per CTA streams the source bytes of the
 //    next bands into a ring of shared-memory stages with TMA bulk copies
-//    (cp.async.bulk + mbarrier transaction counts), skipping 16-byte chunks
-//    that lie wholly inside an erased span.  All threads convert groups of 8
+//    (cp.async.bulk + mbarrier transaction counts), leaving out the 16-byte
+//    chunks that lie wholly inside a wide erased span.  All threads convert groups of 8
 //    (C=3), 16 (C=1), 8 (C=2) or 4 (C=4) pixels: the mirrored gather is done
 //    by choosing source byte lanes with PRMT, the byte becomes 2^23 + x by the
 //    same PRMT, one exact FADD removes 2^23, one FFMA applies scale and bias.
@@ -313,12 +313,13 @@ __device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, c
 }
 
 // Fills stage s with unit u: records the unit for the consumers, arrives on
-// full[s] with the byte count and issues the band's copies, skipping the
-// 16-byte chunks that lie wholly inside the erased source span of the erased
+// full[s] with the byte count and issues the band's copies, leaving out (when
+// allowed and worth a copy) the 16-byte chunks that lie wholly inside the
+// erased source span of the erased
 // rows.
 template <int C, bool CROP>
 __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem,
-                                           const tr_aug_param& a) {
+                                           const tr_aug_param& a, bool allow_skip = true) {
     const Band b = band_of(p, u);
     const int y_begin = b.y_begin, rows = b.rows;
     int flip = 0, erow_lo = 0, erow_hi = 0, ecol_lo = 0, ecol_hi = 0;
@@ -368,7 +369,12 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     const uint32_t a_hi = ((uint32_t)xs_hi * C) & ~15u;
     // test hook for the bounded waits: unit 0's stage then never completes
     const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;
-    if (r_lo >= r_hi || a_hi <= a_lo) {
+    // An erased row's span is left out only when it saves at least
+    // skip_min bytes: each one costs a copy more (tr_tune_tiled flags bits
+    // 12..15 = v: 0 keeps 256 bytes, else (v - 1) * 128).
+    const int v = (p.hints >> 12) & 15;
+    const uint32_t skip_min = v == 0 ? 256u : (uint32_t)(v - 1) * 128u;
+    if (r_lo >= r_hi || a_hi <= a_lo || !allow_skip || a_hi - a_lo < skip_min) {
         mbar_arrive_expect_tx(bar, total + missing);
         load_bytes(p, sdst, g, total, bar);
         return;
@@ -675,7 +681,9 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
                 a = unit_record(u);
                 publish_unit(p, u, s, smem, a);
             } else {
-                issue_unit<C, CROP>(p, u, s, smem, a);
+                // a CTA's first S bands are copied whole (measured faster:
+                // they are the ramp every launch starts with)
+                issue_unit<C, CROP>(p, u, s, smem, a, (p.hints & 2048) || j >= S);
             }
             // the next unit and its record: requested now, used after the
             // next empty wait
@@ -1074,7 +1082,7 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
-    p.hints = g_flags.load(std::memory_order_relaxed) & 127;
+    p.hints = g_flags.load(std::memory_order_relaxed) & (127 | 2048 | 0xF000);
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 

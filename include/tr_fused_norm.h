@@ -489,7 +489,13 @@ int tr_device_status(int* flags, int clear);
  *                    run out after about a second, the launch returns with bit 0
  *                    of the device status word set and its output incomplete;
  *                    crop sources: bit 8 reads 16-byte chunks even where 32-byte
- *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion.
+ *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion;
+ *                    compact sources: erased source spans are left out of a
+ *                    band's copies (one copy more per erased row) only when
+ *                    they save at least 256 bytes a row and not in a CTA's
+ *                    first S bands; bit 11 leaves them out of the first S
+ *                    bands too, bits 12..15 = v != 0 set the threshold to
+ *                    (v - 1) * 128 bytes.
  * Results do not depend on the geometry.  Errors: TR_ERR_INVALID_ARGUMENT
  * for negative values or stages of 1 or above 8.                            */
 int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags);

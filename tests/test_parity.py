@@ -270,8 +270,9 @@ def test_binding_rejects_short_workspace_tensor():
 @pytest.mark.parametrize("shape", SHAPES_TILED)
 def test_record_first_and_early_first_band_agree(shape):
     """A CTA's first band is requested before its record arrives (default) or
-    after it (tr_tune_tiled flags bit 5): both match the oracle and each
-    other bit for bit, with the static and the dynamic schedule."""
+    after it (tr_tune_tiled flags bit 5), and erased spans are left out of
+    the copies by the default rule or everywhere (bits 11, 12..15): all match
+    the oracle and each other bit for bit, with both schedules."""
     N, H, W, C = shape
     src = synth.coordinate_image(N, H, W, C)
     mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
@@ -280,7 +281,7 @@ def test_record_first_and_early_first_band_agree(shape):
     ws = _workspace()
     outs = []
     try:
-        for flags in (0, 32):
+        for flags in (0, 32, 2048 | (1 << 12), 32 | 2048 | (1 << 12)):
             trfn.tr_tune_tiled(0, 0, 0, flags)
             for w in (None, ws.data_ptr()):
                 got, _ = check_case(src, mean, std, aug, F16, NHWC, variant=TILED, workspace=w)

@@ -319,7 +319,7 @@ __device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, c
 // rows.
 template <int C, bool CROP>
 __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem,
-                                           const tr_aug_param& a, bool allow_skip = true) {
+                                           const tr_aug_param& a, bool allow_skip, int2 origin) {
     const Band b = band_of(p, u);
     const int y_begin = b.y_begin, rows = b.rows;
     int flip = 0, erow_lo = 0, erow_hi = 0, ecol_lo = 0, ecol_hi = 0;
@@ -340,11 +340,9 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     if (CROP) {
         // The window's rows, from its 16-byte chunk on, as one box of R rows
         // (rows past the source image arrive as zeros and are not used).
-        int cy = 0, cx = 0;
-        if (p.crop != nullptr) {
-            cy = min(max(p.crop[2 * (size_t)b.n], 0), p.src_H - p.H);
-            cx = min(max(p.crop[2 * (size_t)b.n + 1], 0), p.src_W - p.W);
-        }
+        // the window origin (loaded by the caller with the record), clamped
+        const int cy = min(max(origin.x, 0), p.src_H - p.H);
+        const int cx = min(max(origin.y, 0), p.src_W - p.W);
         const int xb = cx * C;
         rec->flags = flip | ((xb & ((1 << p.chunk_shift) - 1)) << 8);
         const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
@@ -643,9 +641,16 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         const int ngroups = min(kTicketGroups, G);   // every group must have a CTA
         const int group = (int)blockIdx.x % ngroups;
         const int n_dyn = max(0, p.num_units - S * G);   // units handed out by tickets
+        // unit u's record and, for crop sources, its image's window origin:
+        // requested together, ahead of the wait for the stage they go to
+        int2 org = make_int2(0, 0);
         auto unit_record = [&](int u) {
             tr_aug_param r = {0, 0, 0, 0, 0};
             if (p.aug != nullptr) r = p.aug[u / p.bands];
+            if (CROP && p.crop != nullptr) {
+                org.x = p.crop[2 * (size_t)(u / p.bands)];
+                org.y = p.crop[2 * (size_t)(u / p.bands) + 1];
+            }
             return r;
         };
         // the CTA's jn-th unit: static for the first S (or without a
@@ -683,7 +688,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
             } else {
                 // a CTA's first S bands are copied whole (measured faster:
                 // they are the ramp every launch starts with)
-                issue_unit<C, CROP>(p, u, s, smem, a, (p.hints & 2048) || j >= S);
+                issue_unit<C, CROP>(p, u, s, smem, a, (p.hints & 2048) || j >= S, org);
             }
             // the next unit and its record: requested now, used after the
             // next empty wait

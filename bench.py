@@ -29,6 +29,7 @@ import concurrent.futures as cf
 import ctypes
 import hashlib
 import json
+import re
 import os
 import subprocess
 import sys
@@ -120,10 +121,16 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """sha256[:16] of the kernel's source (fused_norm.cu + internal.h) with
+    comments and whitespace removed: what the compiler sees, so a profile
+    stays attached to the code it measured across comment edits."""
     h = hashlib.sha256()
     for fn in ("fused_norm.cu", "internal.h"):
-        with open(os.path.join(ROOT, "image_preprocessing_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "image_preprocessing_gb300", "csrc", fn)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -13,17 +13,18 @@
 //    image ("row bands").  One thread per CTA streams the source bytes of the
 //    next bands into a ring of shared-memory stages with TMA bulk copies
 //    (cp.async.bulk + mbarrier transaction counts), leaving out the 16-byte
-//    chunks that lie wholly inside a wide erased span.  All threads convert groups of 8
-//    (C=3), 16 (C=1), 8 (C=2) or 4 (C=4) pixels: the mirrored gather is done
-//    by choosing source byte lanes with PRMT, the byte becomes 2^23 + x by the
-//    same PRMT, one exact FADD removes 2^23, one FFMA applies scale and bias.
-//    Results go to a double-buffered shared-memory output tile that one TMA
-//    bulk store per band (per plane for NCHW) writes to global memory.
-//    With a crop source (tr_fused_norm_crop) the bands come from windows of a
-//    strided source through a TMA tensor copy (cp.async.bulk.tensor): the
-//    source is described as {16-byte chunk, chunk, row, image}, so a window
-//    may start at any byte; consumers realign the first chunk's offset with
-//    funnel shifts.
+//    chunks that lie wholly inside a wide erased span.  The other warps
+//    convert groups of 8 (C=3), 16 (C=1), 8 (C=2) or 4 (C=4) pixels: the
+//    mirrored gather is done by choosing source byte lanes with PRMT, the
+//    byte becomes 2^23 + x by the same PRMT, one exact FADD removes 2^23,
+//    one FFMA applies scale and bias.  Results go to a double-buffered
+//    shared-memory output tile that one TMA bulk store per band (per plane
+//    for NCHW) writes to global memory.  With a crop source
+//    (tr_fused_norm_crop) the bands come from windows of a strided source
+//    through a TMA tensor copy (cp.async.bulk.tensor): the source is
+//    described as {chunk, chunk index, row, image} with 16- or 32-byte
+//    chunks, so a window may start at any byte; consumers realign the first
+//    chunk's offset with funnel shifts.
 //  * GENERIC: one thread per output element, any shape, stride and alignment.
 //
 // Both kernels compute each value as fma(float(x), scale_c, bias_c) with the
@@ -254,7 +255,7 @@ __device__ __forceinline__ void convert_group(const uint32_t (&w)[Group<C>::kWor
 // ---------------------------------------------------------------- tiled ---
 
 struct TiledParams {
-    CUtensorMap tmap;      // crop sources: {16-byte chunk, chunk, row, image} of the source
+    CUtensorMap tmap;      // crop sources: {chunk, chunk index, row, image} of the source
     const int32_t* crop;   // crop sources: per-image window origin {top, left}, or null
     int src_H, src_W;      // crop sources: source image size
     uint32_t in_pitch;     // bytes per row of an input stage (W*C; chunks*chunk bytes for crop sources)
@@ -273,10 +274,11 @@ struct TiledParams {
     uint32_t plane_bytes;  // NCHW: bytes per plane of one band in the output stage (R*W*ob)
     int stages;
     unsigned int* ws;      // scheduling workspace (ticket counters, finished CTAs), or null
-    int hints;             // tr_tune_tiled flags: bit 0 normal-priority loads, bit 1
-                           // normal-priority stores, bit 2 evict-last stores (default:
-                           // both evict-first); bit 3 early dependent launch; bit 6 test
-                           // hook: unit 0's stage expects 16 bytes that never arrive
+    int hints;             // tr_tune_tiled flags (include/tr_fused_norm.h): L2 policies
+                           // (bits 0-2), early dependent launch (3), exit after the last
+                           // store's shared-memory reads (4), record before the first
+                           // band (5), bounded-wait test hook (6), erased-span rule
+                           // (11, 12-15)
     float scale[4];
     float bias[4];
 };
@@ -284,7 +286,7 @@ struct TiledParams {
 // Per-stage record of the unit held in that stage.
 struct UnitRec {
     int n, y_begin, rows;
-    int flags;             // bit 0: flip; bits 8..11: byte offset of the window in its first chunk
+    int flags;             // bit 0: flip; bits 8..12: byte offset of the window in its first chunk
     int erow_lo, erow_hi;  // erased output rows [lo, hi), clipped to the image
     int ecol_lo, ecol_hi;  // erased output columns [lo, hi), clipped
 };

@@ -483,7 +483,10 @@ int tr_device_status(int* flags, int clear);
  *                    grid's completion still covers the writes); bit 5 makes
  *                    a CTA wait for its first band's record before requesting
  *                    the band (default: the first band of a compact source is
- *                    requested at once, erased span included); bit 6 is a
+ *                    requested at once, erased span included); bit 7 turns
+ *                    off the rotated order of the output tile's 16-byte
+ *                    shared-memory stores (a bank-conflict avoidance for
+ *                    layouts whose groups span 64 bytes or more); bit 6 is a
  *                    test hook for the kernels' bounded waits: the first band
  *                    of a batch waits for 16 bytes that never arrive, its waits
  *                    run out after about a second, the launch returns with bit 0

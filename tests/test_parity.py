@@ -290,3 +290,26 @@ def test_record_first_and_early_first_band_agree(shape):
         trfn.tr_tune_tiled(0, 0, 0, 0)
     for o in outs[1:]:
         assert np.array_equal(outs[0], o)
+
+
+@pytest.mark.parametrize("shape", SHAPES_TILED)
+def test_rotated_and_plain_tile_stores_agree(shape):
+    """The output tile's 16-byte stores go in a rotated order per group for
+    layouts whose groups span 64 bytes or more (default) or in plain order
+    (tr_tune_tiled flags bit 7): both match the oracle, bit for bit alike."""
+    N, H, W, C = shape
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(9 + N, N, H, W, allow_outside=True)
+    try:
+        for dt in (F16, F32):
+            for layout in (NHWC, NHWC4):
+                outs = []
+                for flags in (0, 128):
+                    trfn.tr_tune_tiled(0, 0, 0, flags)
+                    got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED)
+                    outs.append(got)
+                assert np.array_equal(outs[0], outs[1])
+    finally:
+        trfn.tr_tune_tiled(0, 0, 0, 0)

@@ -25,7 +25,7 @@
 //    described as {chunk, chunk index, row, image} with 16- or 32-byte
 //    chunks, so a window may start at any byte; consumers realign the first
 //    chunk's offset with funnel shifts.
-//  * GENERIC: one thread per output element, any shape, stride and alignment.
+//  * GENERIC: one thread per output pixel, any shape, stride and alignment.
 //
 // Both kernels compute each value as fma(float(x), scale_c, bias_c) with the
 // same binary32 operands, so they agree bit for bit.
@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -794,65 +795,124 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
 
 // -------------------------------------------------------------- generic ---
 
+// Unsigned division by a divisor fixed for the launch, by one high multiply
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, Figure 4.1): for d >= 1 and l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1; then for any 32-bit x,
+// t = mulhi(m, x) and x / d = (t + ((x - t) >> 1)) >> (l - 1) (x / 1 = x).
+struct DivU32 {
+    uint32_t d = 1, m = 0;
+    int l = 0;
+};
+
+inline DivU32 make_div(uint32_t d) {
+    DivU32 v;
+    v.d = d;
+    int l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    v.l = l;
+    v.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+    return v;
+}
+
+__device__ __forceinline__ uint32_t div_u32(uint32_t x, const DivU32& v) {
+    if (v.l == 0) return x;   // d == 1
+    const uint32_t t = __umulhi(v.m, x);
+    return (t + ((x - t) >> 1)) >> (v.l - 1);
+}
+
 struct GenericParams {
     const uint8_t* src;
     uint8_t* dst;
     const tr_aug_param* aug;
     const int32_t* crop;   // per-image window origin {top, left}, or null
-    long long total;       // output elements
     long long image_stride, row_stride;   // source strides in bytes
-    int H, W, C;
+    int N, H, W;
     int src_H, src_W;      // source image size (H, W for compact sources)
+    DivU32 div_w, div_h;   // x / W and x / H for 32-bit pixel indices
     float scale[4];
     float bias[4];
 };
 
-template <int OUT_F16, int LAYOUT>
+// One thread per output pixel, consecutive threads on consecutive pixels of
+// a row, so each channel's loads and stores cover contiguous spans; a
+// pixel's outputs go out as one 4-, 8- or 16-byte store where they are that
+// long and aligned.  Pixel indices below 2^31 use 32-bit arithmetic with the
+// invariant-divisor division above.
+template <int C, int OUT_F16, int LAYOUT>
 __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ GenericParams p) {
+    constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
+    constexpr int OB = OUT_F16 ? 2 : 4;
     grid_dependency_wait();
+    const long long pixels = (long long)p.N * p.H * p.W;
     const long long stride = (long long)gridDim.x * blockDim.x;
-    const long long W = p.W, H = p.H, C = p.C;
-    for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < p.total; o += stride) {
-        long long n, y, x, c;
-        if (LAYOUT == TR_LAYOUT_NCHW) {
-            x = o % W;
-            long long t = o / W;
-            y = t % H;
-            t /= H;
-            c = t % C;
-            n = t / C;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < pixels; t += stride) {
+        int n, y, x;
+        if (pixels <= 0x7FFFFFFFll) {
+            const uint32_t ti = (uint32_t)t;
+            const uint32_t row = div_u32(ti, p.div_w);
+            x = (int)(ti - row * (uint32_t)p.W);
+            n = (int)div_u32(row, p.div_h);
+            y = (int)(row - (uint32_t)n * (uint32_t)p.H);
         } else {
-            const long long ch = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
-            c = o % ch;
-            const long long pix = o / ch;
-            x = pix % W;
-            const long long t = pix / W;
-            y = t % H;
-            n = t / H;
+            const long long row = t / p.W;
+            x = (int)(t - row * p.W);
+            n = (int)(row / p.H);
+            y = (int)(row - (long long)n * p.H);
         }
-        float v = 0.0f;
-        if (c < C) {
-            bool flip = false, erased = false;
-            if (p.aug != nullptr) {
-                const tr_aug_param a = p.aug[n];
-                flip = (a.flip != 0);
-                erased = a.h > 0 && a.w > 0 && y >= a.y0 && y < (long long)a.y0 + a.h &&
-                         x >= a.x0 && x < (long long)a.x0 + a.w;
+        bool flip = false, erased = false;
+        if (p.aug != nullptr) {
+            const tr_aug_param a = p.aug[n];
+            flip = (a.flip != 0);
+            erased = a.h > 0 && a.w > 0 && y >= a.y0 && (long long)y < (long long)a.y0 + a.h && x >= a.x0 &&
+                     (long long)x < (long long)a.x0 + a.w;
+        }
+        int cy = 0, cx = 0;
+        if (p.crop != nullptr) {
+            cy = min(max(p.crop[2 * (size_t)n], 0), p.src_H - p.H);
+            cx = min(max(p.crop[2 * (size_t)n + 1], 0), p.src_W - p.W);
+        }
+        const int xs = flip ? (p.W - 1 - x) : x;
+        const uint8_t* sp = p.src + (size_t)n * p.image_stride + (size_t)(cy + y) * p.row_stride + (size_t)(cx + xs) * C;
+        float v[OC];
+#pragma unroll
+        for (int c = 0; c < OC; ++c) {
+            v[c] = 0.0f;
+            if (c < C && !erased) v[c] = __fmaf_rn((float)__ldg(sp + c), p.scale[c], p.bias[c]);
+        }
+        const size_t pix = ((size_t)n * p.H + y) * p.W + x;
+        if (LAYOUT == TR_LAYOUT_NCHW) {
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const size_t o = ((size_t)n * C + c) * p.H * p.W + (size_t)y * p.W + x;
+                if (OUT_F16) reinterpret_cast<__half*>(p.dst)[o] = __float2half_rn(v[c]);
+                else reinterpret_cast<float*>(p.dst)[o] = v[c];
             }
-            if (!erased) {
-                long long cy = 0, cx = 0;
-                if (p.crop != nullptr) {
-                    cy = min(max((long long)p.crop[2 * n], 0ll), (long long)(p.src_H - p.H));
-                    cx = min(max((long long)p.crop[2 * n + 1], 0ll), (long long)(p.src_W - p.W));
+        } else {
+            uint8_t* o = p.dst + pix * OC * OB;
+            constexpr int PB = OC * OB;   // bytes of one pixel's outputs
+            uint32_t w[(PB + 3) / 4];
+            if (OUT_F16) {
+#pragma unroll
+                for (int c = 0; c < OC; c += 2) w[c / 2] = pack_half2(v[c], c + 1 < OC ? v[c + 1] : 0.0f);
+            } else {
+#pragma unroll
+                for (int c = 0; c < OC; ++c) w[c] = __float_as_uint(v[c]);
+            }
+            if (PB == 16 && ((uintptr_t)o & 15u) == 0) {
+                *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2 % ((PB + 3) / 4)], w[3 % ((PB + 3) / 4)]);
+            } else if (PB == 8 && ((uintptr_t)o & 7u) == 0) {
+                *reinterpret_cast<uint2*>(o) = make_uint2(w[0], w[1 % ((PB + 3) / 4)]);
+            } else if (PB == 4 && ((uintptr_t)o & 3u) == 0) {
+                *reinterpret_cast<uint32_t*>(o) = w[0];
+            } else {
+#pragma unroll
+                for (int c = 0; c < OC; ++c) {
+                    if (OUT_F16) reinterpret_cast<__half*>(o)[c] = __float2half_rn(v[c]);
+                    else reinterpret_cast<float*>(o)[c] = v[c];
                 }
-                const long long xs = flip ? (W - 1 - x) : x;
-                const uint8_t b =
-                    __ldg(p.src + n * p.image_stride + (cy + y) * p.row_stride + (cx + xs) * C + c);
-                v = __fmaf_rn((float)b, p.scale[c], p.bias[c]);
             }
         }
-        if (OUT_F16) reinterpret_cast<__half*>(p.dst)[o] = __float2half_rn(v);
-        else reinterpret_cast<float*>(p.dst)[o] = v;
     }
 }
 
@@ -910,16 +970,29 @@ TiledFn pick_tiled(int C, int f16, int layout, bool crop) {
     return crop ? pick_tiled_c<true>(C, f16, layout) : pick_tiled_c<false>(C, f16, layout);
 }
 
-GenericFn pick_generic(int f16, int layout) {
-    if (f16) {
-        if (layout == TR_LAYOUT_NHWC) return generic_kernel<1, TR_LAYOUT_NHWC>;
-        if (layout == TR_LAYOUT_NCHW) return generic_kernel<1, TR_LAYOUT_NCHW>;
-        return generic_kernel<1, TR_LAYOUT_NHWC4>;
+template <int C, int F16>
+GenericFn pick_generic_layout(int layout) {
+    switch (layout) {
+    case TR_LAYOUT_NHWC: return generic_kernel<C, F16, TR_LAYOUT_NHWC>;
+    case TR_LAYOUT_NCHW: return generic_kernel<C, F16, TR_LAYOUT_NCHW>;
+    default: return generic_kernel<C, F16, TR_LAYOUT_NHWC4>;
     }
-    if (layout == TR_LAYOUT_NHWC) return generic_kernel<0, TR_LAYOUT_NHWC>;
-    if (layout == TR_LAYOUT_NCHW) return generic_kernel<0, TR_LAYOUT_NCHW>;
-    return generic_kernel<0, TR_LAYOUT_NHWC4>;
 }
+
+template <int C>
+GenericFn pick_generic_dtype(int f16, int layout) {
+    return f16 ? pick_generic_layout<C, 1>(layout) : pick_generic_layout<C, 0>(layout);
+}
+
+GenericFn pick_generic(int C, int f16, int layout) {
+    switch (C) {
+    case 1: return pick_generic_dtype<1>(f16, layout);
+    case 2: return pick_generic_dtype<2>(f16, layout);
+    case 3: return pick_generic_dtype<3>(f16, layout);
+    default: return pick_generic_dtype<4>(f16, layout);
+    }
+}
+
 
 int group_pixels(int C) { return C == 3 ? 8 : 16 / C; }
 
@@ -1196,13 +1269,11 @@ int launch_generic(const LaunchArgs& a) {
         return TR_ERR_CUDA;
     }
     const int f16 = (a.out_dtype == TR_OUT_F16);
-    const int out_ch = (a.out_layout == TR_LAYOUT_NHWC4) ? 4 : a.C;
     GenericParams p;
     p.src = a.src;
     p.dst = static_cast<uint8_t*>(a.dst);
     p.aug = a.aug;
-    p.total = (long long)a.N * a.H * a.W * out_ch;
-    p.H = a.H; p.W = a.W; p.C = a.C;
+    p.N = a.N; p.H = a.H; p.W = a.W;
     p.crop = a.crop_src ? a.crop : nullptr;
     p.src_H = a.crop_src ? a.src_H : a.H;
     p.src_W = a.crop_src ? a.src_W : a.W;
@@ -1210,10 +1281,18 @@ int launch_generic(const LaunchArgs& a) {
     p.image_stride = a.crop_src ? (long long)a.src_image_stride : (long long)a.H * a.W * a.C;
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
     const int threads = 256;
-    long long grid = (p.total + threads - 1) / threads;
-    grid = std::min<long long>(grid, (long long)di.sm_count * 8);
+    p.div_w = make_div((uint32_t)a.W);
+    p.div_h = make_div((uint32_t)a.H);
+    const long long pixels = (long long)a.N * a.H * a.W;
+    // about 8 pixels per thread, between 8 and 32 blocks per SM (measured:
+    // 32 blocks per SM 11 % faster for 256 x 227x227x3, 8 better for 1024
+    // x 28x28x1)
+    long long grid = pixels / ((long long)threads * 8);
+    grid = std::max<long long>(grid, (long long)di.sm_count * 8);
+    grid = std::min<long long>(grid, (long long)di.sm_count * 32);
+    grid = std::min<long long>(grid, (pixels + threads - 1) / threads);
     if (grid < 1) grid = 1;
-    if (!check_cuda(launch_pdl((const void*)pick_generic(f16, a.out_layout), (unsigned)grid, threads, 0,
+    if (!check_cuda(launch_pdl((const void*)pick_generic(a.C, f16, a.out_layout), (unsigned)grid, threads, 0,
                                a.stream, &p),
                     "generic kernel launch"))
         return TR_ERR_CUDA;

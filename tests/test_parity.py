@@ -313,3 +313,23 @@ def test_rotated_and_plain_tile_stores_agree(shape):
                 assert np.array_equal(outs[0], outs[1])
     finally:
         trfn.tr_tune_tiled(0, 0, 0, 0)
+
+
+GENERIC_LARGE = [(200, 28, 28, 1), (170, 28, 28, 2), (200, 28, 28, 3), (12, 111, 113, 3), (3, 227, 227, 3)]
+
+
+@pytest.mark.parametrize("shape", GENERIC_LARGE)
+@pytest.mark.parametrize("dt", [F16, F32])
+@pytest.mark.parametrize("layout", [NHWC, NCHW, NHWC4])
+def test_generic_kernel_large_odd_rows(shape, dt, layout):
+    """Rows that are not a multiple of 16 bytes in batches of over 2^17
+    pixels (the per-element kernel with its 32-bit invariant-divisor index
+    arithmetic, per-pixel vector stores and grid of 8 to 32 blocks per SM),
+    with flips and rectangles that stick out, against the oracle."""
+    N, H, W, C = shape
+    assert (W * C) % 16 and N * H * W >= 1 << 17
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(21 + N, N, H, W, allow_outside=True)
+    check_case(src, mean, std, aug, dt, layout, variant=AUTO)

@@ -333,3 +333,54 @@ def test_generic_kernel_large_odd_rows(shape, dt, layout):
     std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
     aug = synth.random_records(21 + N, N, H, W, allow_outside=True)
     check_case(src, mean, std, aug, dt, layout, variant=AUTO)
+
+
+def _sampled_check(d_src, d_dst, recs, idx, mean, std, dt, layout):
+    """The oracle on a few images of a large batch, copied back one by one."""
+    import torch
+    for n in idx:
+        src = d_src[n:n + 1].cpu().numpy()
+        ref = oracle.fused_norm(src, mean, std, None if recs is None else recs[n:n + 1], out_dtype=dt, layout=layout)
+        got = d_dst[n:n + 1].cpu()
+        got = got.view(torch.int16).numpy().view(np.uint16) if dt == F16 else got.numpy()
+        assert_parity(got, ref, dt, "image %d" % n)
+
+
+def test_large_batch_beyond_2_31_output_elements():
+    """16,384 x 224x224x3 to binary16: 2.47e9 output elements (4.9 GB), past
+    32-bit element indices; the tiled kernel with the dynamic schedule, the
+    oracle on the first, a middle and the last image."""
+    import torch
+    N, H, W, C = 16384, 224, 224, 3
+    assert N * H * W * C > 2 ** 31
+    g = torch.Generator(device="cuda").manual_seed(5)
+    d_src = torch.randint(0, 256, (N, H, W, C), dtype=torch.uint8, device="cuda", generator=g)
+    recs, _ = trfn.tr_sample_aug_params(77, 0, N, H, W)
+    d_dst = torch.empty((N, H, W, C), dtype=torch.float16, device="cuda")
+    mean = np.array(synth.IMAGENET_MEAN, np.float32)
+    std = np.array(synth.IMAGENET_STD, np.float32)
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    trfn.tr_fused_norm(d_src, d_dst, mean, std, torch.from_numpy(recs).cuda(), out_dtype=F16, workspace=ws)
+    torch.cuda.synchronize()
+    _sampled_check(d_src, d_dst, recs, [0, 1, N // 2, N - 2, N - 1], mean, std, F16, NHWC)
+    assert int(ws.count_nonzero()) == 0
+    del d_src, d_dst
+    torch.cuda.empty_cache()
+
+
+def test_generic_kernel_beyond_2_31_pixels():
+    """2,740,000 x 28x28x1 to binary32 (2.15e9 pixels): the per-element
+    kernel's 64-bit index path, checked on sampled images."""
+    import torch
+    N, H, W, C = 2_740_000, 28, 28, 1
+    assert N * H * W > 2 ** 31
+    g = torch.Generator(device="cuda").manual_seed(6)
+    d_src = torch.randint(0, 256, (N, H, W, C), dtype=torch.uint8, device="cuda", generator=g)
+    d_dst = torch.empty((N, H, W, C), dtype=torch.float32, device="cuda")
+    mean = np.array(synth.MNIST_MEAN, np.float32)
+    std = np.array(synth.MNIST_STD, np.float32)
+    trfn.tr_fused_norm(d_src, d_dst, mean, std, None, out_dtype=F32)
+    torch.cuda.synchronize()
+    _sampled_check(d_src, d_dst, None, [0, 1, N // 2, N - 1], mean, std, F32, NHWC)
+    del d_src, d_dst
+    torch.cuda.empty_cache()

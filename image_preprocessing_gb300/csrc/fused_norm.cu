@@ -270,6 +270,7 @@ struct TiledParams {
     int num_units;         // N * bands
     int gpr;               // groups per row, W / P
     uint64_t gpr_inv;      // ceil(2^32 / gpr): g / gpr == (g * gpr_inv) >> 32 for g, gpr < 2^16
+    uint64_t src_floor16;  // rows not a multiple of 16 bytes: the source's bytes rounded down to 16
     uint32_t in_stage;     // bytes per input stage (R*W*C, multiple of 16)
     uint32_t out_stage;    // bytes per output stage
     uint32_t plane_bytes;  // NCHW: bytes per plane of one band in the output stage (R*W*ob)
@@ -320,7 +321,7 @@ __device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, c
 // allowed and worth a copy) the 16-byte chunks that lie wholly inside the
 // erased source span of the erased
 // rows.
-template <int C, bool CROP>
+template <int C, bool CROP, bool ODD>
 __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem,
                                            const tr_aug_param& a, bool allow_skip, int2 origin) {
     const Band b = band_of(p, u);
@@ -352,6 +353,28 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
         mbar_arrive_expect_tx(bar, (uint32_t)p.R * p.in_pitch);
         tensor_g2s_4d(smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage, &p.tmap, 0, xb >> p.chunk_shift,
                       cy + y_begin, b.n, bar, (p.hints & 1) ? policy_evict_last() : policy_evict_first());
+        return;
+    }
+
+    if (ODD) {
+        // Rows that are not a multiple of 16 bytes: the band's bytes, from
+        // the 16-byte boundary below them, by one bulk copy; the band then
+        // starts `off` bytes into the stage (consumers realign), and any
+        // bytes past the source's last whole 16 are copied by this thread.
+        const uint64_t L = (uint64_t)p.W * C;
+        const uint64_t base = ((uint64_t)b.n * p.H + y_begin) * L;
+        const uint64_t end = base + (uint64_t)rows * L;
+        const uint64_t a0 = base & ~15ull;
+        uint64_t bulk_end = (end + 15) & ~15ull;
+        if (bulk_end > p.src_floor16) bulk_end = p.src_floor16 > a0 ? p.src_floor16 : a0;
+        rec->flags = flip | (int)((uint32_t)(base - a0) << 8);
+        uint8_t* stage = smem + kHeaderBytes + (size_t)s * p.in_stage;
+        for (uint64_t i = bulk_end; i < end; ++i) stage[i - a0] = p.src[i];
+        const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;   // full[s]
+        const uint32_t bulk = (uint32_t)(bulk_end - a0);
+        const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;   // bounded-wait test hook
+        mbar_arrive_expect_tx(bar, bulk + missing);
+        if (bulk > 0) load_bytes(p, smem_u32(stage), p.src + a0, bulk, bar);
         return;
     }
 
@@ -545,7 +568,75 @@ __device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout,
     }
 }
 
-template <int C, int OUT_F16, int LAYOUT, bool CROP>
+// Rows that are not a multiple of 16 bytes: the output tile mirrors the
+// band's global alignment (it starts at the band's global address mod 16,
+// per plane for NCHW), so its bulk store can cover the 16-byte aligned
+// middle; groups are written element by element, only their kv valid pixels.
+template <int C, int OUT_F16, int LAYOUT>
+__device__ __forceinline__ uint32_t odd_shift(const TiledParams& p, const UnitRec& rec, int c) {
+    constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    size_t e;   // the band's first output element in the plane or the tensor
+    if (LAYOUT == TR_LAYOUT_NCHW) e = (((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W;
+    else e = ((size_t)rec.n * p.H + rec.y_begin) * p.W * OC;
+    return (uint32_t)((uintptr_t)(p.dst + e * OB) & 15u);
+}
+
+template <int C, int OUT_F16, int LAYOUT>
+__device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* sout, const UnitRec& rec, int r,
+                                                int gx, int kv, const float (&v)[Group<C>::kBytes]) {
+    constexpr int P = Group<C>::P;
+    constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    auto put = [&](uint8_t* q, float x) {
+        if (OUT_F16) *reinterpret_cast<__half*>(q) = __float2half_rn(x);
+        else *reinterpret_cast<float*>(q) = x;
+    };
+    if (LAYOUT == TR_LAYOUT_NCHW) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) +
+                         ((size_t)r * p.W + (size_t)gx * P) * OB;
+#pragma unroll
+            for (int i = 0; i < P; ++i)
+                if (i < kv) put(o + (size_t)i * OB, v[i * C + c]);
+        }
+    } else {
+        // a pixel's outputs as one 4-, 8- or 16-byte store where they are
+        // that long and aligned, else element by element (runs of 4-byte
+        // stores for 6-byte binary16 pixels measured slower)
+        constexpr int PB = OC * OB;
+        uint8_t* o = sout + odd_shift<C, OUT_F16, LAYOUT>(p, rec, 0) + ((size_t)r * p.W + (size_t)gx * P) * PB;
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            if (i < kv) {
+                uint8_t* q = o + (size_t)i * PB;
+                uint32_t w[(PB + 3) / 4];
+                if (OUT_F16) {
+#pragma unroll
+                    for (int c = 0; c < OC; c += 2)
+                        w[c / 2] = pack_half2(c < C ? v[i * C + c] : 0.0f, c + 1 < C ? v[i * C + c + 1] : 0.0f);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < OC; ++c) w[c] = __float_as_uint(c < C ? v[i * C + c] : 0.0f);
+                }
+                constexpr int NW = (PB + 3) / 4;
+                if (PB == 16 && ((uintptr_t)q & 15u) == 0) {
+                    *reinterpret_cast<uint4*>(q) = make_uint4(w[0], w[1 % NW], w[2 % NW], w[3 % NW]);
+                } else if (PB == 8 && ((uintptr_t)q & 7u) == 0) {
+                    *reinterpret_cast<uint2*>(q) = make_uint2(w[0], w[1 % NW]);
+                } else if (PB == 4 && ((uintptr_t)q & 3u) == 0) {
+                    *reinterpret_cast<uint32_t*>(q) = w[0];
+                } else {
+#pragma unroll
+                    for (int c = 0; c < OC; ++c) put(q + (size_t)c * OB, c < C ? v[i * C + c] : 0.0f);
+                }
+            }
+        }
+    }
+}
+
+template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
 __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
                                              uint8_t* sout, const UnitRec& rec, int tid, int nthr) {
     constexpr int P = Group<C>::P;
@@ -556,6 +647,7 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
         const int r = (int)(((uint64_t)(uint32_t)g * p.gpr_inv) >> 32);
         const int gx = g - r * p.gpr;
         const int y = rec.y_begin + r;
+        const int kv = ODD ? min(P, p.W - gx * P) : P;   // valid pixels (the last group of an odd row is short)
         int lo = 0, hi = 0;  // erased pixels [lo, hi) of this group
         if (y >= rec.erow_lo && y < rec.erow_hi) {
             lo = min(max(rec.ecol_lo - gx * P, 0), P);
@@ -569,11 +661,22 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
             const int sgx = (rec.flags & 1) ? (p.gpr - 1 - gx) : gx;
             const uint8_t* s = sin + (size_t)r * L + (size_t)sgx * GB;
             uint32_t w[Group<C>::kWords];
-            if (CROP) {
-                // the group starts at any byte: aligned words, then funnel shifts
-                const uint32_t at = (uint32_t)r * p.in_pitch + (uint32_t)(rec.flags >> 8) + (uint32_t)sgx * GB;
-                const uint32_t* wp = reinterpret_cast<const uint32_t*>(sin + (at & ~3u));
-                const uint32_t sh = (at & 3u) * 8u;
+            if (CROP || ODD) {
+                // the group starts at any byte: aligned words, then funnel
+                // shifts.  For a short mirrored group of an odd row the
+                // window starts before the row (those pixels are dropped).
+                const uint32_t* wp;
+                uint32_t sh;
+                if (ODD) {
+                    const int src_px = (rec.flags & 1) ? (p.W - gx * P - P) : gx * P;
+                    const uint8_t* q = sin + ((int)(rec.flags >> 8) + r * L + src_px * C);
+                    wp = reinterpret_cast<const uint32_t*>((uintptr_t)q & ~(uintptr_t)3);
+                    sh = (uint32_t)((uintptr_t)q & 3u) * 8u;
+                } else {
+                    const uint32_t at = (uint32_t)r * p.in_pitch + (uint32_t)(rec.flags >> 8) + (uint32_t)sgx * GB;
+                    wp = reinterpret_cast<const uint32_t*>(sin + (at & ~3u));
+                    sh = (at & 3u) * 8u;
+                }
                 uint32_t raw[Group<C>::kWords + 1];
 #pragma unroll
                 for (int q = 0; q <= Group<C>::kWords; ++q) raw[q] = wp[q];
@@ -600,11 +703,12 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
                 }
             }
         }
-        store_group<C, OUT_F16, LAYOUT>(p, sout, r, gx, v);
+        if (ODD) store_group_odd<C, OUT_F16, LAYOUT>(p, sout, rec, r, gx, kv, v);
+        else store_group<C, OUT_F16, LAYOUT>(p, sout, r, gx, v);
     }
 }
 
-template <int C, int OUT_F16, int LAYOUT>
+template <int C, int OUT_F16, int LAYOUT, bool ODD>
 __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* sout,
                                            const UnitRec& rec) {
     constexpr int OB = OUT_F16 ? 2 : 4;
@@ -618,6 +722,40 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
         if (plain) bulk_s2g(g, from, bytes);
         else bulk_s2g_hint(g, from, bytes, pol);
     };
+    if (ODD) {
+        // per plane (NCHW) or for the band: the 16-byte aligned middle by a
+        // bulk store, the unaligned first and last bytes element by element
+        constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
+        constexpr int NP = (LAYOUT == TR_LAYOUT_NCHW) ? C : 1;
+#pragma unroll
+        for (int c = 0; c < NP; ++c) {
+            size_t e;
+            uint32_t bytes;
+            if (LAYOUT == TR_LAYOUT_NCHW) {
+                e = (((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W;
+                bytes = (uint32_t)rec.rows * p.W * OB;
+            } else {
+                e = ((size_t)rec.n * p.H + rec.y_begin) * p.W * OC;
+                bytes = (uint32_t)rec.rows * p.W * OC * OB;
+            }
+            uint8_t* g = p.dst + e * OB;
+            const uint32_t sh = (uint32_t)((uintptr_t)g & 15u);
+            const uint8_t* t = sout + (size_t)c * p.plane_bytes + sh;
+            const uint32_t head = min(bytes, (16u - sh) & 15u);
+            const uint32_t mid = (bytes - head) & ~15u;
+            for (uint32_t i = 0; i < head; i += OB) {
+                if (OUT_F16) *reinterpret_cast<uint16_t*>(g + i) = *reinterpret_cast<const uint16_t*>(t + i);
+                else *reinterpret_cast<uint32_t*>(g + i) = *reinterpret_cast<const uint32_t*>(t + i);
+            }
+            for (uint32_t i = head + mid; i < bytes; i += OB) {
+                if (OUT_F16) *reinterpret_cast<uint16_t*>(g + i) = *reinterpret_cast<const uint16_t*>(t + i);
+                else *reinterpret_cast<uint32_t*>(g + i) = *reinterpret_cast<const uint32_t*>(t + i);
+            }
+            if (mid > 0) put(g + head, src + (uint32_t)(c * p.plane_bytes + sh + head), mid);
+        }
+        bulk_commit();
+        return;
+    }
     if (LAYOUT == TR_LAYOUT_NCHW) {
         const uint32_t bytes = (uint32_t)rec.rows * p.W * OB;
 #pragma unroll
@@ -654,7 +792,7 @@ constexpr int kDoneWord = kTicketGroups * kTicketStride;
 // stage and issues the TMA store of the tile.
 // (An explicit minimum of one CTA per SM lets ptxas use up to 63 registers
 // here, against 61 without it, and measured 0.9 % faster at 256x224x224x3.)
-template <int C, int OUT_F16, int LAYOUT, bool CROP>
+template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
 __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ TiledParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
@@ -709,7 +847,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         // the first unit's band is requested before its record has arrived
         // (its erased span is then read too); measured 0.9 % faster at
         // 256x224x224x3 than waiting for the record
-        const bool early0 = !CROP && !(p.hints & 32) && u < p.num_units;
+        const bool early0 = !CROP && !ODD && !(p.hints & 32) && u < p.num_units;
         if (!early0 && u < p.num_units) a = unit_record(u);
         int j = 0;
         bool ok = true;
@@ -732,7 +870,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
             } else {
                 // a CTA's first S bands are copied whole (measured faster:
                 // they are the ramp every launch starts with)
-                issue_unit<C, CROP>(p, u, s, smem, a, (p.hints & 2048) || j >= S, org);
+                issue_unit<C, CROP, ODD>(p, u, s, smem, a, (p.hints & 2048) || j >= S, org);
             }
             // the next unit and its record: requested now, used after the
             // next empty wait
@@ -774,7 +912,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         const bool ok = mbar_wait_bounded(full0 + 8u * s, (uint32_t)(i / S) & 1u);
         const UnitRec rec = recs[s];
         uint8_t* ob = sout + (size_t)(i & 1) * p.out_stage;
-        if (ok) compute_unit<C, OUT_F16, LAYOUT, CROP>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
+        if (ok) compute_unit<C, OUT_F16, LAYOUT, CROP, ODD>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
         fence_proxy_async_smem();
         // The store issued last iteration reads the other output tile, which
         // the next iteration overwrites: it must be done reading first.
@@ -783,7 +921,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         if (rec.rows == 0) break;   // the producer's end mark
         if (storer) {
             mbar_arrive(empty0 + 8u * s);
-            store_unit<C, OUT_F16, LAYOUT>(p, ob, rec);
+            store_unit<C, OUT_F16, LAYOUT, ODD>(p, ob, rec);
         }
     }
     if (storer) {
@@ -942,32 +1080,35 @@ DeviceInfo device_info(int dev) {
 using TiledFn = void (*)(TiledParams);
 using GenericFn = void (*)(GenericParams);
 
-template <int C, int F16, bool CROP>
+template <int C, int F16, bool CROP, bool ODD>
 TiledFn pick_tiled_layout(int layout) {
     switch (layout) {
-    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC, CROP>;
-    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW, CROP>;
-    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4, CROP>;
+    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC, CROP, ODD>;
+    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW, CROP, ODD>;
+    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4, CROP, ODD>;
     }
 }
 
-template <int C, bool CROP>
+template <int C, bool CROP, bool ODD>
 TiledFn pick_tiled_dtype(int f16, int layout) {
-    return f16 ? pick_tiled_layout<C, 1, CROP>(layout) : pick_tiled_layout<C, 0, CROP>(layout);
+    return f16 ? pick_tiled_layout<C, 1, CROP, ODD>(layout) : pick_tiled_layout<C, 0, CROP, ODD>(layout);
 }
 
-template <bool CROP>
+template <bool CROP, bool ODD>
 TiledFn pick_tiled_c(int C, int f16, int layout) {
     switch (C) {
-    case 1: return pick_tiled_dtype<1, CROP>(f16, layout);
-    case 2: return pick_tiled_dtype<2, CROP>(f16, layout);
-    case 3: return pick_tiled_dtype<3, CROP>(f16, layout);
-    default: return pick_tiled_dtype<4, CROP>(f16, layout);
+    case 1: return pick_tiled_dtype<1, CROP, ODD>(f16, layout);
+    case 2: return pick_tiled_dtype<2, CROP, ODD>(f16, layout);
+    case 3: return pick_tiled_dtype<3, CROP, ODD>(f16, layout);
+    default: return pick_tiled_dtype<4, CROP, ODD>(f16, layout);
     }
 }
 
-TiledFn pick_tiled(int C, int f16, int layout, bool crop) {
-    return crop ? pick_tiled_c<true>(C, f16, layout) : pick_tiled_c<false>(C, f16, layout);
+// odd: compact sources whose rows (or NCHW output rows, or the output
+// pointer) are not 16-byte aligned
+TiledFn pick_tiled(int C, int f16, int layout, bool crop, bool odd) {
+    if (crop) return pick_tiled_c<true, false>(C, f16, layout);
+    return odd ? pick_tiled_c<false, true>(C, f16, layout) : pick_tiled_c<false, false>(C, f16, layout);
 }
 
 template <int C, int F16>
@@ -1012,7 +1153,7 @@ std::atomic<int> g_band_bytes{0}, g_stages{0}, g_ctas_per_sm{0}, g_flags{0};
 // pitch: bytes of one staged source row (W*C, or the crop box's chunks*chunk);
 // slack: extra bytes after a stage's rows (crop consumers read one word past).
 TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch, size_t slack,
-                       int R_force);
+                       int R_force, bool odd = false);
 
 TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch = 0,
                      size_t slack = 0) {
@@ -1043,13 +1184,16 @@ TiledPlan plan_tiled_crop(int H, int W, int C, int f16, int layout, int smem_lim
     return pl;
 }
 
+// odd: rows that are not a multiple of 16 bytes (the last group of a row is
+// short, and each output tile region gets 16 bytes to follow its band's
+// global alignment).
 TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch, size_t slack,
-                       int R_force) {
+                       int R_force, bool odd) {
     TiledPlan pl;
     const int ob = f16 ? 2 : 4;
     const int P = group_pixels(C);
     const size_t L = (size_t)W * C;
-    const int gpr = W / P;
+    const int gpr = odd ? (W + P - 1) / P : W / P;
     const int out_ch = (layout == TR_LAYOUT_NHWC4) ? 4 : C;
     const size_t out_row = (size_t)W * out_ch * ob;
     // About 32 KB of output per band (band_bytes overrides with source bytes);
@@ -1071,7 +1215,10 @@ TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit,
     if (pitch == 0) pitch = L;
     for (;;) {
         const size_t in_stage = round_up((size_t)R * pitch + slack, 128);
-        const size_t out_stage = round_up((size_t)R * out_row, 128);
+        const size_t plane = odd ? round_up((size_t)R * W * ob + 16, 16) : (size_t)R * W * ob;
+        const size_t out_stage = !odd ? round_up((size_t)R * out_row, 128)
+                                 : layout == TR_LAYOUT_NCHW ? round_up((size_t)C * plane, 128)
+                                                            : round_up((size_t)R * out_row + 16, 128);
         const size_t smem = kHeaderBytes + stages * in_stage + 2 * out_stage;
         if (in_stage < (1u << 20) && smem <= (size_t)smem_limit && R <= 256) {
             pl.ok = true;
@@ -1080,7 +1227,7 @@ TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit,
             pl.stages = stages;
             pl.in_stage = (uint32_t)in_stage;
             pl.out_stage = (uint32_t)out_stage;
-            pl.plane_bytes = (uint32_t)((size_t)R * W * ob);
+            pl.plane_bytes = (uint32_t)plane;
             pl.smem = smem;
             const int groups = R * gpr;
             pl.threads = 32 + (int)std::min<size_t>(224, std::max<size_t>(64, round_up(groups, 32)));
@@ -1174,8 +1321,12 @@ int launch_tiled(const LaunchArgs& a) {
     const size_t chunk = (size_t)1 << chunk_shift;
     const size_t nch = crop ? (L + 2 * (chunk - 1)) / chunk : 0;
     if (crop && nch > 256) return TR_ERR_NOT_SUPPORTED;
+    // compact sources whose rows, NCHW output rows or output pointer are
+    // not 16-byte aligned take the odd-row form of the kernel
+    const bool odd = !crop && !tiled_aligned(a.src, a.dst, a.W, a.C, f16, a.out_layout);
     const TiledPlan pl = crop ? plan_tiled_crop(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm,
                                                 di.smem_reserved, nch * chunk, 16)
+                        : odd ? plan_tiled_r(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, 0, 64, 0, true)
                               : plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin);
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 
@@ -1197,7 +1348,8 @@ int launch_tiled(const LaunchArgs& a) {
     p.R = pl.R;
     p.bands = pl.bands;
     p.num_units = a.N * pl.bands;
-    p.gpr = a.W / group_pixels(a.C);
+    p.gpr = odd ? (a.W + group_pixels(a.C) - 1) / group_pixels(a.C) : a.W / group_pixels(a.C);
+    p.src_floor16 = ((uint64_t)a.N * a.H * a.W * a.C) & ~15ull;
     p.gpr_inv = ((1ull << 32) + (uint64_t)p.gpr - 1) / (uint64_t)p.gpr;
     p.in_stage = pl.in_stage;
     p.out_stage = pl.out_stage;
@@ -1207,7 +1359,7 @@ int launch_tiled(const LaunchArgs& a) {
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 
-    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop);
+    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop, odd);
     // Per-kernel opt-in to the device's largest dynamic shared memory (once),
     // and the occupancy of each (threads, shared memory) geometry.
     struct Cached { const void* fn; int dev; size_t smem; int threads; int blocks; };
@@ -1304,20 +1456,34 @@ std::atomic<uint64_t> g_launches{0};
 
 }  // namespace
 
-bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C, int out_dtype,
-                     int out_layout) {
-    const int ob = (out_dtype == TR_OUT_F16) ? 2 : 4;
-    if (C < 1 || C > 4) return false;
+// The aligned form's conditions: 16-byte aligned pointers, source rows (and
+// NCHW output rows) a multiple of 16 bytes.
+bool tiled_aligned(const uint8_t* src, const void* dst, int W, int C, int f16, int out_layout) {
+    const int ob = f16 ? 2 : 4;
     if (((uintptr_t)src & 15u) != 0 || ((uintptr_t)dst & 15u) != 0) return false;
     if (((long long)W * C) % 16 != 0) return false;
     if (out_layout == TR_LAYOUT_NCHW && ((long long)W * ob) % 16 != 0) return false;
+    return true;
+}
+
+// The tiled kernel takes compact sources with a 16-byte aligned base; rows
+// of any length (the odd-row form realigns them).
+bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C, int out_dtype,
+                     int out_layout) {
+    (void)dst;
+    (void)out_dtype;
+    (void)out_layout;
+    if (C < 1 || C > 4) return false;
+    if (((uintptr_t)src & 15u) != 0) return false;
     if ((long long)N * H > (1LL << 31) - 1) return false;   // unit indices are int
+    if ((long long)W * C > (1 << 24)) return false;         // int byte offsets within a band
     return true;
 }
 
 bool tiled_crop_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C, int out_dtype,
                           int out_layout, int src_H, int src_W, size_t row_stride, size_t image_stride) {
     if (!tiled_supported(src, dst, N, H, W, C, out_dtype, out_layout)) return false;
+    if (!tiled_aligned(src, dst, W, C, out_dtype == TR_OUT_F16, out_layout)) return false;
     if (((size_t)src_W * C) % 16 != 0 || row_stride % 16 != 0 || image_stride % 16 != 0) return false;
     if (image_stride < (size_t)src_H * row_stride) return false;
     if (((size_t)W * C + 30) / 16 > 256) return false;

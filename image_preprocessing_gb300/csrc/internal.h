@@ -41,6 +41,11 @@ struct LaunchArgs {
 
 constexpr size_t kWorkspaceBytes = 2048;
 
+// Whether the tiled kernel's aligned form applies (16-byte aligned pointers,
+// rows and NCHW output rows a multiple of 16 bytes); otherwise a supported
+// compact source takes its odd-row form.
+bool tiled_aligned(const uint8_t* src, const void* dst, int W, int C, int f16, int out_layout);
+
 // Whether the tiled kernel's preconditions hold for these arguments.
 bool tiled_supported(const uint8_t* src, const void* dst, int N, int H, int W, int C,
                      int out_dtype, int out_layout);

@@ -91,8 +91,8 @@ def test_empty_batch_is_a_no_op():
 
 def test_forced_tiled_on_unsupported_shape_is_not_supported():
     L = _native.lib()
-    # W*C = 28 is not a multiple of 16
-    assert L.tr_fused_norm_variant(0x1000, 0x100000, 2, 28, 28, 1, M3, S3, None, 0, 0, None, 1) == NOT_SUPPORTED
+    # rows of more than 2^24 bytes
+    assert L.tr_fused_norm_variant(0x1000, 0x40000000, 1, 1, 1 << 23, 3, M3, S3, None, 0, 0, None, 1) == NOT_SUPPORTED
     # misaligned source pointer
     assert L.tr_fused_norm_variant(0x1001, 0x100000, 2, 32, 32, 3, M3, S3, None, 0, 0, None, 1) == NOT_SUPPORTED
 
@@ -103,7 +103,9 @@ def test_forced_tiled_on_unsupported_shape_is_not_supported():
     ((16, 32, 32, 3), 0, 0, 0x1000, 0x10000000, 2),   # small batch: the per-element kernel
     ((86, 32, 32, 3), 0, 0, 0x1000, 0x10000000, 1),   # 264,192 output elements
     ((200, 28, 28, 1), 0, 0, 0x1000, 0x10000000, 2),  # W*C = 28
-    ((128, 64, 12, 4), 1, 1, 0x1000, 0x10000000, 2),  # NCHW fp16 row of 24 bytes
+    ((128, 64, 12, 4), 1, 1, 0x1000, 0x10000000, 1),  # NCHW fp16 row of 24 bytes: the odd-row form
+    ((256, 227, 227, 3), 1, 0, 0x1000, 0x10000000, 1),  # 681-byte rows: the odd-row form
+    ((256, 224, 224, 3), 1, 0, 0x1000, 0x10000002, 1),  # dst 2 bytes off 16: the odd-row form
     ((128, 64, 12, 4), 0, 1, 0x1000, 0x10000000, 1),
     ((4, 8, 16, 3), 1, 0, 0x1008, 0x10000000, 2),     # src not 16-byte aligned
     ((4, 8, 16, 3), 1, 0, 0x1000, 0x10000004, 2),     # dst not 16-byte aligned

@@ -384,3 +384,33 @@ def test_generic_kernel_beyond_2_31_pixels():
     _sampled_check(d_src, d_dst, None, [0, 1, N // 2, N - 1], mean, std, F32, NHWC)
     del d_src, d_dst
     torch.cuda.empty_cache()
+
+
+ODD_SHAPES = [(3, 5, 7, 3), (4, 28, 28, 1), (2, 11, 13, 2), (1, 3, 5, 4), (5, 37, 227, 3), (2, 17, 299, 3),
+              (3, 9, 10, 1), (2, 64, 12, 4), (7, 3, 33, 3)]
+
+
+@pytest.mark.parametrize("shape", ODD_SHAPES)
+def test_odd_row_tiled_form(shape):
+    """Rows (or NCHW output rows, or the output pointer) that are not 16-byte
+    aligned: the tiled kernel's odd-row form (bands staged from the 16-byte
+    boundary below them and realigned, short last groups, output tiles that
+    follow the band's global alignment with element stores at both ends,
+    the batch's last bytes past its last whole 16 copied by the producer),
+    forced, against the oracle and the per-element kernel, with guard bytes,
+    both schedules and an output pointer 2 or 4 bytes off 16."""
+    import torch
+    N, H, W, C = shape
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(31 + N + W, N, H, W, allow_outside=True)
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    for dt in (F16, F32):
+        for layout in (NHWC, NCHW, NHWC4):
+            ref_g, _ = gpu_run(src, mean, std, aug, dt, layout, GENERIC)
+            for w, dst_off in ((None, 0), (ws.data_ptr(), 0), (None, 2 if dt == F16 else 4)):
+                got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED, workspace=w, dst_offset=dst_off)
+                assert np.array_equal(got, ref_g)
+    assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0

@@ -387,7 +387,8 @@ def test_generic_kernel_beyond_2_31_pixels():
 
 
 ODD_SHAPES = [(3, 5, 7, 3), (4, 28, 28, 1), (2, 11, 13, 2), (1, 3, 5, 4), (5, 37, 227, 3), (2, 17, 299, 3),
-              (3, 9, 10, 1), (2, 64, 12, 4), (7, 3, 33, 3)]
+              (3, 9, 10, 1), (2, 64, 12, 4), (7, 3, 33, 3),
+              (1, 1, 1, 1), (2, 1, 4099, 3), (1, 300, 1, 3), (64, 2, 2, 2), (3, 2, 15, 4)]
 
 
 @pytest.mark.parametrize("shape", ODD_SHAPES)

@@ -84,14 +84,18 @@ typedef struct tr_aug_param {
 } tr_aug_param;
 
 /* Kernel selection, for tests and benchmarks.  AUTO picks TILED whenever its
- * preconditions hold (16-byte aligned src/dst, W*C a multiple of 16, and for
- * NCHW W*sizeof(out) a multiple of 16) and the batch has at least 2^18 output
- * elements (below that the per-element kernel finishes first), else GENERIC.
- * Forcing TILED where its preconditions fail returns TR_ERR_NOT_SUPPORTED.  */
+ * preconditions hold (a 16-byte aligned source, rows of at most 2^24 bytes,
+ * fewer than 2^31 image rows) and the batch has at least 2^18 output elements
+ * (below that the per-element kernel finishes first), else GENERIC.  TILED
+ * runs its aligned form when dst is 16-byte aligned, W*C is a multiple of 16
+ * and, for NCHW, W*sizeof(out) is a multiple of 16; otherwise its odd-row
+ * form (bands realigned in shared memory, unaligned ends of the output
+ * stored element by element), about half as fast.  Forcing TILED where its
+ * preconditions fail returns TR_ERR_NOT_SUPPORTED.                          */
 typedef enum tr_variant {
     TR_VARIANT_AUTO = 0,
     TR_VARIANT_TILED = 1,     /* persistent CTAs, TMA bulk row-band staging, TMA bulk stores */
-    TR_VARIANT_GENERIC = 2    /* one thread per output element, any shape and alignment      */
+    TR_VARIANT_GENERIC = 2    /* one thread per output pixel, any shape, stride and alignment */
 } tr_variant;
 
 /* ------------------------------------------------------------------------
@@ -116,7 +120,8 @@ typedef enum tr_variant {
  * dst or aug_params off their element alignment, non-finite or zero std,
  * overlapping src/dst, sizes beyond 2^40 elements),
  * TR_ERR_NOT_SUPPORTED (C > 4), TR_ERR_CUDA (launch failure).  Pointers off
- * a 16-byte boundary are not an error: they take the GENERIC kernel.         */
+ * a 16-byte boundary are not an error: a source off 16 bytes takes the
+ * GENERIC kernel, an output off 16 bytes the TILED kernel's odd-row form.   */
 int tr_fused_norm(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
                   const float* mean, const float* std, const tr_aug_param* aug_params,
                   int out_dtype, int out_layout, void* stream);

@@ -415,3 +415,31 @@ def test_odd_row_tiled_form(shape):
                 assert np.array_equal(got, ref_g)
     assert int(ws.count_nonzero()) == 0
     assert trfn.tr_device_status() == 0
+
+
+def test_concurrent_streams_with_their_own_workspaces():
+    """Launches on four streams at once, each with its own workspace (the
+    rule for launches that may overlap): every output matches the oracle and
+    every workspace is zero again."""
+    import torch
+    N, H, W, C = 48, 224, 224, 3
+    mean, std = IMNET
+    K = 4
+    srcs = [synth.pixels_uniform(60 + i, N, H, W, C) for i in range(K)]
+    augs = [oracle.sample_aug_params(70 + i, 0, N, H, W)[0] for i in range(K)]
+    d_src = [torch.from_numpy(x).cuda() for x in srcs]
+    d_aug = [torch.from_numpy(a).cuda() for a in augs]
+    outs = [torch.empty((N, H, W, C), dtype=torch.float16, device="cuda") for _ in range(K)]
+    wss = [_workspace() for _ in range(K)]
+    streams = [torch.cuda.Stream() for _ in range(K)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for i in range(K):
+            trfn.tr_fused_norm(d_src[i], outs[i], mean, std, d_aug[i], out_dtype=F16, stream=streams[i],
+                               workspace=wss[i])
+    torch.cuda.synchronize()
+    for i in range(K):
+        assert int(wss[i].count_nonzero()) == 0
+        ref = oracle.fused_norm(srcs[i], mean, std, augs[i], out_dtype=F16)
+        assert_parity(outs[i].cpu().view(torch.int16).numpy().view(np.uint16), ref, F16, "stream %d" % i)
+    assert trfn.tr_device_status() == 0

@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--crop", type=int, default=0,
                     help="read each image as a window of an SxS source (random origins when the workload "
                          "flips/erases, else the centre): tr_fused_norm_crop")
+    ap.add_argument("--size", default=None,
+                    help="override the config's image size as HxW (e.g. 299x299: rows of 897 bytes, the "
+                         "odd-row form of the tiled kernel)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
     ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
     ap.add_argument("--fused-sampling", action="store_true",
@@ -219,6 +222,13 @@ def workload(args):
     if args.batch:
         name = name.replace("n%d_" % cfg["N"], "n%d_" % args.batch, 1)
         cfg["N"] = args.batch
+    size = getattr(args, "size", None)
+    if size:
+        H, W = (int(v) for v in size.lower().split("x"))
+        if H < 1 or W < 1:
+            raise SystemExit("--size wants HxW with H, W >= 1")
+        name = name.replace("_%dx%dx%d_" % (cfg["H"], cfg["W"], cfg["C"]), "_%dx%dx%d_" % (H, W, cfg["C"]), 1)
+        cfg["H"], cfg["W"] = H, W
     cfg["crop"] = getattr(args, "crop", 0)
     if cfg["crop"]:
         name += "_crop_from_%dx%d" % (cfg["crop"], cfg["crop"])
@@ -411,7 +421,7 @@ def run_ours(args, rank, local, world, pg):
     if not args.no_e2e:
         e2e = run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg)
     pipeline = None
-    if not args.no_pipeline and args.config == 3 and not S and not args.batch and not args.layout:
+    if not args.no_pipeline and args.config == 3 and not S and not args.batch and not args.layout and not args.size:
         pipeline = run_pipeline(dev, rank, pg)
 
     value = aggregate_images_per_s(world, N, K, ms_max)

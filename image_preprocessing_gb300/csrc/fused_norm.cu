@@ -582,6 +582,75 @@ __device__ __forceinline__ uint32_t odd_shift(const TiledParams& p, const UnitRe
     return (uint32_t)((uintptr_t)(p.dst + e * OB) & 15u);
 }
 
+// Writes len bytes (at least 16 - (s0 & 15), a multiple of EB) of the word
+// stream w to tile + s0 (s0 a multiple of EB, tile 16-byte aligned), using
+// only 16-byte stores for the chunks the range covers whole and at most three
+// 2-, 4- or 8-byte stores at each end.  The stream is first moved to the
+// tile's 16-byte frame: a funnel shift by s0 & 3 bytes, then a shift by
+// (s0 >> 2) & 3 words in two select steps (registers only).  A chunk shared
+// with a neighbouring group receives only this group's bytes, so threads
+// writing neighbouring groups never touch the same bytes.
+template <int NW, int EB>
+__device__ __forceinline__ void put_stream(uint8_t* tile, uint32_t s0, uint32_t len, const uint32_t (&w)[NW]) {
+    constexpr int NC = (4 * NW + 30) / 16;   // 16-byte chunks the range can touch
+    constexpr int NO = 4 * NC;
+    const uint32_t d = s0 & 15u, e = d + len;
+    uint8_t* a = tile + (s0 - d);
+    uint32_t sb[NW + 1];
+    if (EB >= 4) {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) sb[i] = w[i];
+        sb[NW] = 0u;
+    } else {
+        const uint32_t db = (d & 3u) * 8u;
+        sb[0] = __funnelshift_l(0u, w[0], db);
+#pragma unroll
+        for (int i = 1; i < NW; ++i) sb[i] = __funnelshift_l(w[i - 1], w[i], db);
+        sb[NW] = __funnelshift_l(w[NW - 1], 0u, db);
+    }
+    const uint32_t dw = d >> 2;
+    uint32_t t1[NO], o[NO];
+#pragma unroll
+    for (int j = 0; j < NO; ++j) {
+        const uint32_t x0 = j <= NW ? sb[j] : 0u;
+        const uint32_t x1 = (j >= 1 && j - 1 <= NW) ? sb[j - 1] : 0u;
+        t1[j] = (dw & 1u) ? x1 : x0;
+    }
+#pragma unroll
+    for (int j = 0; j < NO; ++j) o[j] = (dw & 2u) ? (j >= 2 ? t1[j - 2] : 0u) : t1[j];
+    // the first chunk's part from byte d on
+    if (d != 0) {
+        const uint32_t s = 16u - d;
+        if (s & 8u) *reinterpret_cast<uint2*>(a + 8) = make_uint2(o[2], o[3]);
+        if (s & 4u) *reinterpret_cast<uint32_t*>(a + ((s & 8u) ? 4 : 12)) = (s & 8u) ? o[1] : o[3];
+        if (EB < 4 && (s & 2u)) {
+            const uint32_t lo = (d & 4u) ? o[1] : o[0], hi = (d & 4u) ? o[3] : o[2];
+            *reinterpret_cast<uint16_t*>(a + d) = (uint16_t)(((d & 8u) ? hi : lo) >> 16);
+        }
+    }
+    // whole chunks
+    const uint32_t kt = e >> 4;
+#pragma unroll
+    for (int k = 0; k < NC; ++k)
+        if ((k > 0 || d == 0) && (uint32_t)k < kt)
+            *reinterpret_cast<uint4*>(a + 16 * k) = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+    // the last chunk's part below byte e & 15
+    const uint32_t t = e & 15u;
+    if (t != 0) {
+        uint32_t c0 = o[4], c1 = o[5], c2 = o[6], c3 = o[7];
+#pragma unroll
+        for (int k = 2; k < NC; ++k)
+            if (kt == (uint32_t)k) { c0 = o[4 * k]; c1 = o[4 * k + 1]; c2 = o[4 * k + 2]; c3 = o[4 * k + 3]; }
+        uint8_t* q = a + 16u * kt;
+        if (t & 8u) *reinterpret_cast<uint2*>(q) = make_uint2(c0, c1);
+        if (t & 4u) *reinterpret_cast<uint32_t*>(q + (t & 8u)) = (t & 8u) ? c2 : c0;
+        if (EB < 4 && (t & 2u)) {
+            const uint32_t lo = (t & 4u) ? c1 : c0, hi = (t & 4u) ? c3 : c2;
+            *reinterpret_cast<uint16_t*>(q + (t & 12u)) = (uint16_t)((t & 8u) ? hi : lo);
+        }
+    }
+}
+
 template <int C, int OUT_F16, int LAYOUT>
 __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* sout, const UnitRec& rec, int r,
                                                 int gx, int kv, const float (&v)[Group<C>::kBytes]) {
@@ -592,6 +661,55 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
         if (OUT_F16) *reinterpret_cast<__half*>(q) = __float2half_rn(x);
         else *reinterpret_cast<float*>(q) = x;
     };
+    // Register realignment pays where the element path stores 2-, 4- or
+    // 12-byte pixels or short planes element by element: NHWC pixels of 2, 4,
+    // 6 or 12 bytes, NCHW plane runs of 32 bytes or more.  Pixels of 8 or 16
+    // bytes keep one aligned store each, and 16-byte plane runs would spend
+    // more on the shifts than they save (measured at 256x299x299).
+    constexpr bool kStreamNHWC = LAYOUT == TR_LAYOUT_NHWC && (C * OB) % 8 != 0;
+    constexpr bool kStreamNCHW = LAYOUT == TR_LAYOUT_NCHW && P * OB >= 32;
+    const bool streams = !(p.hints & 1024);
+    if (kStreamNHWC && streams) {
+        // the group's kv pixels are one run of output bytes
+        constexpr int NW = P * C * OB / 4;
+        const uint32_t s0 = odd_shift<C, OUT_F16, LAYOUT>(p, rec, 0) + ((uint32_t)r * p.W + (uint32_t)gx * P) * (C * OB);
+        const uint32_t len = (uint32_t)kv * (C * OB);
+        if ((s0 & 15u) + len >= 16u) {
+            uint32_t w[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                if constexpr (OUT_F16 != 0) w[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+                else w[i] = __float_as_uint(v[i]);
+            }
+            put_stream<NW, OB>(sout, s0, len, w);
+            return;
+        }
+    }
+    if (kStreamNCHW && streams) {
+        // per plane, the group's kv pixels are one run of output bytes
+        constexpr int NW = P * OB / 4;
+        const uint32_t at = ((uint32_t)r * p.W + (uint32_t)gx * P) * OB;
+        const uint32_t len = (uint32_t)kv * OB;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const uint32_t s0 = odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) + at;
+            uint8_t* plane = sout + (size_t)c * p.plane_bytes;
+            if ((s0 & 15u) + len >= 16u) {
+                uint32_t w[NW];
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    if constexpr (OUT_F16 != 0) w[i] = pack_half2(v[(2 * i) * C + c], v[(2 * i + 1) * C + c]);
+                    else w[i] = __float_as_uint(v[i * C + c]);
+                }
+                put_stream<NW, OB>(plane, s0, len, w);
+            } else {
+#pragma unroll
+                for (int i = 0; i < P; ++i)
+                    if (i < kv) put(plane + s0 + (size_t)i * OB, v[i * C + c]);
+            }
+        }
+        return;
+    }
     if (LAYOUT == TR_LAYOUT_NCHW) {
 #pragma unroll
         for (int c = 0; c < C; ++c) {
@@ -1153,7 +1271,7 @@ std::atomic<int> g_band_bytes{0}, g_stages{0}, g_ctas_per_sm{0}, g_flags{0};
 // pitch: bytes of one staged source row (W*C, or the crop box's chunks*chunk);
 // slack: extra bytes after a stage's rows (crop consumers read one word past).
 TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch, size_t slack,
-                       int R_force, bool odd = false);
+                       int R_force, bool odd = false, int S_force = 0);
 
 TiledPlan plan_tiled(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch = 0,
                      size_t slack = 0) {
@@ -1165,30 +1283,134 @@ int smem_residency(const TiledPlan& pl, int smem_per_sm, int reserved) {
     return pl.ok ? (int)((size_t)smem_per_sm / (pl.smem + (size_t)reserved)) : 0;
 }
 
-// A crop box stages wider rows than the window (whole chunks), which can cost
-// one resident CTA per SM against the compact geometry; then take the largest
-// lower band height (down to half, divisors of H first) that restores it.
-TiledPlan plan_tiled_crop(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm,
-                          int reserved, size_t pitch, size_t slack) {
-    const TiledPlan pl = plan_tiled(H, W, C, f16, layout, smem_limit, pitch, slack);
+// The largest lower band height (down to half, divisors of H first, same
+// stage count) at which `want` CTAs fit an SM's shared memory; pl itself if
+// it already fits them, or if no such height exists or the band height is set
+// by tr_tune_tiled.
+TiledPlan lower_to_residency(const TiledPlan& pl, int want, int H, int W, int C, int f16, int layout,
+                             int smem_limit, int smem_per_sm, int reserved, size_t pitch, size_t slack, bool odd) {
     if (!pl.ok || smem_per_sm <= 0 || g_band_bytes.load(std::memory_order_relaxed) > 0) return pl;
-    const int want = smem_residency(plan_tiled(H, W, C, f16, layout, smem_limit), smem_per_sm, reserved);
     if (smem_residency(pl, smem_per_sm, reserved) >= want) return pl;
     for (int pass = 0; pass < 2; ++pass) {
         for (int r = pl.R - 1; r >= (pl.R + 1) / 2 && r >= 1; --r) {
             if (pass == 0 && H % r != 0) continue;
-            const TiledPlan q = plan_tiled_r(H, W, C, f16, layout, smem_limit, pitch, slack, r);
+            const TiledPlan q = plan_tiled_r(H, W, C, f16, layout, smem_limit, pitch, slack, r, odd);
             if (q.ok && q.stages == pl.stages && smem_residency(q, smem_per_sm, reserved) >= want) return q;
         }
     }
     return pl;
 }
 
+// Compact sources: the band height of about 32 KB of output per band, lowered
+// where that leaves fewer than three CTAs on an SM (wide rows: at 256x299x299
+// binary16 13-row bands fit two).  Three resident CTAs keep three times
+// `stages` bands in flight per SM and 21 converting warps.  Only for plans of
+// at most three stages (bands above 8 KB of source): at 256x224x224 it takes
+// 3-stage binary16 plans from 0.53 to 0.59 of the copy peak (grayscale), 0.84
+// to 0.88 (four channels), 256x256x3 from 0.84 to 0.88, while the 4-stage
+// binary32 plans it would touch ran 1-3 % slower with three CTAs of smaller
+// bands than with two.  tr_tune_tiled flags bit 16 keeps the 32 KB height.
+constexpr int kWantResidency = 3;
+constexpr long long kStreamMinBandsPerCta = 5;
+
+// Share of the consumer threads' group slots that hold a group: consumers
+// walk a band's groups in strides of their thread count and all meet at the
+// end of the band, so a last stride that is mostly empty idles most of them.
+double stride_fill(const TiledPlan& pl, int gpr) {
+    const long long groups = (long long)pl.R * gpr;
+    const long long nc = pl.threads - 32;
+    const long long strides = (groups + nc - 1) / nc;
+    return strides > 0 ? (double)groups / (double)(strides * nc) : 0.0;
+}
+
+// The largest height from pl.R down to half (same stage count, at least
+// `want` CTAs per SM) whose strides are at least 84 % full; pl if none is.
+// Measured at 256x299x299 (38 groups a row for RGB, 19 for grayscale):
+// binary16 RGB 12 rows (456 groups: 68 % full) 0.58 of the copy peak, 11 rows
+// (93 %) 0.60; binary32 RGB 7 rows (59 %) 0.83, 5 rows (99 %) 0.93; grayscale
+// 36 rows (76 %) 0.37, 23 rows (98 %) 0.43.  tr_tune_tiled flags bit 18
+// keeps the height as it was.
+constexpr double kMinStrideFill = 0.84;
+
+TiledPlan balance_strides(const TiledPlan& pl, int want, int H, int W, int C, int f16, int layout, int smem_limit,
+                          int smem_per_sm, int reserved, size_t pitch, size_t slack, bool odd) {
+    if (!pl.ok || g_band_bytes.load(std::memory_order_relaxed) > 0) return pl;
+    if (g_flags.load(std::memory_order_relaxed) & 262144) return pl;
+    const int P = group_pixels(C);
+    const int gpr = odd ? (W + P - 1) / P : W / P;
+    if (stride_fill(pl, gpr) >= kMinStrideFill) return pl;
+    for (int r = pl.R - 1; r >= (pl.R + 1) / 2 && r >= 1; --r) {
+        const TiledPlan q = plan_tiled_r(H, W, C, f16, layout, smem_limit, pitch, slack, r, odd);
+        if (q.ok && q.stages == pl.stages && smem_residency(q, smem_per_sm, reserved) >= want &&
+            stride_fill(q, gpr) >= kMinStrideFill)
+            return q;
+    }
+    return pl;
+}
+
+TiledPlan plan_tiled_compact(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm,
+                             int reserved, bool odd, long long N, int sm_count) {
+    const size_t slack = odd ? 64 : 0;
+    const TiledPlan pl = plan_tiled_r(H, W, C, f16, layout, smem_limit, 0, slack, 0, odd);
+    if (g_flags.load(std::memory_order_relaxed) & 65536) return pl;
+    // 4-stage plans (small bands) are lowered only where each CTA gets few
+    // bands, so that latency, not bandwidth, bounds the launch (1024x50x50x3
+    // to binary32: 0.48 -> 0.55 of the copy peak with the lower height)
+    const long long slots = (long long)std::max(1, smem_residency(pl, smem_per_sm, reserved)) * std::max(1, sm_count);
+    const bool few_bands = pl.ok && N * pl.bands < kStreamMinBandsPerCta * slots;
+    const TiledPlan fit = (pl.stages > 3 && !few_bands)
+                              ? pl
+                              : lower_to_residency(pl, kWantResidency, H, W, C, f16, layout, smem_limit, smem_per_sm,
+                                                   reserved, 0, slack, odd);
+    const int want = std::min(kWantResidency, smem_residency(fit, smem_per_sm, reserved));
+    return balance_strides(fit, want, H, W, C, f16, layout, smem_limit, smem_per_sm, reserved, 0, slack, odd);
+}
+
+// The odd-row form is bound by its conversion (realigning loads, element or
+// realigned stores), not by copies in flight: two stages, and the largest
+// height from the 32 KB one down to half at which the most CTAs per SM (up to
+// four, as the kernel's registers allow: reg_res) fit with strides at least
+// 84 % full.  The launch takes this plan only where each CTA streams at least
+// five bands and it raises the CTAs per SM.  Measured at 256x299x299 against
+// the aligned form's planning (three stages, three CTAs): binary16 RGB NHWC
+// 0.60 -> 0.67 of the copy peak (10-row bands, four CTAs), 256x227x227 0.56 ->
+// 0.59, grayscale 0.39 -> 0.43, two channels 0.49 -> 0.53.  tr_tune_tiled
+// flags bit 19 plans the odd-row form like the aligned one.
+TiledPlan plan_tiled_odd(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm, int reserved,
+                         int reg_res) {
+    const int sknob = g_stages.load(std::memory_order_relaxed);
+    const int S = sknob >= 2 ? sknob : 2;
+    const TiledPlan base = plan_tiled_r(H, W, C, f16, layout, smem_limit, 0, 64, 0, true, S);
+    if (!base.ok || smem_per_sm <= 0 || g_band_bytes.load(std::memory_order_relaxed) > 0) return base;
+    const int gpr = (W + group_pixels(C) - 1) / group_pixels(C);
+    for (int want = std::max(1, std::min(4, reg_res)); want >= 1; --want) {
+        for (int r = base.R; r >= (base.R + 1) / 2 && r >= 1; --r) {
+            const TiledPlan q = plan_tiled_r(H, W, C, f16, layout, smem_limit, 0, 64, r, true, S);
+            if (q.ok && q.stages == base.stages && smem_residency(q, smem_per_sm, reserved) >= want &&
+                stride_fill(q, gpr) >= kMinStrideFill)
+                return q;
+        }
+    }
+    return base;
+}
+
+// A crop box stages wider rows than the window (whole chunks), which can cost
+// one resident CTA per SM against the compact geometry; then take the largest
+// lower band height that restores it.
+TiledPlan plan_tiled_crop(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm,
+                          int reserved, size_t pitch, size_t slack, long long N, int sm_count) {
+    const TiledPlan pl = plan_tiled(H, W, C, f16, layout, smem_limit, pitch, slack);
+    const int want = smem_residency(plan_tiled_compact(H, W, C, f16, layout, smem_limit, smem_per_sm, reserved, false,
+                                                       N, sm_count),
+                                    smem_per_sm, reserved);
+    return lower_to_residency(pl, want, H, W, C, f16, layout, smem_limit, smem_per_sm, reserved, pitch, slack, false);
+}
+
 // odd: rows that are not a multiple of 16 bytes (the last group of a row is
 // short, and each output tile region gets 16 bytes to follow its band's
 // global alignment).
 TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit, size_t pitch, size_t slack,
-                       int R_force, bool odd) {
+                       int R_force, bool odd, int S_force) {
     TiledPlan pl;
     const int ob = f16 ? 2 : 4;
     const int P = group_pixels(C);
@@ -1203,14 +1425,19 @@ TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit,
     const int knob = g_band_bytes.load(std::memory_order_relaxed);
     int R = (int)std::max<size_t>(1, std::min<size_t>((size_t)H, knob > 0 ? (size_t)knob / L
                                                                           : 32768 / out_row));
+    bool divides = false;
     for (int r = R; r >= (R + 1) / 2; --r) {
-        if (H % r == 0) { R = r; break; }
+        if (H % r == 0) { R = r; divides = true; break; }
     }
+    // otherwise the same number of bands with heights as even as a fixed
+    // height allows (75 rows at a 72-row target: 38 + 37, not 72 + 3)
+    if (!divides) R = (H + (H + R - 1) / R - 1) / ((H + R - 1) / R);
     if (R_force > 0) R = std::min(R_force, H);
     while (R > 1 && (size_t)R * gpr >= 65536) --R;
     if ((size_t)R * gpr >= 65536) return pl;
     const int sknob = g_stages.load(std::memory_order_relaxed);
-    const int stages0 = std::min(sknob >= 2 ? sknob : ((size_t)R * L > 8192 ? 3 : 4), kMaxStages);
+    const int stages0 = std::min(S_force >= 2 ? S_force : sknob >= 2 ? sknob : ((size_t)R * L > 8192 ? 3 : 4),
+                                 kMaxStages);
     int stages = stages0;
     if (pitch == 0) pitch = L;
     for (;;) {
@@ -1302,6 +1529,42 @@ int encode_crop_map(CUtensorMap* map, const LaunchArgs& a, uint32_t chunk, uint3
     return TR_OK;
 }
 
+// CTAs of fn with this many threads and bytes of dynamic shared memory that
+// fit one SM (cached per kernel, device and geometry), after the kernel's
+// one-time opt-in to the device's largest dynamic shared memory.
+int tiled_occupancy(TiledFn fn, int dev, int smem_optin, int threads, size_t smem, int* blocks) {
+    struct Cached { const void* fn; int dev; size_t smem; int threads; int blocks; };
+    static std::mutex mu;
+    static Cached cache[256];
+    static int ncache = 0;
+    static const void* opted[64][64];
+    static int nopted[64];
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= 64) return TR_ERR_CUDA;
+    bool done = false;
+    for (int k = 0; k < nopted[dev]; ++k) done = done || opted[dev][k] == (const void*)fn;
+    if (!done) {
+        if (!check_cuda(cudaFuncSetAttribute((const void*)fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin),
+                        "cudaFuncSetAttribute"))
+            return TR_ERR_CUDA;
+        if (nopted[dev] < 64) opted[dev][nopted[dev]++] = (const void*)fn;
+    }
+    for (int k = 0; k < ncache; ++k) {
+        if (cache[k].fn == (const void*)fn && cache[k].dev == dev && cache[k].smem == smem &&
+            cache[k].threads == threads) {
+            *blocks = cache[k].blocks;
+            return TR_OK;
+        }
+    }
+    int b = 0;
+    if (!check_cuda(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, (const void*)fn, threads, smem),
+                    "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
+        return TR_ERR_CUDA;
+    if (ncache < 256 && b > 0) cache[ncache++] = Cached{(const void*)fn, dev, smem, threads, b};
+    *blocks = b;
+    return TR_OK;
+}
+
 int launch_tiled(const LaunchArgs& a) {
     int dev = 0;
     if (!check_cuda(cudaGetDevice(&dev), "cudaGetDevice")) return TR_ERR_CUDA;
@@ -1324,10 +1587,40 @@ int launch_tiled(const LaunchArgs& a) {
     // compact sources whose rows, NCHW output rows or output pointer are
     // not 16-byte aligned take the odd-row form of the kernel
     const bool odd = !crop && !tiled_aligned(a.src, a.dst, a.W, a.C, f16, a.out_layout);
-    const TiledPlan pl = crop ? plan_tiled_crop(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm,
-                                                di.smem_reserved, nch * chunk, 16)
-                        : odd ? plan_tiled_r(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, 0, 64, 0, true)
-                              : plan_tiled(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin);
+    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop, odd);
+    TiledPlan pl;
+    if (crop) {
+        pl = plan_tiled_crop(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
+                             nch * chunk, 16, a.N, di.sm_count);
+    } else if (odd && !(tflags & 524288)) {
+        // Launches in which each CTA streams many bands are bound by the
+        // conversion: there the odd-row planning (two stages, more CTAs per
+        // SM) is taken when it does raise the CTAs per SM.  With few bands a
+        // CTA the copies' latency dominates and the aligned form's planning
+        // does better (100x100 and 50x50 images), as it does where the odd-row
+        // planning cannot add a CTA (binary32 RGB, 4-channel outputs).
+        pl = plan_tiled_compact(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
+                                true, a.N, di.sm_count);
+        int res = 0, reg_res = 0;
+        int rc = pl.ok ? tiled_occupancy(fn, dev, di.smem_optin, pl.threads, pl.smem, &res) : TR_OK;
+        if (rc == TR_OK) rc = tiled_occupancy(fn, dev, di.smem_optin, 256, 0, &reg_res);
+        if (rc != TR_OK) return rc;
+        const long long units = (long long)a.N * pl.bands;
+        const long long slots = (long long)std::max(1, res) * di.sm_count;
+        if (pl.ok && (units + slots - 1) / slots >= kStreamMinBandsPerCta) {
+            const TiledPlan q = plan_tiled_odd(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm,
+                                               di.smem_reserved, reg_res);
+            int qres = 0;
+            if (q.ok) {
+                rc = tiled_occupancy(fn, dev, di.smem_optin, q.threads, q.smem, &qres);
+                if (rc != TR_OK) return rc;
+            }
+            if (qres > res) pl = q;
+        }
+    } else {
+        pl = plan_tiled_compact(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
+                                odd, a.N, di.sm_count);
+    }
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 
     TiledParams p;
@@ -1355,47 +1648,15 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
-    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 2048 | 0xF000);
+    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000);
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 
-    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop, odd);
-    // Per-kernel opt-in to the device's largest dynamic shared memory (once),
-    // and the occupancy of each (threads, shared memory) geometry.
-    struct Cached { const void* fn; int dev; size_t smem; int threads; int blocks; };
-    static std::mutex mu;
-    static Cached cache[256];
-    static int ncache = 0;
-    static const void* opted[64][64];
-    static int nopted[64];
     int blocks_per_sm = 0;
     {
-        std::lock_guard<std::mutex> lock(mu);
-        bool done = false;
-        for (int k = 0; k < nopted[dev]; ++k) done = done || opted[dev][k] == (const void*)fn;
-        if (!done) {
-            if (!check_cuda(cudaFuncSetAttribute((const void*)fn,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 di.smem_optin),
-                            "cudaFuncSetAttribute"))
-                return TR_ERR_CUDA;
-            if (nopted[dev] < 64) opted[dev][nopted[dev]++] = (const void*)fn;
-        }
-        for (int k = 0; k < ncache; ++k) {
-            if (cache[k].fn == (const void*)fn && cache[k].dev == dev && cache[k].smem == pl.smem &&
-                cache[k].threads == pl.threads) {
-                blocks_per_sm = cache[k].blocks;
-                break;
-            }
-        }
-        if (blocks_per_sm == 0) {
-            if (!check_cuda(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, (const void*)fn,
-                                                                         pl.threads, pl.smem),
-                            "cudaOccupancyMaxActiveBlocksPerMultiprocessor"))
-                return TR_ERR_CUDA;
-            if (blocks_per_sm <= 0) return TR_ERR_NOT_SUPPORTED;
-            if (ncache < 256) cache[ncache++] = Cached{(const void*)fn, dev, pl.smem, pl.threads, blocks_per_sm};
-        }
+        const int rc = tiled_occupancy(fn, dev, di.smem_optin, pl.threads, pl.smem, &blocks_per_sm);
+        if (rc != TR_OK) return rc;
+        if (blocks_per_sm <= 0) return TR_ERR_NOT_SUPPORTED;
     }
     const int cap = g_ctas_per_sm.load(std::memory_order_relaxed);
     if (cap > 0) blocks_per_sm = std::min(blocks_per_sm, cap);
@@ -1404,6 +1665,15 @@ int launch_tiled(const LaunchArgs& a) {
     // equalise the number of units per CTA
     const long long waves = (p.num_units + grid - 1) / grid;
     grid = (p.num_units + waves - 1) / waves;
+    // The odd-row form's register realignment of group outputs lengthens a
+    // band's conversion: it pays when a CTA streams many bands (6 to 13 for
+    // 227- and 299-pixel rows: 0.51 to 0.56 and 0.53 to 0.58 of the copy peak
+    // for binary16 RGB NHWC, 0.64 to 0.83 for binary32, 0.36 to 0.37 for
+    // binary16 grayscale), not when each CTA converts one to four bands and
+    // the conversion is on the critical path (28x28 to 100x100 images: 2-12 %
+    // slower).  Those launches keep the element stores (tr_tune_tiled flags
+    // bit 17 asks for the realignment regardless).
+    if (odd && waves < kStreamMinBandsPerCta && !(tflags & 131072)) p.hints |= 1024;
 
     if (!check_cuda(launch_pdl((const void*)fn, (unsigned)grid, pl.threads, pl.smem, a.stream, &p),
                     "tiled kernel launch"))

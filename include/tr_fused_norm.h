@@ -471,11 +471,18 @@ int tr_device_status(int* flags, int clear);
  * 0 keeps the default for that knob):
  *   band_bytes       source bytes per row band (default: about 32 KB of
  *                    output per band; the band height is the largest divisor
- *                    of H near the target, else the target; crop sources may
- *                    lower it so that as many CTAs fit an SM as for a compact
- *                    source),
+ *                    of H near the target, else the height that splits H into
+ *                    as many bands as evenly as a fixed height allows; for
+ *                    3-stage plans lowered (down to half) where three CTAs
+ *                    would not fit an SM, then lowered where a band's groups
+ *                    leave the consumer threads' last stride mostly empty;
+ *                    crop sources may lower it so that as many CTAs fit an
+ *                    SM as for a compact source; the odd-row form, where each
+ *                    CTA streams at least five bands, takes two stages and
+ *                    the height that fits the most CTAs, up to four),
  *   stages           shared-memory input stages, 2..8 (default 3 for bands
- *                    above 8 KB of source, else 4),
+ *                    above 8 KB of source, else 4; 2 for the odd-row form's
+ *                    own planning),
  *   max_ctas_per_sm  cap on resident CTAs per SM (default: occupancy limit),
  *   flags            L2 policies (default: source loads and output stores
  *                    both evict-first): bit 0 normal-priority loads, bit 1
@@ -496,6 +503,14 @@ int tr_device_status(int* flags, int clear);
  *                    of a batch waits for 16 bytes that never arrive, its waits
  *                    run out after about a second, the launch returns with bit 0
  *                    of the device status word set and its output incomplete;
+ *                    bit 10 makes the odd-row form write its output tile
+ *                    element by element (default, for NHWC pixels of 2, 4, 6
+ *                    or 12 bytes and NCHW plane runs of 32 bytes or more
+ *                    when the launch gives each CTA at least five bands:
+ *                    each group's output bytes moved to the tile's 16-byte
+ *                    frame in registers and written with 16-byte stores,
+ *                    2/4/8-byte stores only at its ends), bit 17 uses that
+ *                    realignment however few bands a CTA gets;
  *                    crop sources: bit 8 reads 16-byte chunks even where 32-byte
  *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion;
  *                    compact sources: erased source spans are left out of a
@@ -503,7 +518,16 @@ int tr_device_status(int* flags, int clear);
  *                    they save at least 256 bytes a row and not in a CTA's
  *                    first S bands; bit 11 leaves them out of the first S
  *                    bands too, bits 12..15 = v != 0 set the threshold to
- *                    (v - 1) * 128 bytes.
+ *                    (v - 1) * 128 bytes; bit 16 keeps the band height of
+ *                    about 32 KB of output where it leaves fewer than three
+ *                    CTAs on an SM (default, for plans of at most three
+ *                    stages: the largest lower height, down to half, at
+ *                    which three fit), bit 18 keeps that height
+ *                    even where a band's last stride of consumer threads is
+ *                    mostly empty (default: the largest lower height, down to
+ *                    half, at which a band's groups fill at least 84 % of the
+ *                    consumer threads' strides), bit 19 plans the odd-row
+ *                    form like the aligned one.
  * Results do not depend on the geometry.  Errors: TR_ERR_INVALID_ARGUMENT
  * for negative values or stages of 1 or above 8.                            */
 int tr_tune_tiled(int band_bytes, int stages, int max_ctas_per_sm, int flags);

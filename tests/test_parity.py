@@ -18,6 +18,7 @@ F32, F16 = trfn.OUT_F32, trfn.OUT_F16
 NHWC, NCHW, NHWC4 = trfn.LAYOUT_NHWC, trfn.LAYOUT_NCHW, trfn.LAYOUT_NHWC4
 AUTO, TILED, GENERIC = trfn.VARIANT_AUTO, trfn.VARIANT_TILED, trfn.VARIANT_GENERIC
 IMNET = (np.array(synth.IMAGENET_MEAN, np.float32), np.array(synth.IMAGENET_STD, np.float32))
+STREAMS = 1 << 17   # tr_tune_tiled flags: odd-row form, register-realigned output stores at any size
 
 
 def _config_case(k):
@@ -410,10 +411,57 @@ def test_odd_row_tiled_form(shape):
     for dt in (F16, F32):
         for layout in (NHWC, NCHW, NHWC4):
             ref_g, _ = gpu_run(src, mean, std, aug, dt, layout, GENERIC)
-            for w, dst_off in ((None, 0), (ws.data_ptr(), 0), (None, 2 if dt == F16 else 4)):
-                got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED, workspace=w, dst_offset=dst_off)
-                assert np.array_equal(got, ref_g)
+            # default stores (element stores at these sizes), then the
+            # register-realigned stores forced (tr_tune_tiled flags bit 17)
+            for flags in (0, STREAMS):
+                for w, dst_off in ((None, 0), (ws.data_ptr(), 0), (None, 2 if dt == F16 else 4)):
+                    try:
+                        trfn.tr_tune_tiled(0, 0, 0, flags)
+                        got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED, workspace=w,
+                                            dst_offset=dst_off)
+                    finally:
+                        trfn.tr_tune_tiled(0, 0, 0, 0)
+                    assert np.array_equal(got, ref_g)
     assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0
+
+
+@pytest.mark.parametrize("dt,layout", [(F16, NHWC), (F32, NHWC), (F32, NCHW), (F16, NCHW)])
+def test_odd_row_full_size(dt, layout):
+    """256 x 299x299x3 (Inception-sized rows of 897 bytes) through AUTO: the
+    odd-row form with its default stores at a size where each CTA streams
+    many bands (register-realigned stores for binary16/binary32 NHWC and
+    binary32 NCHW), whole output against the oracle, guard bytes intact."""
+    N, H, W, C = 256, 299, 299, 3
+    src = synth.pixels_uniform(299, N, H, W, C)
+    aug, _ = oracle.sample_aug_params(2990, 0, N, H, W)
+    check_case(src, IMNET[0], IMNET[1], aug, dt, layout)
+    assert trfn.tr_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(2, 17, 299, 3), (3, 9, 10, 1), (7, 3, 33, 3), (3, 2, 15, 4), (2, 11, 13, 2)])
+def test_odd_row_output_stores_same_bits(shape):
+    """The odd-row form's two ways of writing its output tile (16-byte
+    stores of register-realigned group outputs, forced by tr_tune_tiled flags
+    bit 17; element stores, bit 10) give the same bits in every layout and
+    type, with the output pointer on and off 16."""
+    N, H, W, C = shape
+    src = synth.coordinate_image(N, H, W, C)
+    mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
+    std = np.array([0.25, 0.5, 0.3, 0.2], np.float32)[:C]
+    aug = synth.random_records(77 + W, N, H, W, allow_outside=True)
+    for dt in (F16, F32):
+        for layout in (NHWC, NCHW, NHWC4):
+            for dst_off in (0, 2 if dt == F16 else 4, 6 if dt == F16 else 12):
+                outs = []
+                for fl in (STREAMS, 1024):
+                    try:
+                        trfn.tr_tune_tiled(0, 0, 0, fl)
+                        got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED, dst_offset=dst_off)
+                    finally:
+                        trfn.tr_tune_tiled(0, 0, 0, 0)
+                    outs.append(got)
+                assert np.array_equal(outs[0], outs[1]), (dt, layout, dst_off)
     assert trfn.tr_device_status() == 0
 
 

@@ -8,7 +8,10 @@ on the host from a seed.  Prints ONE JSON line.
   value      images/s of the CUDA kernel with inputs resident in HBM; the
              timed steps are replays of a CUDA graph of launches that rotate
              over enough distinct (src, dst, records) sets to exceed L2 four
-             times, so no step reads what the previous one left in L2.
+             times, so no step reads what the previous one left in L2.  The
+             batches share no buffer, so each launch overlaps the previous
+             one's drain (TR_LAUNCH_OVERLAP_PREVIOUS); isolated_launches
+             times the same launches each waiting for the one before.
   roofline   algorithmic bytes per launch (N*H*W*C*(1 + out_bytes) minus the
              erased source reads) / average launch time, against the measured
              HBM copy bandwidth (MEASURED_PEAKS.json).
@@ -62,6 +65,10 @@ def parse():
                          "odd-row form of the tiled kernel)")
     ap.add_argument("--variant", type=int, default=0, help="0 auto, 1 tiled, 2 generic")
     ap.add_argument("--static", action="store_true", help="static band schedule (no workspace)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="each launch waits for the previous one to complete before touching memory (no "
+                         "TR_LAUNCH_OVERLAP_PREVIOUS); by default consecutive batches, which share no buffer, "
+                         "overlap one launch's drain with the next one's first copies")
     ap.add_argument("--fused-sampling", action="store_true",
                     help="records drawn inside the fused kernel each step (tr_fused_norm_sampled)")
     ap.add_argument("--device-sampling", action="store_true",
@@ -314,14 +321,25 @@ def run_ours(args, rank, local, world, pg):
     alg_bytes = [algorithmic_bytes(cfg, r) for r in recs_all]
 
     stream = torch.cuda.Stream(device=dev)
-    # one scheduling workspace serves every launch of the stream (they run one
-    # after another); --static measures the workspace-free schedule
-    ws = None if args.static else torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
+    # scheduling workspaces that differ from one launch to the next, so that a
+    # launch may overlap the one before it (TR_LAUNCH_OVERLAP_PREVIOUS: the
+    # batches share no buffer).  Full graphs (even length) alternate 0/1;
+    # shorter runs (eager remainders, the tail graph, any length) alternate
+    # 2/1, so they start on another workspace than a full graph ends on (1)
+    # and end on another than one starts on (0).  --static measures the
+    # workspace-free schedule.
+    wss = [None] * 3 if args.static else [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev)
+                                          for _ in range(3)]
 
     dev_sampling = args.device_sampling and (cfg["flip"] or cfg["erase"])
     fused_sampling = args.fused_sampling and (cfg["flip"] or cfg["erase"]) and not S
+    # crop windows and GPU-sampled records launch without the option (the
+    # kernel reads records the sampler just wrote)
+    overlap_ok = not (S or dev_sampling or fused_sampling)
+    overlap = {"on": overlap_ok and not args.no_overlap}
 
-    def launch(j):
+    def launch(j, k=0, part=False):
+        ws = wss[(2, 1)[k % 2]] if part else wss[k % 2]
         if fused_sampling:
             trfn.tr_fused_norm_sampled(srcs[j], dsts[j], mean, std, 4000 + j, 0, augs[j], flip=cfg["flip"],
                                        erase=cfg["erase"], erase_p=cfg["erase_p"], out_dtype=dt, layout=layout,
@@ -336,26 +354,29 @@ def run_ours(args, rank, local, world, pg):
                                     workspace=ws)
         else:
             trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout, stream=stream,
-                               variant=args.variant, workspace=ws)
+                               variant=args.variant, workspace=ws, overlap_previous=overlap["on"])
 
-    # warm the library's per-kernel caches, then capture graphs of launches
+    # warm the library's per-kernel caches (ending on an odd launch index, so
+    # the next launch takes the other workspace), then capture graphs of
+    # launches; G is even, so workspaces alternate across replays too
     with torch.cuda.stream(stream):
-        for j in range(nsets):
-            launch(j)
+        for k in range(nsets + nsets % 2):
+            launch(k % nsets, k)
     torch.cuda.synchronize()
     G = nsets * max(1, 60 // nsets)
+    G += G % 2
 
-    def capture(count):
+    def capture(count, part=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for k in range(count):
-                launch(k % nsets)
+                launch(k % nsets, k, part)
         return g
 
     launches_before = trfn.tr_launch_count()
     g_full = capture(G)
     K, Wm = args.steps, args.warmup
-    g_tail = capture(K % G) if K % G else None
+    g_tail = capture(K % G, part=True) if K % G else None
     captured = trfn.tr_launch_count() - launches_before
 
     def run_steps(steps, exact_tail=None, marks=None):
@@ -374,7 +395,7 @@ def run_ours(args, rank, local, world, pg):
                 exact_tail.replay()
             elif rem:
                 for k in range(rem):
-                    launch(k % nsets)
+                    launch(k % nsets, k, part=True)
 
     run_steps(Wm)
     torch.cuda.synchronize()
@@ -417,6 +438,30 @@ def run_ours(args, rank, local, world, pg):
     # sampled parity of the last outputs against the oracle (bench's own launch configuration)
     parity = parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets, crops)
 
+    # the same launches, each waiting for the previous one to complete before
+    # it touches memory (no overlap): a graph replayed for about a fifth of the
+    # timed steps, reported beside the main figure
+    isolated = None
+    if overlap["on"]:
+        overlap["on"] = False
+        g_iso = capture(G)
+        reps = max(1, min(K // G, 200) // 5)
+        e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g_iso.replay()
+            e_a.record(stream)
+            for _ in range(reps):
+                g_iso.replay()
+            e_b.record(stream)
+        e_b.synchronize()
+        iso_s = e_a.elapsed_time(e_b) / 1000.0 / (reps * G)
+        iso_gbs = float(np.mean([alg_bytes[k % nsets] for k in range(G)])) / iso_s / 1e9
+        isolated = {"ms_per_step": iso_s * 1000.0, "images_per_s": N / iso_s, "achieved": iso_gbs,
+                    "frac": iso_gbs / peak, "steps": reps * G,
+                    "launch": "each launch waits for the previous one to complete (no TR_LAUNCH_OVERLAP_PREVIOUS)"}
+        overlap["on"] = True
+        del g_iso
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg)
@@ -444,7 +489,11 @@ def run_ours(args, rank, local, world, pg):
             "flip_p": 0.5 if cfg["flip"] else 0.0, "erase_p": cfg["erase_p"],
             "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB >= 4x L2 (%.0f MB)" % (
                 nsets, nsets * set_bytes / 1e6, l2 / 1e6),
-            "launch": "CUDA graph of %d launches replayed; variant %d" % (G, args.variant),
+            "launch": "CUDA graph of %d launches replayed; variant %d; %s" % (
+                G, args.variant,
+                "consecutive launches overlap (tr_fused_norm_ex, TR_LAUNCH_OVERLAP_PREVIOUS: independent batches, "
+                "workspaces differing from one launch to the next)" if overlap["on"]
+                else "each launch waits for the previous one to complete"),
             "schedule": "static (tr_fused_norm)" if args.static else "dynamic bands (tr_fused_norm_ws)",
             "source": ("%dx%d windows of %dx%d images (tr_fused_norm_crop)" % (H, W, S, S)) if S else "compact",
             "records": ("sampled inside the fused kernel every step (tr_fused_norm_sampled)" if fused_sampling
@@ -468,6 +517,8 @@ def run_ours(args, rank, local, world, pg):
         res["clocks"] = clk
     if trials is not None:
         res["trials"] = trials
+    if isolated is not None:
+        res["isolated_launches"] = isolated
     if e2e is not None:
         res["e2e"] = e2e
     if pipeline is not None:

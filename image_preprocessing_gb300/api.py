@@ -14,6 +14,7 @@ from ._native import AugParam, AugSampling, StageBatch, StageSlot, TrError, chec
 OUT_F32, OUT_F16 = 0, 1
 LAYOUT_NHWC, LAYOUT_NCHW, LAYOUT_NHWC4 = 0, 1, 2
 VARIANT_AUTO, VARIANT_TILED, VARIANT_GENERIC = 0, 1, 2
+LAUNCH_OVERLAP_PREVIOUS = 1   # tr_fused_norm_ex flags
 PRESETS = {"NO_NORM": 0, "MNIST": 1, "CIFAR": 2, "IMAGENET": 3, "MLPERF": 4}
 
 _DTYPES = {"f32": OUT_F32, "float32": OUT_F32, "f16": OUT_F16, "float16": OUT_F16}
@@ -65,14 +66,17 @@ def _workspace_ptr(ws, where):
 
 
 def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOUT_NHWC, stream=None,
-                  variant=VARIANT_AUTO, shape=None, workspace=None):
+                  variant=VARIANT_AUTO, shape=None, workspace=None, overlap_previous=False):
     """Enqueue the fused step: src uint8 (N,H,W,C) CUDA tensor -> dst.
 
     dst: CUDA tensor of float32/float16 with out_shape(N,H,W,C,layout)
     elements; aug: CUDA int32 tensor (N,5) of {flip,y0,x0,h,w} or None;
     raw device addresses (ints) are accepted with shape=(N,H,W,C).
     workspace: zeroed CUDA buffer of tr_workspace_bytes() bytes for the
-    dynamic band schedule (tr_fused_norm_ws), or None."""
+    dynamic band schedule (tr_fused_norm_ws), or None.
+    overlap_previous: the caller's promise that this launch shares no buffer
+    (workspace included) with the kernel before it in the stream
+    (tr_fused_norm_ex with TR_LAUNCH_OVERLAP_PREVIOUS)."""
     dt = _code(out_dtype, _DTYPES)
     lay = _code(layout, _LAYOUTS)
     if shape is not None:
@@ -88,9 +92,10 @@ def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOU
         if aug is not None and (aug.dtype != torch.int32 or aug.numel() != 5 * N):
             raise TrError(1, "tr_fused_norm", "aug must be int32 with N*5 elements")
     m, s = float_array(mean), float_array(std)
-    rc = lib().tr_fused_norm_ws(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
+    rc = lib().tr_fused_norm_ex(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
                                 _dev_ptr(aug, "aug"), dt, lay, _stream_handle(stream), int(variant),
-                                _workspace_ptr(workspace, "tr_fused_norm"))
+                                _workspace_ptr(workspace, "tr_fused_norm"),
+                                LAUNCH_OVERLAP_PREVIOUS if overlap_previous else 0)
     check(rc, "tr_fused_norm")
 
 

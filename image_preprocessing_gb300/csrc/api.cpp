@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -65,10 +66,33 @@ struct Sampling {
     tr_aug_param* out = nullptr;   // device, N records
 };
 
+// The workspace of the last launch this library made on each stream (a small
+// table, oldest entry replaced): a launch asking to overlap the kernel before
+// it must not share that kernel's workspace, whose ticket counters are still
+// in use and are zeroed by its last CTA.
+bool note_stream_workspace(void* stream, void* workspace) {
+    struct Entry { void* stream; void* ws; bool used; };
+    static std::mutex mu;
+    static Entry table[64];
+    static int next = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (Entry& e : table) {
+        if (e.used && e.stream == stream) {
+            const bool same = (workspace != nullptr && e.ws == workspace);
+            e.ws = workspace;
+            return same;
+        }
+    }
+    table[next] = Entry{stream, workspace, true};
+    next = (next + 1) % 64;
+    return false;
+}
+
 int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,
                     const float* stdv, const tr_aug_param* aug, int out_dtype, int out_layout,
                     void* stream, int variant, void* workspace, const CropSource& cs = CropSource(),
-                    const Sampling& smp = Sampling()) {
+                    const Sampling& smp = Sampling(), unsigned flags = 0) {
+    if ((flags & ~(unsigned)TR_LAUNCH_OVERLAP_PREVIOUS) != 0) return TR_ERR_INVALID_ARGUMENT;
     int rc = check_shape(N, H, W, C, out_dtype, out_layout);
     if (rc != TR_OK) return rc;
     if (variant != TR_VARIANT_AUTO && variant != TR_VARIANT_TILED && variant != TR_VARIANT_GENERIC)
@@ -139,6 +163,10 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     a.src_W = cs.src_W;
     a.src_row_stride = cs.row_stride;
     a.src_image_stride = cs.image_stride;
+    // overlap only what the caller declared independent, never a kernel that
+    // used the same workspace, and never the records' own sampler
+    const bool same_ws = note_stream_workspace(stream, workspace);
+    a.overlap_prev = (flags & TR_LAUNCH_OVERLAP_PREVIOUS) != 0 && !same_ws && !smp.on;
     if (smp.on) {
         // the records first, into smp.out, then the kernel reads them in
         // stream order (its prologue overlaps the sampler)
@@ -181,6 +209,13 @@ int tr_fused_norm_ws(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
                      void* stream, int variant, void* workspace) {
     return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
                            stream, variant, workspace);
+}
+
+int tr_fused_norm_ex(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,
+                     const float* std, const tr_aug_param* aug_params, int out_dtype, int out_layout,
+                     void* stream, int variant, void* workspace, unsigned flags) {
+    return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
+                           stream, variant, workspace, CropSource(), Sampling(), flags);
 }
 
 size_t tr_workspace_bytes(void) { return kWorkspaceBytes; }

@@ -929,8 +929,12 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
     }
     __syncthreads();
     // everything above overlaps the previous grid in the stream; global
-    // memory is touched only below
-    grid_dependency_wait();
+    // memory is touched only below, after that grid has completed, unless
+    // the caller has promised that this launch shares no buffer with it
+    // (hints bit 8): then the copies start at once and each CTA's storer
+    // waits for the previous grid before it exits, so this grid still
+    // completes after it and later work in the stream sees both
+    if (!(p.hints & 256)) grid_dependency_wait();
     if ((p.hints & 8) && threadIdx.x == 0) grid_launch_dependents();
 
     if (threadIdx.x < 32) {
@@ -1046,6 +1050,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         if (aborted) atomicOr(&g_device_status, kStatusTimeout);
         if (p.hints & 16) bulk_wait_read<0>();
         else bulk_wait_all<0>();
+        if (p.hints & 256) grid_dependency_wait();
     }
 }
 
@@ -1649,6 +1654,7 @@ int launch_tiled(const LaunchArgs& a) {
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
     p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000);
+    if (a.overlap_prev) p.hints |= 256;   // copies may start before the previous grid completes
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 

@@ -31,6 +31,9 @@ struct LaunchArgs {
     int out_layout;
     void* stream;
     void* workspace;  // scheduling workspace (tr_workspace_bytes(), zeroed), or null
+    // the launch shares no buffer with the kernel before it in the stream:
+    // the tiled kernel may start its copies while that kernel drains
+    bool overlap_prev = false;
     // windows of a strided source (tr_fused_norm_crop); otherwise a compact
     // NHWC source of H x W images
     bool crop_src = false;

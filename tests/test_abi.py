@@ -78,6 +78,10 @@ def test_null_and_bad_constants_rejected():
     # a workspace off a 16-byte boundary
     assert L.tr_fused_norm_ws(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0, 0x3004) == INVALID
     assert L.tr_workspace_bytes() == 2048
+    # launch options: unknown bits, and the flag on otherwise bad arguments
+    assert L.tr_fused_norm_ex(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0, None, 2) == INVALID
+    assert L.tr_fused_norm_ex(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0, 0x3004, 1) == INVALID
+    assert L.tr_fused_norm_ex(0x1000, 0x100000, 0, 2, 2, 3, M3, S3, None, 0, 0, None, 0, None, 1) == 0
     # overlapping src and dst
     assert L.tr_fused_norm(0x1000, 0x1004, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
     # a bad kernel choice

@@ -1,0 +1,142 @@
+"""Launches that overlap the kernel before them (tr_fused_norm_ex with
+TR_LAUNCH_OVERLAP_PREVIOUS): consecutive batches with their own buffers and
+workspaces alternating between two, eagerly and inside a CUDA graph, aligned
+and odd-row forms, against the oracle; stream order for later work; the flag
+dropped when a launch reuses the previous launch's workspace."""
+import numpy as np
+import pytest
+
+import oracle
+import image_preprocessing_gb300 as trfn
+from image_preprocessing_gb300 import synth
+from parity_util import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+F16, F32 = trfn.OUT_F16, trfn.OUT_F32
+NHWC, NCHW = trfn.LAYOUT_NHWC, trfn.LAYOUT_NCHW
+MEAN = np.array(synth.IMAGENET_MEAN, np.float32)
+STD = np.array(synth.IMAGENET_STD, np.float32)
+
+
+def _bits(t, dt):
+    import torch
+    t = t.cpu()
+    return t.view(torch.int16).numpy().view(np.uint16) if dt == F16 else t.numpy()
+
+
+def _batches(K, N, H, W, C, dt, layout, seed):
+    import torch
+    tdt = torch.float16 if dt == F16 else torch.float32
+    srcs, recs, d_src, d_rec, dsts = [], [], [], [], []
+    for k in range(K):
+        src = synth.pixels_uniform(seed + k, N, H, W, C)
+        rec, _ = oracle.sample_aug_params(seed + 100 + k, 0, N, H, W)
+        srcs.append(src)
+        recs.append(rec)
+        d_src.append(torch.from_numpy(src).cuda())
+        d_rec.append(torch.from_numpy(rec).cuda())
+        dsts.append(torch.full(trfn.out_shape(N, H, W, C, layout), 7.0, dtype=tdt, device="cuda"))
+    return srcs, recs, d_src, d_rec, dsts
+
+
+def _check(srcs, recs, dsts, dt, layout):
+    for k, (src, rec, dst) in enumerate(zip(srcs, recs, dsts)):
+        ref = oracle.fused_norm(src, MEAN, STD, rec, out_dtype=dt, layout=layout)
+        assert_parity(_bits(dst, dt), ref, dt, "overlapped batch %d" % k)
+
+
+@pytest.mark.parametrize("shape,dt,layout,schedule", [
+    ((64, 224, 224, 3), F16, NHWC, "dynamic"),
+    ((64, 224, 224, 3), F32, NCHW, "static"),
+    ((48, 299, 299, 3), F16, NHWC, "dynamic"),       # odd-row form
+    ((256, 28, 28, 1), F32, NHWC, "dynamic"),        # odd-row form, small images
+])
+def test_consecutive_overlapped_launches(shape, dt, layout, schedule):
+    import torch
+    N, H, W, C = shape
+    K = 6
+    srcs, recs, d_src, d_rec, dsts = _batches(K, N, H, W, C, dt, layout, 4000 + W)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        for k in range(K):
+            ws = wss[k % 2] if schedule == "dynamic" else None
+            trfn.tr_fused_norm(d_src[k], dsts[k], MEAN, STD, d_rec[k], out_dtype=dt, layout=layout, stream=st,
+                               workspace=ws, overlap_previous=True)
+    torch.cuda.synchronize()
+    _check(srcs, recs, dsts, dt, layout)
+    for ws in wss:
+        assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0
+
+
+def test_overlapped_launches_in_a_graph():
+    import torch
+    N, H, W, C = 64, 224, 224, 3
+    K = 4
+    srcs, recs, d_src, d_rec, dsts = _batches(K, N, H, W, C, F16, NHWC, 4500)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for k in range(K):
+            trfn.tr_fused_norm(d_src[k], dsts[k], MEAN, STD, d_rec[k], out_dtype=F16, stream=st,
+                               workspace=wss[k % 2], overlap_previous=True)
+    for rep in range(3):
+        for d in dsts:
+            d.fill_(5.0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            g.replay()
+        torch.cuda.synchronize()
+        _check(srcs, recs, dsts, F16, NHWC)
+    for ws in wss:
+        assert int(ws.count_nonzero()) == 0
+
+
+def test_later_work_sees_both_launches():
+    """A large launch, then a small overlapped one, then a torch copy of the
+    large launch's output on the same stream: the copy sees it complete
+    (the overlapped launch completes only after the one before it)."""
+    import torch
+    (src_a,), (rec_a,), (d_src_a,), (d_rec_a,), (dst_a,) = _batches(1, 256, 224, 224, 3, F16, NHWC, 4700)
+    srcs_b, recs_b, d_src_b, d_rec_b, dsts_b = _batches(1, 8, 224, 224, 3, F16, NHWC, 4800)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for rep in range(3):
+        dst_a.fill_(3.0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            trfn.tr_fused_norm(d_src_a, dst_a, MEAN, STD, d_rec_a, out_dtype=F16, stream=st, workspace=wss[0])
+            trfn.tr_fused_norm(d_src_b[0], dsts_b[0], MEAN, STD, d_rec_b[0], out_dtype=F16, stream=st,
+                               workspace=wss[1], overlap_previous=True, variant=trfn.VARIANT_TILED)
+            copy = dst_a.clone()
+        torch.cuda.synchronize()
+        ref = oracle.fused_norm(src_a, MEAN, STD, rec_a, out_dtype=F16)
+        assert_parity(_bits(copy, F16), ref, F16, "copy after the overlapped launch")
+    _check(srcs_b, recs_b, dsts_b, F16, NHWC)
+
+
+def test_shared_workspace_drops_the_overlap():
+    """The flag on launches that share one workspace: the library does not
+    overlap them (their ticket counters would collide); results exact and the
+    workspace zero again."""
+    import torch
+    N, H, W, C = 64, 224, 224, 3
+    K = 5
+    srcs, recs, d_src, d_rec, dsts = _batches(K, N, H, W, C, F16, NHWC, 4900)
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        for k in range(K):
+            trfn.tr_fused_norm(d_src[k], dsts[k], MEAN, STD, d_rec[k], out_dtype=F16, stream=st, workspace=ws,
+                               overlap_previous=True)
+    torch.cuda.synchronize()
+    _check(srcs, recs, dsts, F16, NHWC)
+    assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0

@@ -333,9 +333,9 @@ def run_ours(args, rank, local, world, pg):
 
     dev_sampling = args.device_sampling and (cfg["flip"] or cfg["erase"])
     fused_sampling = args.fused_sampling and (cfg["flip"] or cfg["erase"]) and not S
-    # crop windows and GPU-sampled records launch without the option (the
-    # kernel reads records the sampler just wrote)
-    overlap_ok = not (S or dev_sampling or fused_sampling)
+    # GPU-sampled records launch without the option (the kernel reads records
+    # the sampler just wrote)
+    overlap_ok = not (dev_sampling or fused_sampling)
     overlap = {"on": overlap_ok and not args.no_overlap}
 
     def launch(j, k=0, part=False):
@@ -351,7 +351,7 @@ def run_ours(args, rank, local, world, pg):
         if S:
             trfn.tr_fused_norm_crop(srcs[j], S, S, S * C, S * S * C, dsts[j], N, H, W, C, mean, std, crop=crops[j],
                                     aug=augs[j], out_dtype=dt, layout=layout, stream=stream, variant=args.variant,
-                                    workspace=ws)
+                                    workspace=ws, overlap_previous=overlap["on"])
         else:
             trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout, stream=stream,
                                variant=args.variant, workspace=ws, overlap_previous=overlap["on"])

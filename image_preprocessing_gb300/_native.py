@@ -67,6 +67,8 @@ _SIGNATURES = {
                                    ctypes.POINTER(_u64), _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_crop": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
                                 _vp, _i, _i, _vp, _i, _vp]),
+    "tr_fused_norm_crop_ex": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
+                                   _vp, _i, _i, _vp, _i, _vp, ctypes.c_uint]),
     "tr_fused_norm_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp]),
     "tr_fused_norm_plan": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]),
     "tr_norm_preset": (_i, [_i, _fp, _fp, ctypes.POINTER(_i)]),

@@ -130,17 +130,20 @@ def tr_fused_norm_sampled(src, dst, mean, std, seed, offset, records, flip=True,
 
 def tr_fused_norm_crop(src, src_H, src_W, row_stride, image_stride, dst, N, H, W, C, mean, std, crop=None,
                        aug=None, out_dtype=OUT_F16, layout=LAYOUT_NHWC, stream=None, variant=VARIANT_AUTO,
-                       workspace=None):
+                       workspace=None, overlap_previous=False):
     """Enqueue the fused step on H x W windows of a strided source.
 
     src: CUDA uint8 tensor (or device address) holding N images with the given
     row and image strides in bytes; crop: CUDA int32 (N, 2) {top, left} or
-    None; dst: CUDA output with out_shape(N, H, W, C, layout) elements."""
+    None; dst: CUDA output with out_shape(N, H, W, C, layout) elements;
+    overlap_previous as tr_fused_norm (tr_fused_norm_crop_ex)."""
     m, s = float_array(mean), float_array(std)
-    rc = lib().tr_fused_norm_crop(_dev_ptr(src, "src"), src_H, src_W, row_stride, image_stride,
-                                  _dev_ptr(crop, "crop"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
-                                  _dev_ptr(aug, "aug"), _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS),
-                                  _stream_handle(stream), int(variant), _workspace_ptr(workspace, "tr_fused_norm_crop"))
+    rc = lib().tr_fused_norm_crop_ex(_dev_ptr(src, "src"), src_H, src_W, row_stride, image_stride,
+                                     _dev_ptr(crop, "crop"), _dev_ptr(dst, "dst"), N, H, W, C, m, s,
+                                     _dev_ptr(aug, "aug"), _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS),
+                                     _stream_handle(stream), int(variant),
+                                     _workspace_ptr(workspace, "tr_fused_norm_crop"),
+                                     LAUNCH_OVERLAP_PREVIOUS if overlap_previous else 0)
     check(rc, "tr_fused_norm_crop")
 
 

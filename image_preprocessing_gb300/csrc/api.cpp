@@ -255,6 +255,22 @@ int tr_fused_norm_crop(const uint8_t* src_u8, int src_H, int src_W, size_t src_r
                            variant, workspace, cs);
 }
 
+int tr_fused_norm_crop_ex(const uint8_t* src_u8, int src_H, int src_W, size_t src_row_stride,
+                          size_t src_image_stride, const int32_t* crop_yx, void* dst, int N, int H, int W, int C,
+                          const float* mean, const float* std, const tr_aug_param* aug_params, int out_dtype,
+                          int out_layout, void* stream, int variant, void* workspace, unsigned flags) {
+    if (src_H < 1 || src_W < 1) return TR_ERR_INVALID_ARGUMENT;
+    CropSource cs;
+    cs.on = true;
+    cs.crop = crop_yx;
+    cs.src_H = src_H;
+    cs.src_W = src_W;
+    cs.row_stride = src_row_stride;
+    cs.image_stride = src_image_stride;
+    return fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout, stream,
+                           variant, workspace, cs, Sampling(), flags);
+}
+
 int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,
                        int out_dtype, int out_layout, int* variant) {
     const int rc = check_shape(N, H, W, C, out_dtype, out_layout);

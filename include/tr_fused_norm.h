@@ -203,6 +203,15 @@ int tr_fused_norm_crop(const uint8_t* src_u8, int src_H, int src_W, size_t src_r
                        const float* mean, const float* std, const tr_aug_param* aug_params, int out_dtype,
                        int out_layout, void* stream, int variant, void* workspace);
 
+/* tr_fused_norm_crop with launch options (flags as tr_fused_norm_ex; the
+ * crop origins are read like the other inputs, so they too must not be
+ * written by the kernel before the launch when TR_LAUNCH_OVERLAP_PREVIOUS is
+ * given).  Other arguments, results and errors as tr_fused_norm_crop.       */
+int tr_fused_norm_crop_ex(const uint8_t* src_u8, int src_H, int src_W, size_t src_row_stride,
+                          size_t src_image_stride, const int32_t* crop_yx, void* dst, int N, int H, int W, int C,
+                          const float* mean, const float* std, const tr_aug_param* aug_params, int out_dtype,
+                          int out_layout, void* stream, int variant, void* workspace, unsigned flags);
+
 /* Bytes of the scheduling workspace (2048). */
 size_t tr_workspace_bytes(void);
 

@@ -140,3 +140,37 @@ def test_shared_workspace_drops_the_overlap():
     _check(srcs, recs, dsts, F16, NHWC)
     assert int(ws.count_nonzero()) == 0
     assert trfn.tr_device_status() == 0
+
+
+def test_overlapped_crop_windows():
+    """tr_fused_norm_crop_ex: consecutive crop launches overlapping, each with
+    its own source, windows, records and output, workspaces alternating."""
+    import torch
+    N, H, W, C, S = 48, 224, 224, 3, 256
+    K = 4
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    srcs, recs, crops, outs, d = [], [], [], [], []
+    for k in range(K):
+        src = synth.pixels_uniform(5100 + k, N, S, S, C)
+        g = np.random.default_rng(5200 + k)
+        crop = np.stack([g.integers(0, S - H + 1, N), g.integers(0, S - W + 1, N)], 1).astype(np.int32)
+        rec, _ = oracle.sample_aug_params(5300 + k, 0, N, H, W)
+        srcs.append(src); recs.append(rec); crops.append(crop)
+        d.append((torch.from_numpy(src).cuda(), torch.from_numpy(crop).cuda(), torch.from_numpy(rec).cuda()))
+        outs.append(torch.full((N, H, W, C), 7.0, dtype=torch.float16, device="cuda"))
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        for k in range(K):
+            d_src, d_crop, d_rec = d[k]
+            trfn.tr_fused_norm_crop(d_src, S, S, S * C, S * S * C, outs[k], N, H, W, C, MEAN, STD, crop=d_crop,
+                                    aug=d_rec, out_dtype=F16, stream=st, workspace=wss[k % 2],
+                                    overlap_previous=True)
+    torch.cuda.synchronize()
+    for k in range(K):
+        win = np.stack([srcs[k][n, crops[k][n, 0]:crops[k][n, 0] + H, crops[k][n, 1]:crops[k][n, 1] + W]
+                        for n in range(N)])
+        ref = oracle.fused_norm(win, MEAN, STD, recs[k], out_dtype=F16)
+        assert_parity(_bits(outs[k], F16), ref, F16, "overlapped crop batch %d" % k)
+    for ws in wss:
+        assert int(ws.count_nonzero()) == 0

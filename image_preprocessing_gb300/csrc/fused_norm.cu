@@ -931,11 +931,19 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
     // everything above overlaps the previous grid in the stream; global
     // memory is touched only below, after that grid has completed, unless
     // the caller has promised that this launch shares no buffer with it
-    // (hints bit 8): then the copies start at once and each CTA's storer
-    // waits for the previous grid before it exits, so this grid still
-    // completes after it and later work in the stream sees both
-    if (!(p.hints & 256)) grid_dependency_wait();
-    if ((p.hints & 8) && threadIdx.x == 0) grid_launch_dependents();
+    // (hints bit 8): then the copies start at once, the producer waits for
+    // the previous grid once it has issued its first S bands, and each
+    // CTA's storer waits for it again before it exits, so this grid still
+    // completes after it and later work in the stream sees both.
+    // A CTA releases the next grid in the stream only after the previous one
+    // has completed, so that no more than two grids of the stream (this one
+    // and the next, which its caller declared independent of this one) are
+    // ever in flight: here when this launch waited above, else after the
+    // producer's wait.  (hints bit 3 delays the release until the CTA's
+    // copies are all issued.)
+    const bool overlapped = (p.hints & 256) != 0;
+    if (!overlapped) grid_dependency_wait();
+    if (!overlapped && !(p.hints & 8) && threadIdx.x == 0) grid_launch_dependents();
 
     if (threadIdx.x < 32) {
         // The producer: lane 0 waits on barriers, issues copies, takes
@@ -973,6 +981,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         if (!early0 && u < p.num_units) a = unit_record(u);
         int j = 0;
         bool ok = true;
+        bool waited = !overlapped;   // the previous grid has completed
         for (;; ++j) {
             const int s = j % S;
             if (j >= S && !mbar_wait_bounded(empty0 + 8u * s, (uint32_t)(j / S - 1) & 1u)) {
@@ -998,8 +1007,15 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
             // next empty wait
             u = next_unit(j + 1);
             if (u < p.num_units) a = unit_record(u);
+            if (!waited && j + 1 >= S) {
+                // overlapped launch: its first S bands are in flight
+                grid_dependency_wait();
+                waited = true;
+                if (!(p.hints & 8)) grid_launch_dependents();
+            }
         }
         {
+            if (!waited) grid_dependency_wait();
             grid_launch_dependents();
             if (!ok) {
                 atomicOr(&g_device_status, kStatusTimeout);

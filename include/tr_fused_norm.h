@@ -161,7 +161,10 @@ enum {
      * can be overlapped; after a copy, a memset or another library's kernel
      * stream order is unchanged.  A launch whose workspace equals the one of
      * this library's previous launch on the same stream is not overlapped (the
-     * flag is dropped).  The GENERIC kernel ignores the flag.               */
+     * flag is dropped).  A launch releases the next kernel in the stream only
+     * once the kernel before it has completed, so no launch ever overlaps
+     * more than the one kernel before it.  The GENERIC kernel ignores the
+     * flag.                                                                 */
     TR_LAUNCH_OVERLAP_PREVIOUS = 1
 };
 
@@ -525,9 +528,10 @@ int tr_device_status(int* flags, int clear);
  *   flags            L2 policies (default: source loads and output stores
  *                    both evict-first): bit 0 normal-priority loads, bit 1
  *                    normal-priority stores, bit 2 evict-last stores (for a
- *                    consumer that reads the output from L2); bit 3 lets the
- *                    next kernel in the stream launch as soon as this one has
- *                    started (default: once its loads are issued); bit 4
+ *                    consumer that reads the output from L2); bit 3 makes a
+ *                    CTA release the next kernel in the stream only once its
+ *                    copies are all issued (default: as soon as the previous
+ *                    kernel has completed); bit 4
  *                    lets a CTA exit once its last store has read shared
  *                    memory instead of once the store has completed (the
  *                    grid's completion still covers the writes); bit 5 makes

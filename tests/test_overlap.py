@@ -174,3 +174,36 @@ def test_overlapped_crop_windows():
         assert_parity(_bits(outs[k], F16), ref, F16, "overlapped crop batch %d" % k)
     for ws in wss:
         assert int(ws.count_nonzero()) == 0
+
+
+def test_small_launches_never_run_ahead_of_a_large_one():
+    """A large launch, then a chain of small overlapped launches alternating
+    two workspaces, so launch k + 2 reuses launch k's workspace.  Small
+    launches issue all their bands at once; were a launch to release its
+    successor before its own predecessor completed, launch 2 could start
+    while the large launch still holds the shared workspace's counters.  All
+    outputs exact, workspaces zero, every time."""
+    import torch
+    (src_a,), (rec_a,), (d_src_a,), (d_rec_a,), (dst_a,) = _batches(1, 512, 224, 224, 3, F16, NHWC, 5500)
+    K = 12
+    srcs, recs, d_src, d_rec, dsts = _batches(K, 8, 224, 224, 3, F16, NHWC, 5600)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    st = torch.cuda.Stream()
+    ref_a = oracle.fused_norm(src_a, MEAN, STD, rec_a, out_dtype=F16)
+    for rep in range(4):
+        dst_a.fill_(3.0)
+        for d in dsts:
+            d.fill_(3.0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            trfn.tr_fused_norm(d_src_a, dst_a, MEAN, STD, d_rec_a, out_dtype=F16, stream=st, workspace=wss[0],
+                               overlap_previous=True)
+            for k in range(K):
+                trfn.tr_fused_norm(d_src[k], dsts[k], MEAN, STD, d_rec[k], out_dtype=F16, stream=st,
+                                   workspace=wss[(k + 1) % 2], overlap_previous=True, variant=trfn.VARIANT_TILED)
+        torch.cuda.synchronize()
+        assert_parity(_bits(dst_a, F16), ref_a, F16, "large launch, repetition %d" % rep)
+        _check(srcs, recs, dsts, F16, NHWC)
+        for ws in wss:
+            assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0

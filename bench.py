@@ -333,9 +333,10 @@ def run_ours(args, rank, local, world, pg):
 
     dev_sampling = args.device_sampling and (cfg["flip"] or cfg["erase"])
     fused_sampling = args.fused_sampling and (cfg["flip"] or cfg["erase"]) and not S
-    # GPU-sampled records launch without the option (the kernel reads records
-    # the sampler just wrote)
-    overlap_ok = not (dev_sampling or fused_sampling)
+    # records sampled by a separate call launch without the option (the
+    # kernel reads records the call before it wrote); the one-call form
+    # (tr_fused_norm_sampled) overlaps its sampler with the previous launch
+    overlap_ok = not dev_sampling
     overlap = {"on": overlap_ok and not args.no_overlap}
 
     def launch(j, k=0, part=False):
@@ -343,7 +344,8 @@ def run_ours(args, rank, local, world, pg):
         if fused_sampling:
             trfn.tr_fused_norm_sampled(srcs[j], dsts[j], mean, std, 4000 + j, 0, augs[j], flip=cfg["flip"],
                                        erase=cfg["erase"], erase_p=cfg["erase_p"], out_dtype=dt, layout=layout,
-                                       stream=stream, variant=args.variant, workspace=ws)
+                                       stream=stream, variant=args.variant, workspace=ws,
+                                       overlap_previous=overlap["on"])
             return
         if dev_sampling:
             trfn.tr_sample_aug_params_device(4000 + j, 0, N, H, W, augs[j], flip=cfg["flip"], erase=cfg["erase"],
@@ -509,7 +511,7 @@ def run_ours(args, rank, local, world, pg):
             "algorithmic_bytes_per_launch": avg_bytes,
             "traffic": profiled_traffic(cfg["workload"]),
         },
-        "gpu_launches": K * (2 if dev_sampling else 1),
+        "gpu_launches": K * (2 if (dev_sampling or fused_sampling) else 1),   # sampler + fused kernel
         "captured_launches": int(captured),
         "parity_sample": parity,
     }

@@ -65,6 +65,8 @@ _SIGNATURES = {
     "tr_workspace_bytes": (ctypes.c_size_t, []),
     "tr_fused_norm_sampled": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _u64, _u64, ctypes.POINTER(AugSampling), _vp,
                                    ctypes.POINTER(_u64), _i, _i, _vp, _i, _vp]),
+    "tr_fused_norm_sampled_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _u64, _u64, ctypes.POINTER(AugSampling), _vp,
+                                      ctypes.POINTER(_u64), _i, _i, _vp, _i, _vp, ctypes.c_uint]),
     "tr_fused_norm_crop": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
                                 _vp, _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_crop_ex": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,

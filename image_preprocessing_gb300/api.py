@@ -101,10 +101,11 @@ def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOU
 
 def tr_fused_norm_sampled(src, dst, mean, std, seed, offset, records, flip=True, flip_p=0.5, erase=True,
                           erase_p=0.5, scale=(0.02, 0.33), ratio=(0.3, 3.3), out_dtype=OUT_F16, layout=LAYOUT_NHWC,
-                          stream=None, variant=VARIANT_AUTO, workspace=None):
+                          stream=None, variant=VARIANT_AUTO, workspace=None, overlap_previous=False):
     """tr_fused_norm with the records drawn on the GPU in the same launch
     (image n's record = tr_sample_aug_params_device's, counter block
-    offset + 24n); records: CUDA int32 (N, 5) tensor receiving them.
+    offset + 24n); records: CUDA int32 (N, 5) tensor receiving them;
+    overlap_previous as tr_fused_norm (tr_fused_norm_sampled_ex).
     Returns the next free offset."""
     import torch
     if src.dtype != torch.uint8 or src.dim() != 4:
@@ -119,11 +120,12 @@ def tr_fused_norm_sampled(src, dst, mean, std, seed, offset, records, flip=True,
     sp = AugSampling(int(bool(flip)), float(flip_p), int(bool(erase)), float(erase_p), float(scale[0]),
                      float(scale[1]), float(ratio[0]), float(ratio[1]))
     nxt = ctypes.c_uint64(0)
-    check(lib().tr_fused_norm_sampled(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C, float_array(mean),
-                                      float_array(std), int(seed), int(offset), ctypes.byref(sp),
-                                      _dev_ptr(records, "records"), ctypes.byref(nxt), dt, lay,
-                                      _stream_handle(stream), int(variant),
-                                      _workspace_ptr(workspace, "tr_fused_norm_sampled")),
+    check(lib().tr_fused_norm_sampled_ex(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), N, H, W, C,
+                                         float_array(mean), float_array(std), int(seed), int(offset),
+                                         ctypes.byref(sp), _dev_ptr(records, "records"), ctypes.byref(nxt), dt, lay,
+                                         _stream_handle(stream), int(variant),
+                                         _workspace_ptr(workspace, "tr_fused_norm_sampled"),
+                                         LAUNCH_OVERLAP_PREVIOUS if overlap_previous else 0),
           "tr_fused_norm_sampled")
     return nxt.value
 

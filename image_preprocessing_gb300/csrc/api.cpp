@@ -164,15 +164,18 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     a.src_row_stride = cs.row_stride;
     a.src_image_stride = cs.image_stride;
     // overlap only what the caller declared independent, never a kernel that
-    // used the same workspace, and never the records' own sampler
+    // used the same workspace; with GPU-made records the sampler overlaps the
+    // previous kernel and the fused kernel reads the records once the sampler
+    // (hence that kernel too) has completed
     const bool same_ws = note_stream_workspace(stream, workspace);
-    a.overlap_prev = (flags & TR_LAUNCH_OVERLAP_PREVIOUS) != 0 && !same_ws && !smp.on;
+    a.overlap_prev = (flags & TR_LAUNCH_OVERLAP_PREVIOUS) != 0 && !same_ws;
     if (smp.on) {
         // the records first, into smp.out, then the kernel reads them in
         // stream order (its prologue overlaps the sampler)
-        rc = launch_sampler(smp.spec, N, smp.out, stream);
+        rc = launch_sampler(smp.spec, N, smp.out, stream, a.overlap_prev);
         if (rc != TR_OK) return rc;
         a.aug = smp.out;
+        a.records_from_prev = true;
     }
     rc = launch(a, variant);
     if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {
@@ -224,6 +227,14 @@ int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W,
                           const float* std, uint64_t seed, uint64_t offset, const tr_aug_sampling* sampling,
                           tr_aug_param* d_records, uint64_t* next_offset, int out_dtype, int out_layout,
                           void* stream, int variant, void* workspace) {
+    return tr_fused_norm_sampled_ex(src_u8, dst, N, H, W, C, mean, std, seed, offset, sampling, d_records,
+                                    next_offset, out_dtype, out_layout, stream, variant, workspace, 0u);
+}
+
+int tr_fused_norm_sampled_ex(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,
+                             const float* std, uint64_t seed, uint64_t offset, const tr_aug_sampling* sampling,
+                             tr_aug_param* d_records, uint64_t* next_offset, int out_dtype, int out_layout,
+                             void* stream, int variant, void* workspace, unsigned flags) {
     if (sampling == nullptr || H < 1 || W < 1) return TR_ERR_INVALID_ARGUMENT;
     Sampling smp;
     smp.on = true;
@@ -234,7 +245,7 @@ int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W,
     if (rc != TR_OK) return rc;
     if (N > 0 && d_records == nullptr) return TR_ERR_INVALID_ARGUMENT;
     rc = fused_norm_impl(src_u8, dst, N, H, W, C, mean, std, nullptr, out_dtype, out_layout, stream, variant,
-                         workspace, CropSource(), smp);
+                         workspace, CropSource(), smp, flags);
     if (rc == TR_OK && next_offset != nullptr) *next_offset = offset + (uint64_t)N * 24u;
     return rc;
 }

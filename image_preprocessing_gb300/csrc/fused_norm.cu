@@ -974,14 +974,34 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         };
         int u = blockIdx.x;
         tr_aug_param a = {0, 0, 0, 0, 0};
+        // records written by the previous grid (the device sampler) while
+        // this launch overlaps it (hints bit 9, compact aligned sources): the
+        // first S bands are requested whole before that grid has completed,
+        // and their records are read and published after the wait
+        const bool recdep = !CROP && !ODD && overlapped && (p.hints & 512);
         // the first unit's band is requested before its record has arrived
         // (its erased span is then read too); measured 0.9 % faster at
         // 256x224x224x3 than waiting for the record
-        const bool early0 = !CROP && !ODD && !(p.hints & 32) && u < p.num_units;
-        if (!early0 && u < p.num_units) a = unit_record(u);
+        const bool early0 = !CROP && !ODD && !recdep && !(p.hints & 32) && u < p.num_units;
+        if (!early0 && !recdep && u < p.num_units) a = unit_record(u);
         int j = 0;
         bool ok = true;
         bool waited = !overlapped;   // the previous grid has completed
+        if (recdep) {
+            int first[kMaxStages];
+            for (; j < S; ++j) {
+                const int uu = (int)blockIdx.x + j * G;
+                if (uu >= p.num_units) break;
+                first[j] = uu;
+                issue_unit_uncut<C>(p, uu, j, smem);
+            }
+            grid_dependency_wait();
+            waited = true;
+            if (!(p.hints & 8)) grid_launch_dependents();
+            for (int t = 0; t < j; ++t) publish_unit(p, first[t], t, smem, unit_record(first[t]));
+            u = next_unit(j);
+            if (u < p.num_units) a = unit_record(u);
+        }
         for (;; ++j) {
             const int s = j % S;
             if (j >= S && !mbar_wait_bounded(empty0 + 8u * s, (uint32_t)(j / S - 1) & 1u)) {
@@ -1670,7 +1690,11 @@ int launch_tiled(const LaunchArgs& a) {
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
     p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000);
-    if (a.overlap_prev) p.hints |= 256;   // copies may start before the previous grid completes
+    // copies may start before the previous grid completes; records that grid
+    // wrote are read after it (compact aligned sources; the crop and
+    // odd-row forms then wait for it before they touch memory)
+    if (a.overlap_prev && !(a.records_from_prev && (crop || odd))) p.hints |= 256;
+    if (a.overlap_prev && a.records_from_prev && !crop && !odd) p.hints |= 512;
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 

@@ -34,6 +34,10 @@ struct LaunchArgs {
     // the launch shares no buffer with the kernel before it in the stream:
     // the tiled kernel may start its copies while that kernel drains
     bool overlap_prev = false;
+    // the records were just written by the previous kernel in the stream (the
+    // device sampler): with overlap_prev the tiled kernel requests its first
+    // bands before that kernel has completed and reads the records after
+    bool records_from_prev = false;
     // windows of a strided source (tr_fused_norm_crop); otherwise a compact
     // NHWC source of H x W images
     bool crop_src = false;
@@ -78,7 +82,10 @@ void tune_tiled(int band_bytes, int stages, int ctas_per_sm, int flags);
 int make_sample_spec(uint64_t seed, uint64_t offset, int H, int W, int flip_enabled, float flip_p,
                      int erase_enabled, float erase_p, float scale_lo, float scale_hi, float ratio_lo,
                      float ratio_hi, SampleSpec* sp);
-int launch_sampler(const SampleSpec& sp, int N, tr_aug_param* d_out, void* stream);
+// overlap: the previous kernel in the stream does not use d_out (see
+// sample_kernel); the sampler then writes at once and waits for that kernel
+// only before it exits.
+int launch_sampler(const SampleSpec& sp, int N, tr_aug_param* d_out, void* stream, bool overlap = false);
 
 // Count of kernels launched by this library.
 void count_launch();

@@ -14,30 +14,43 @@
 namespace trfn {
 namespace {
 
+// Launched with programmatic stream serialization.  Normally the records
+// buffer may still be read by the previous kernel in the stream, so the
+// kernel waits for it before writing and then lets the next kernel start.
+// With `overlap` the caller has promised that the previous kernel does not
+// use the records buffer: the kernel lets the next one start and writes at
+// once, and waits for the previous kernel only before it exits, so it still
+// completes after it (the fused kernel that reads these records waits for
+// this one, hence for both).
+__device__ __forceinline__ void sampler_enter(int overlap) {
+    if (!overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void sampler_leave(int overlap) {
+    if (overlap) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // One thread per image: for batches too large for a warp each in one wave.
 __global__ void __launch_bounds__(128) sample_kernel(const __grid_constant__ SampleSpec sp, int N,
-                                                     tr_aug_param* out) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                                                     tr_aug_param* out, int overlap) {
+    sampler_enter(overlap);
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
-    out[n] = sample_record(sp, n);
+    if (n < N) out[n] = sample_record(sp, n);
+    sampler_leave(overlap);
 }
 
 // One warp per image: lane k computes the image's draw k, so a record costs
 // one Philox evaluation of latency instead of one per draw.
 __global__ void __launch_bounds__(128) sample_kernel_warp(const __grid_constant__ SampleSpec sp, int N,
-                                                          tr_aug_param* out) {
-    // launched with programmatic stream serialization: the records buffer may
-    // still be read by the previous kernel in the stream, so wait for it
-    // before writing, and let the next kernel start its prologue right away
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+                                                          tr_aug_param* out, int overlap) {
+    sampler_enter(overlap);
     const int n = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
-    if (n >= N) return;   // whole warps leave together
-    const tr_aug_param a = sample_record_warp(sp, n, lane);
-    if (lane == 0) out[n] = a;
+    if (n < N) {   // whole warps take the same branch
+        const tr_aug_param a = sample_record_warp(sp, n, lane);
+        if (lane == 0) out[n] = a;
+    }
+    sampler_leave(overlap);
 }
 
 }  // namespace
@@ -67,7 +80,7 @@ int make_sample_spec(uint64_t seed, uint64_t offset, int H, int W, int flip_enab
     return TR_OK;
 }
 
-int launch_sampler(const SampleSpec& sp, int N, tr_aug_param* d_out, void* stream) {
+int launch_sampler(const SampleSpec& sp, int N, tr_aug_param* d_out, void* stream, bool overlap) {
     if (N == 0) return TR_OK;
     // A warp per image for small batches (shortest latency: 1.3 us for 256
     // images against 1.6 us), a thread per image beyond (a warp per image
@@ -91,8 +104,9 @@ int launch_sampler(const SampleSpec& sp, int N, tr_aug_param* d_out, void* strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = per_warp ? cudaLaunchKernelEx(&cfg, sample_kernel_warp, sp, N, d_out)
-                                   : cudaLaunchKernelEx(&cfg, sample_kernel, sp, N, d_out);
+    const int ov = overlap ? 1 : 0;
+    const cudaError_t e = per_warp ? cudaLaunchKernelEx(&cfg, sample_kernel_warp, sp, N, d_out, ov)
+                                   : cudaLaunchKernelEx(&cfg, sample_kernel, sp, N, d_out, ov);
     if (e != cudaSuccess) {
         set_last_error("sample kernel launch", (int)e);
         return TR_ERR_CUDA;

@@ -322,6 +322,19 @@ int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W,
                           const tr_aug_sampling* sampling, tr_aug_param* d_records, uint64_t* next_offset,
                           int out_dtype, int out_layout, void* stream, int variant, void* workspace);
 
+/* tr_fused_norm_sampled with launch options (flags as tr_fused_norm_ex).
+ * With TR_LAUNCH_OVERLAP_PREVIOUS the caller promises that the kernel before
+ * this call in the stream uses none of src, dst, d_records and workspace: the
+ * sampler then writes the records while that kernel drains, and the fused
+ * kernel requests its first bands at once and reads the records once the
+ * sampler (which itself completes only after the previous kernel) is done.
+ * The crop and odd-row forms wait for the sampler before they touch memory. */
+int tr_fused_norm_sampled_ex(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
+                             const float* mean, const float* std, uint64_t seed, uint64_t offset,
+                             const tr_aug_sampling* sampling, tr_aug_param* d_records, uint64_t* next_offset,
+                             int out_dtype, int out_layout, void* stream, int variant, void* workspace,
+                             unsigned flags);
+
 /* Host check of N records: TR_OK when every rectangle is either "no erase"
  * (h <= 0 or w <= 0) or lies inside the H x W image; else
  * TR_ERR_INVALID_ARGUMENT with the first bad index in *bad_index (may be

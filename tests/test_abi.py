@@ -82,6 +82,8 @@ def test_null_and_bad_constants_rejected():
     assert L.tr_fused_norm_ex(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0, None, 2) == INVALID
     assert L.tr_fused_norm_ex(0x1000, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0, 0x3004, 1) == INVALID
     assert L.tr_fused_norm_ex(0x1000, 0x100000, 0, 2, 2, 3, M3, S3, None, 0, 0, None, 0, None, 1) == 0
+    assert L.tr_fused_norm_crop_ex(0x1000, 2, 2, 6, 12, None, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0,
+                                   None, 4) == INVALID
     # overlapping src and dst
     assert L.tr_fused_norm(0x1000, 0x1004, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
     # a bad kernel choice

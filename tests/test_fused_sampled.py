@@ -105,3 +105,48 @@ def test_bad_arguments_launch_nothing():
         trfn.tr_fused_norm_sampled(src, dst, MEAN[:C], STD[:C], 0, 0,
                                    dst.view(-1).view(torch.int32)[:N * 5].view(N, 5))
     assert trfn.tr_launch_count() == before
+
+
+@pytest.mark.parametrize("shape,dt,layout", [((64, 224, 224, 3), trfn.OUT_F16, trfn.LAYOUT_NHWC),
+                                             ((32, 224, 224, 3), trfn.OUT_F32, trfn.LAYOUT_NCHW),
+                                             ((24, 299, 299, 3), trfn.OUT_F16, trfn.LAYOUT_NHWC)])   # odd-row form
+def test_overlapped_sampled_launches(shape, dt, layout):
+    """tr_fused_norm_sampled_ex with TR_LAUNCH_OVERLAP_PREVIOUS: a large
+    launch, then consecutive sampled batches with their own source, output
+    and records, workspaces alternating.  Each sampler writes while the
+    kernel before it drains, each fused kernel requests its first bands
+    before its sampler is done: records and outputs equal the oracle's."""
+    import torch
+    N, H, W, C = shape
+    K = 6
+    tdt = torch.float16 if dt == trfn.OUT_F16 else torch.float32
+    srcs = [synth.pixels_uniform(900 + k, N, H, W, C) for k in range(K)]
+    d_src = [torch.from_numpy(x).cuda() for x in srcs]
+    dsts = [torch.full(trfn.out_shape(N, H, W, C, layout), 3.0, dtype=tdt, device="cuda") for _ in range(K)]
+    recs = [torch.full((N, 5), -7, dtype=torch.int32, device="cuda") for _ in range(K)]
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    big = synth.pixels_uniform(950, 256, 224, 224, 3)
+    d_big = torch.from_numpy(big).cuda()
+    d_big_out = torch.empty((256, 224, 224, 3), dtype=torch.float16, device="cuda")
+    st = torch.cuda.Stream()
+    for rep in range(2):
+        for d in dsts:
+            d.fill_(3.0)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            trfn.tr_fused_norm(d_big, d_big_out, MEAN[:3], STD[:3], None, stream=st, workspace=wss[1])
+            for k in range(K):
+                trfn.tr_fused_norm_sampled(d_src[k], dsts[k], MEAN[:C], STD[:C], 70 + k, 24 * k, recs[k],
+                                           out_dtype=dt, layout=layout, stream=st, workspace=wss[k % 2],
+                                           overlap_previous=True)
+        torch.cuda.synchronize()
+        for k in range(K):
+            ref_rec, _ = oracle.sample_aug_params_blocked(70 + k, 24 * k, N, H, W)
+            assert np.array_equal(recs[k].cpu().numpy(), ref_rec)
+            ref = oracle.fused_norm(srcs[k], MEAN[:C], STD[:C], ref_rec, out_dtype=dt, layout=layout)
+            assert_parity(_bits(dsts[k], dt), ref, dt, "overlapped sampled batch %d" % k)
+        for ws in wss:
+            assert int(ws.count_nonzero()) == 0
+    ref_big = oracle.fused_norm(big, MEAN[:3], STD[:3], None, out_dtype=trfn.OUT_F16)
+    assert_parity(_bits(d_big_out, trfn.OUT_F16), ref_big, trfn.OUT_F16, "launch before the chain")
+    assert trfn.tr_device_status() == 0

@@ -1803,7 +1803,7 @@ bool tiled_crop_supported(const uint8_t* src, const void* dst, int N, int H, int
     if (((size_t)src_W * C) % 16 != 0 || row_stride % 16 != 0 || image_stride % 16 != 0) return false;
     if (image_stride < (size_t)src_H * row_stride) return false;
     if (((size_t)W * C + 30) / 16 > 256) return false;
-    if ((size_t)src_W * C / 16 > 0xFFFFFFFFull || (long long)src_H > 0xFFFFFFFFll) return false;
+    if ((size_t)src_W * C / 16 > 0xFFFFFFFFull) return false;   // chunk count of a source row (uint32)
     return true;
 }
 

@@ -24,7 +24,14 @@
 //    through a TMA tensor copy (cp.async.bulk.tensor): the source is
 //    described as {chunk, chunk index, row, image} with 16- or 32-byte
 //    chunks, so a window may start at any byte; consumers realign the first
-//    chunk's offset with funnel shifts.
+//    chunk's offset with funnel shifts.  Rows (or output rows, or an output
+//    pointer) that are not 16-byte aligned take an odd-row form: bands staged
+//    from the 16-byte boundary below them, groups realigned in registers,
+//    output tiles that follow the band's global alignment.
+//    Launches are chained with programmatic dependent launch: a CTA releases
+//    the next grid once the previous one has completed; a launch its caller
+//    declared independent of the previous one starts its copies before that
+//    grid has completed (TR_LAUNCH_OVERLAP_PREVIOUS).
 //  * GENERIC: one thread per output pixel, any shape, stride and alignment.
 //
 // Both kernels compute each value as fma(float(x), scale_c, bias_c) with the
@@ -277,10 +284,12 @@ struct TiledParams {
     int stages;
     unsigned int* ws;      // scheduling workspace (ticket counters, finished CTAs), or null
     int hints;             // tr_tune_tiled flags (include/tr_fused_norm.h): L2 policies
-                           // (bits 0-2), early dependent launch (3), exit after the last
-                           // store's shared-memory reads (4), record before the first
-                           // band (5), bounded-wait test hook (6), erased-span rule
-                           // (11, 12-15)
+                           // (bits 0-2), late release of the next grid (3), exit after
+                           // the last store's shared-memory reads (4), record before the
+                           // first band (5), bounded-wait test hook (6), unrotated tile
+                           // stores (7), erased-span rule (11, 12-15); set by the launch:
+                           // overlap the previous grid (8), records written by it (9),
+                           // odd-row element stores (10)
     float scale[4];
     float bias[4];
 };

@@ -95,6 +95,10 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     if ((flags & ~(unsigned)TR_LAUNCH_OVERLAP_PREVIOUS) != 0) return TR_ERR_INVALID_ARGUMENT;
     int rc = check_shape(N, H, W, C, out_dtype, out_layout);
     if (rc != TR_OK) return rc;
+    // one channel: NCHW and NHWC are the same bytes; the NHWC path's tile
+    // stores avoid shared-memory bank conflicts (binary32 256x224x224x1:
+    // 0.88 -> 0.94 of the copy peak)
+    if (C == 1 && out_layout == TR_LAYOUT_NCHW) out_layout = TR_LAYOUT_NHWC;
     if (variant != TR_VARIANT_AUTO && variant != TR_VARIANT_TILED && variant != TR_VARIANT_GENERIC)
         return TR_ERR_INVALID_ARGUMENT;
     if (mean == nullptr || stdv == nullptr) return TR_ERR_INVALID_ARGUMENT;
@@ -287,6 +291,7 @@ int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int
     const int rc = check_shape(N, H, W, C, out_dtype, out_layout);
     if (rc != TR_OK) return rc;
     if (variant == nullptr) return TR_ERR_INVALID_ARGUMENT;
+    if (C == 1 && out_layout == TR_LAYOUT_NCHW) out_layout = TR_LAYOUT_NHWC;   // the same bytes, as in the launch
     *variant = (tiled_supported(src_u8, dst, N, H, W, C, out_dtype, out_layout) &&
                 !small_batch(N, H, W, C, out_layout))
                    ? TR_VARIANT_TILED

@@ -1399,16 +1399,19 @@ TiledPlan balance_strides(const TiledPlan& pl, int want, int H, int W, int C, in
 }
 
 TiledPlan plan_tiled_compact(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm,
-                             int reserved, bool odd, long long N, int sm_count) {
+                             int reserved, bool odd, long long N, int sm_count, bool overlapped) {
     const size_t slack = odd ? 64 : 0;
     const TiledPlan pl = plan_tiled_r(H, W, C, f16, layout, smem_limit, 0, slack, 0, odd);
     if (g_flags.load(std::memory_order_relaxed) & 65536) return pl;
     // 4-stage plans (small bands) are lowered only where each CTA gets few
     // bands, so that latency, not bandwidth, bounds the launch (1024x50x50x3
-    // to binary32: 0.48 -> 0.55 of the copy peak with the lower height)
+    // to binary32: 0.48 -> 0.55 of the copy peak with the lower height), or
+    // where the launch overlaps the previous one, whose drain then hides the
+    // extra bands' cost (256x224x224 binary32, overlapping: grayscale 0.938 ->
+    // 0.965, four channels 0.998 -> 1.003, RGB NHWC4 0.995 -> 0.997)
     const long long slots = (long long)std::max(1, smem_residency(pl, smem_per_sm, reserved)) * std::max(1, sm_count);
     const bool few_bands = pl.ok && N * pl.bands < kStreamMinBandsPerCta * slots;
-    const TiledPlan fit = (pl.stages > 3 && !few_bands)
+    const TiledPlan fit = (pl.stages > 3 && !few_bands && !overlapped)
                               ? pl
                               : lower_to_residency(pl, kWantResidency, H, W, C, f16, layout, smem_limit, smem_per_sm,
                                                    reserved, 0, slack, odd);
@@ -1448,10 +1451,10 @@ TiledPlan plan_tiled_odd(int H, int W, int C, int f16, int layout, int smem_limi
 // one resident CTA per SM against the compact geometry; then take the largest
 // lower band height that restores it.
 TiledPlan plan_tiled_crop(int H, int W, int C, int f16, int layout, int smem_limit, int smem_per_sm,
-                          int reserved, size_t pitch, size_t slack, long long N, int sm_count) {
+                          int reserved, size_t pitch, size_t slack, long long N, int sm_count, bool overlapped) {
     const TiledPlan pl = plan_tiled(H, W, C, f16, layout, smem_limit, pitch, slack);
     const int want = smem_residency(plan_tiled_compact(H, W, C, f16, layout, smem_limit, smem_per_sm, reserved, false,
-                                                       N, sm_count),
+                                                       N, sm_count, overlapped),
                                     smem_per_sm, reserved);
     return lower_to_residency(pl, want, H, W, C, f16, layout, smem_limit, smem_per_sm, reserved, pitch, slack, false);
 }
@@ -1641,7 +1644,7 @@ int launch_tiled(const LaunchArgs& a) {
     TiledPlan pl;
     if (crop) {
         pl = plan_tiled_crop(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
-                             nch * chunk, 16, a.N, di.sm_count);
+                             nch * chunk, 16, a.N, di.sm_count, a.overlap_prev);
     } else if (odd && !(tflags & 524288)) {
         // Launches in which each CTA streams many bands are bound by the
         // conversion: there the odd-row planning (two stages, more CTAs per
@@ -1650,7 +1653,7 @@ int launch_tiled(const LaunchArgs& a) {
         // does better (100x100 and 50x50 images), as it does where the odd-row
         // planning cannot add a CTA (binary32 RGB, 4-channel outputs).
         pl = plan_tiled_compact(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
-                                true, a.N, di.sm_count);
+                                true, a.N, di.sm_count, a.overlap_prev);
         int res = 0, reg_res = 0;
         int rc = pl.ok ? tiled_occupancy(fn, dev, di.smem_optin, pl.threads, pl.smem, &res) : TR_OK;
         if (rc == TR_OK) rc = tiled_occupancy(fn, dev, di.smem_optin, 256, 0, &reg_res);
@@ -1669,7 +1672,7 @@ int launch_tiled(const LaunchArgs& a) {
         }
     } else {
         pl = plan_tiled_compact(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
-                                odd, a.N, di.sm_count);
+                                odd, a.N, di.sm_count, a.overlap_prev);
     }
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 

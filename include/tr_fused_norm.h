@@ -526,9 +526,11 @@ int tr_device_status(int* flags, int clear);
  *   band_bytes       source bytes per row band (default: about 32 KB of
  *                    output per band; the band height is the largest divisor
  *                    of H near the target, else the height that splits H into
- *                    as many bands as evenly as a fixed height allows; for
- *                    3-stage plans lowered (down to half) where three CTAs
- *                    would not fit an SM, then lowered where a band's groups
+ *                    as many bands as evenly as a fixed height allows;
+ *                    lowered (down to half) where three CTAs would not fit an
+ *                    SM — for 4-stage plans only when the launch overlaps the
+ *                    previous one or gives each CTA fewer than five bands —
+ *                    then lowered where a band's groups
  *                    leave the consumer threads' last stride mostly empty;
  *                    crop sources may lower it so that as many CTAs fit an
  *                    SM as for a compact source; the odd-row form, where each
@@ -575,8 +577,8 @@ int tr_device_status(int* flags, int clear);
  *                    bands too, bits 12..15 = v != 0 set the threshold to
  *                    (v - 1) * 128 bytes; bit 16 keeps the band height of
  *                    about 32 KB of output where it leaves fewer than three
- *                    CTAs on an SM (default, for plans of at most three
- *                    stages: the largest lower height, down to half, at
+ *                    CTAs on an SM (default, with the exceptions given under
+ *                    band_bytes: the largest lower height, down to half, at
  *                    which three fit), bit 18 keeps that height
  *                    even where a band's last stride of consumer threads is
  *                    mostly empty (default: the largest lower height, down to

@@ -207,3 +207,66 @@ def test_small_launches_never_run_ahead_of_a_large_one():
         for ws in wss:
             assert int(ws.count_nonzero()) == 0
     assert trfn.tr_device_status() == 0
+
+
+def test_random_overlapped_chains_match_waiting_launches():
+    """About ten seconds of random chains of overlapped launches (sizes from
+    2 to 512 images, aligned and odd-row forms, every layout, both types,
+    workspaces alternating, eager and replayed from graphs): every output
+    equals, bit for bit, the same launch run without the option, and the
+    workspaces are zero after every chain."""
+    import time
+    import torch
+    rng = np.random.default_rng(11)
+    shapes = [(256, 224, 224, 3), (8, 224, 224, 3), (64, 299, 299, 3), (512, 28, 28, 3), (2, 224, 224, 3),
+              (128, 256, 256, 3), (16, 32, 32, 3), (96, 227, 227, 3)]
+    bufs = []
+    for i, (N, H, W, C) in enumerate(shapes):
+        g = torch.Generator(device="cuda").manual_seed(300 + i)
+        src = torch.randint(0, 256, (N, H, W, C), dtype=torch.uint8, device="cuda", generator=g)
+        rec, _ = oracle.sample_aug_params(400 + i, 0, N, H, W)
+        aug = torch.from_numpy(rec).cuda()
+        dt = F16 if i % 2 == 0 else F32
+        lay = (NHWC, NCHW, trfn.LAYOUT_NHWC4)[i % 3]
+        tdt = torch.float16 if dt == F16 else torch.float32
+        out = torch.empty(trfn.out_shape(N, H, W, C, lay), dtype=tdt, device="cuda")
+        ref = torch.empty_like(out)
+        trfn.tr_fused_norm(src, ref, MEAN, STD, aug, out_dtype=dt, layout=lay)
+        bufs.append((src, aug, dt, lay, out, ref))
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    t0, chains = time.time(), 0
+    while time.time() - t0 < 10.0:
+        order = rng.permutation(len(bufs)).tolist() + rng.integers(0, len(bufs), 4).tolist()
+        seq = [order[0]] + [b for a, b in zip(order, order[1:]) if a != b]   # no buffer twice in a row
+
+        def run():
+            for k, j in enumerate(seq):
+                src, aug, dt, lay, out, _ = bufs[j]
+                trfn.tr_fused_norm(src, out, MEAN, STD, aug, out_dtype=dt, layout=lay, stream=st,
+                                   workspace=wss[k % 2], overlap_previous=True)
+        for b in bufs:
+            b[4].fill_(7.0)
+        torch.cuda.synchronize()
+        if chains % 3 == 2:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=st):
+                run()
+            for b in bufs:
+                b[4].fill_(7.0)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(st):
+                graph.replay()
+                graph.replay()
+        else:
+            with torch.cuda.stream(st):
+                run()
+        torch.cuda.synchronize()
+        for j in set(seq):
+            assert torch.equal(bufs[j][4], bufs[j][5]), "chain %d, buffer %d, sequence %s" % (chains, j, seq)
+        for w in wss:
+            assert int(w.count_nonzero()) == 0, "chain %d" % chains
+        chains += 1
+    assert chains > 100
+    assert trfn.tr_device_status() == 0

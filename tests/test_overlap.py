@@ -212,9 +212,10 @@ def test_small_launches_never_run_ahead_of_a_large_one():
 def test_random_overlapped_chains_match_waiting_launches():
     """About ten seconds of random chains of overlapped launches (sizes from
     2 to 512 images, aligned and odd-row forms, every layout, both types,
-    workspaces alternating, eager and replayed from graphs): every output
-    equals, bit for bit, the same launch run without the option, and the
-    workspaces are zero after every chain."""
+    host-made records and records drawn on the GPU in the same call,
+    workspaces alternating, eager and replayed from graphs): every output and
+    every GPU-made record equals, bit for bit, the same launch run without the
+    option, and the workspaces are zero after every chain."""
     import time
     import torch
     rng = np.random.default_rng(11)
@@ -231,8 +232,13 @@ def test_random_overlapped_chains_match_waiting_launches():
         tdt = torch.float16 if dt == F16 else torch.float32
         out = torch.empty(trfn.out_shape(N, H, W, C, lay), dtype=tdt, device="cuda")
         ref = torch.empty_like(out)
-        trfn.tr_fused_norm(src, ref, MEAN, STD, aug, out_dtype=dt, layout=lay)
-        bufs.append((src, aug, dt, lay, out, ref))
+        sampled = i % 4 == 1
+        rref = aug.clone()
+        if sampled:
+            trfn.tr_fused_norm_sampled(src, ref, MEAN, STD, 600 + i, 24 * i, rref, out_dtype=dt, layout=lay)
+        else:
+            trfn.tr_fused_norm(src, ref, MEAN, STD, aug, out_dtype=dt, layout=lay)
+        bufs.append((src, aug, dt, lay, out, ref, sampled, i, rref))
     wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
     st = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -243,19 +249,26 @@ def test_random_overlapped_chains_match_waiting_launches():
 
         def run():
             for k, j in enumerate(seq):
-                src, aug, dt, lay, out, _ = bufs[j]
-                trfn.tr_fused_norm(src, out, MEAN, STD, aug, out_dtype=dt, layout=lay, stream=st,
-                                   workspace=wss[k % 2], overlap_previous=True)
-        for b in bufs:
-            b[4].fill_(7.0)
-        torch.cuda.synchronize()
+                src, aug, dt, lay, out, _, sampled, i, _ = bufs[j]
+                if sampled:
+                    trfn.tr_fused_norm_sampled(src, out, MEAN, STD, 600 + i, 24 * i, aug, out_dtype=dt, layout=lay,
+                                               stream=st, workspace=wss[k % 2], overlap_previous=True)
+                else:
+                    trfn.tr_fused_norm(src, out, MEAN, STD, aug, out_dtype=dt, layout=lay, stream=st,
+                                       workspace=wss[k % 2], overlap_previous=True)
+
+        def reset():
+            for b in bufs:
+                b[4].fill_(7.0)
+                if b[6]:
+                    b[1].fill_(-9)
+            torch.cuda.synchronize()
+        reset()
         if chains % 3 == 2:
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=st):
                 run()
-            for b in bufs:
-                b[4].fill_(7.0)
-            torch.cuda.synchronize()
+            reset()
             with torch.cuda.stream(st):
                 graph.replay()
                 graph.replay()
@@ -265,6 +278,7 @@ def test_random_overlapped_chains_match_waiting_launches():
         torch.cuda.synchronize()
         for j in set(seq):
             assert torch.equal(bufs[j][4], bufs[j][5]), "chain %d, buffer %d, sequence %s" % (chains, j, seq)
+            assert torch.equal(bufs[j][1], bufs[j][8]), "records: chain %d, buffer %d" % (chains, j)
         for w in wss:
             assert int(w.count_nonzero()) == 0, "chain %d" % chains
         chains += 1

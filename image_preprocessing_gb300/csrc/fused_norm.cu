@@ -1138,6 +1138,7 @@ struct GenericParams {
     DivU32 div_w, div_h;   // x / W and x / H for 32-bit pixel indices
     float scale[4];
     float bias[4];
+    int overlap;           // the launch shares no buffer with the previous grid in the stream
 };
 
 // One thread per output pixel, consecutive threads on consecutive pixels of
@@ -1149,7 +1150,15 @@ template <int C, int OUT_F16, int LAYOUT>
 __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ GenericParams p) {
     constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
     constexpr int OB = OUT_F16 ? 2 : 4;
-    grid_dependency_wait();
+    // Global memory only after the previous grid in the stream has completed,
+    // unless the caller declared this launch independent of it: then thread
+    // 0 of each block waits for it while the others start, so the grid still
+    // completes after it.  Either way a block releases the next grid only
+    // once the previous one has completed (as the tiled kernel does).
+    if (!p.overlap || threadIdx.x == 0) {
+        grid_dependency_wait();
+        if (threadIdx.x == 0) grid_launch_dependents();
+    }
     const long long pixels = (long long)p.N * p.H * p.W;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < pixels; t += stride) {
@@ -1763,6 +1772,9 @@ int launch_generic(const LaunchArgs& a) {
     const int threads = 256;
     p.div_w = make_div((uint32_t)a.W);
     p.div_h = make_div((uint32_t)a.H);
+    // records written by the previous grid (the device sampler) are read only
+    // after it has completed
+    p.overlap = (a.overlap_prev && !a.records_from_prev) ? 1 : 0;
     const long long pixels = (long long)a.N * a.H * a.W;
     // about 8 pixels per thread, between 8 and 32 blocks per SM (measured:
     // 32 blocks per SM 11 % faster for 256 x 227x227x3, 8 better for 1024

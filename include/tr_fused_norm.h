@@ -163,8 +163,9 @@ enum {
      * this library's previous launch on the same stream is not overlapped (the
      * flag is dropped).  A launch releases the next kernel in the stream only
      * once the kernel before it has completed, so no launch ever overlaps
-     * more than the one kernel before it.  The GENERIC kernel ignores the
-     * flag.                                                                 */
+     * more than the one kernel before it.  The GENERIC kernel (small batches,
+     * strided or unaligned buffers) honours the flag the same way: one thread
+     * of each block waits for the previous kernel while the others work.     */
     TR_LAUNCH_OVERLAP_PREVIOUS = 1
 };
 

@@ -72,6 +72,8 @@ _SIGNATURES = {
     "tr_fused_norm_crop_ex": (_i, [_vp, _i, _i, ctypes.c_size_t, ctypes.c_size_t, _vp, _vp, _i, _i, _i, _i, _fp, _fp,
                                    _vp, _i, _i, _vp, _i, _vp, ctypes.c_uint]),
     "tr_fused_norm_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp]),
+    "tr_fused_norm_geometry": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_uint, ctypes.POINTER(_i),
+                                    ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "tr_fused_norm_plan": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i)]),
     "tr_norm_preset": (_i, [_i, _fp, _fp, ctypes.POINTER(_i)]),
     "tr_sample_aug_params": (_i, [_u64, _u64, _i, _i, _i, _i, _f, _i, _f, _f, _f, _f, _f, _vp,

@@ -160,6 +160,19 @@ def tr_fused_norm_plan(src, dst, N, H, W, C, out_dtype, layout):
     return v.value
 
 
+def tr_fused_norm_geometry(N, H, W, C, out_dtype=OUT_F16, layout=LAYOUT_NHWC, src=0x100000000, dst=0x200000000,
+                           overlap_previous=False):
+    """The TILED kernel's geometry for these arguments (tr_fused_norm_geometry):
+    dict of rows, stages, ctas_per_sm, grid, odd_form.  src and dst are device
+    addresses whose alignment the choice depends on (16-byte aligned
+    defaults)."""
+    out = [ctypes.c_int(0) for _ in range(5)]
+    check(lib().tr_fused_norm_geometry(src, dst, N, H, W, C, _code(out_dtype, _DTYPES), _code(layout, _LAYOUTS),
+                                       LAUNCH_OVERLAP_PREVIOUS if overlap_previous else 0,
+                                       *[ctypes.byref(o) for o in out]), "tr_fused_norm_geometry")
+    return dict(zip(("rows", "stages", "ctas_per_sm", "grid", "odd_form"), (o.value for o in out)))
+
+
 def tr_norm_preset(preset):
     pid = PRESETS[preset] if isinstance(preset, str) else int(preset)
     m = (ctypes.c_float * 3)()

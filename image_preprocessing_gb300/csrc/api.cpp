@@ -299,6 +299,39 @@ int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int
     return TR_OK;
 }
 
+int tr_fused_norm_geometry(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C, int out_dtype,
+                           int out_layout, unsigned flags, int* rows, int* stages, int* ctas_per_sm, int* grid,
+                           int* odd_form) {
+    if ((flags & ~(unsigned)TR_LAUNCH_OVERLAP_PREVIOUS) != 0) return TR_ERR_INVALID_ARGUMENT;
+    const int rc = check_shape(N, H, W, C, out_dtype, out_layout);
+    if (rc != TR_OK) return rc;
+    if (N < 1 || rows == nullptr || stages == nullptr || ctas_per_sm == nullptr || grid == nullptr ||
+        odd_form == nullptr)
+        return TR_ERR_INVALID_ARGUMENT;
+    if (C == 1 && out_layout == TR_LAYOUT_NCHW) out_layout = TR_LAYOUT_NHWC;   // as in the launch
+    if (!tiled_supported(src_u8, dst, N, H, W, C, out_dtype, out_layout)) return TR_ERR_NOT_SUPPORTED;
+    LaunchArgs a;
+    for (int c = 0; c < 4; ++c) { a.scale[c] = 0.0f; a.bias[c] = 0.0f; }
+    a.src = src_u8;
+    a.dst = const_cast<void*>(dst);
+    a.N = N; a.H = H; a.W = W; a.C = C;
+    a.aug = nullptr;
+    a.out_dtype = out_dtype;
+    a.out_layout = out_layout;
+    a.stream = nullptr;
+    a.workspace = nullptr;
+    a.overlap_prev = (flags & TR_LAUNCH_OVERLAP_PREVIOUS) != 0;
+    TiledGeometry g;
+    const int r2 = tiled_geometry(a, &g);
+    if (r2 != TR_OK) return r2;
+    *rows = g.rows;
+    *stages = g.stages;
+    *ctas_per_sm = g.ctas_per_sm;
+    *grid = g.grid;
+    *odd_form = g.odd_form;
+    return TR_OK;
+}
+
 int tr_norm_preset(int preset, float mean[3], float std[3], int* channels) {
     if (mean == nullptr || std == nullptr || channels == nullptr) return TR_ERR_INVALID_ARGUMENT;
     // values of the preset table in the FusedNormalization article, §九

@@ -1627,7 +1627,21 @@ int tiled_occupancy(TiledFn fn, int dev, int smem_optin, int threads, size_t sme
     return TR_OK;
 }
 
-int launch_tiled(const LaunchArgs& a) {
+// Everything a tiled launch decides before its parameters: the kernel form,
+// the band plan, CTAs per SM and the grid (shared by the launch and by
+// tr_fused_norm_geometry).
+struct TiledSetup {
+    TiledPlan pl;
+    TiledFn fn = nullptr;
+    bool crop = false, odd = false;
+    int chunk_shift = 4;
+    size_t chunk = 16, nch = 0;
+    int blocks_per_sm = 0;
+    long long grid = 0, waves = 0;
+    int tflags = 0;
+};
+
+int setup_tiled(const LaunchArgs& a, TiledSetup* t) {
     int dev = 0;
     if (!check_cuda(cudaGetDevice(&dev), "cudaGetDevice")) return TR_ERR_CUDA;
     const DeviceInfo di = device_info(dev);
@@ -1685,12 +1699,53 @@ int launch_tiled(const LaunchArgs& a) {
     }
     if (!pl.ok) return TR_ERR_NOT_SUPPORTED;
 
+    int blocks_per_sm = 0;
+    {
+        const int rc = tiled_occupancy(fn, dev, di.smem_optin, pl.threads, pl.smem, &blocks_per_sm);
+        if (rc != TR_OK) return rc;
+        if (blocks_per_sm <= 0) return TR_ERR_NOT_SUPPORTED;
+    }
+    const int cap = g_ctas_per_sm.load(std::memory_order_relaxed);
+    if (cap > 0) blocks_per_sm = std::min(blocks_per_sm, cap);
+    const long long num_units = (long long)a.N * pl.bands;
+    const long long max_ctas = (long long)blocks_per_sm * di.sm_count;
+    long long grid = std::min<long long>(num_units, max_ctas);
+    // equalise the number of units per CTA
+    const long long waves = (num_units + grid - 1) / grid;
+    grid = (num_units + waves - 1) / waves;
+
+    t->pl = pl;
+    t->fn = fn;
+    t->crop = crop;
+    t->odd = odd;
+    t->chunk_shift = chunk_shift;
+    t->chunk = chunk;
+    t->nch = nch;
+    t->blocks_per_sm = blocks_per_sm;
+    t->grid = grid;
+    t->waves = waves;
+    t->tflags = tflags;
+    return TR_OK;
+}
+
+int launch_tiled(const LaunchArgs& a) {
+    TiledSetup t;
+    {
+        const int rc = setup_tiled(a, &t);
+        if (rc != TR_OK) return rc;
+    }
+    const TiledPlan& pl = t.pl;
+    const bool crop = t.crop, odd = t.odd;
+    const size_t chunk = t.chunk, nch = t.nch;
+    const int tflags = t.tflags;
+    const size_t L = (size_t)a.W * a.C;
+
     TiledParams p;
     p.crop = a.crop;
     p.src_H = crop ? a.src_H : a.H;
     p.src_W = crop ? a.src_W : a.W;
     p.in_pitch = (uint32_t)(crop ? nch * chunk : L);
-    p.chunk_shift = chunk_shift;
+    p.chunk_shift = t.chunk_shift;
     if (crop) {
         const int rc = encode_crop_map(&p.tmap, a, (uint32_t)chunk, (uint32_t)nch, (uint32_t)pl.R,
                                        (tflags & 512) != 0);
@@ -1719,19 +1774,6 @@ int launch_tiled(const LaunchArgs& a) {
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
 
-    int blocks_per_sm = 0;
-    {
-        const int rc = tiled_occupancy(fn, dev, di.smem_optin, pl.threads, pl.smem, &blocks_per_sm);
-        if (rc != TR_OK) return rc;
-        if (blocks_per_sm <= 0) return TR_ERR_NOT_SUPPORTED;
-    }
-    const int cap = g_ctas_per_sm.load(std::memory_order_relaxed);
-    if (cap > 0) blocks_per_sm = std::min(blocks_per_sm, cap);
-    const long long max_ctas = (long long)blocks_per_sm * di.sm_count;
-    long long grid = std::min<long long>(p.num_units, max_ctas);
-    // equalise the number of units per CTA
-    const long long waves = (p.num_units + grid - 1) / grid;
-    grid = (p.num_units + waves - 1) / waves;
     // The odd-row form's register realignment of group outputs lengthens a
     // band's conversion: it pays when a CTA streams many bands (6 to 13 for
     // 227- and 299-pixel rows: 0.51 to 0.56 and 0.53 to 0.58 of the copy peak
@@ -1740,9 +1782,9 @@ int launch_tiled(const LaunchArgs& a) {
     // the conversion is on the critical path (28x28 to 100x100 images: 2-12 %
     // slower).  Those launches keep the element stores (tr_tune_tiled flags
     // bit 17 asks for the realignment regardless).
-    if (odd && waves < kStreamMinBandsPerCta && !(tflags & 131072)) p.hints |= 1024;
+    if (odd && t.waves < kStreamMinBandsPerCta && !(tflags & 131072)) p.hints |= 1024;
 
-    if (!check_cuda(launch_pdl((const void*)fn, (unsigned)grid, pl.threads, pl.smem, a.stream, &p),
+    if (!check_cuda(launch_pdl((const void*)t.fn, (unsigned)t.grid, pl.threads, pl.smem, a.stream, &p),
                     "tiled kernel launch"))
         return TR_ERR_CUDA;
     count_launch();
@@ -1829,6 +1871,19 @@ bool tiled_crop_supported(const uint8_t* src, const void* dst, int N, int H, int
     if (((size_t)W * C + 30) / 16 > 256) return false;
     if ((size_t)src_W * C / 16 > 0xFFFFFFFFull) return false;   // chunk count of a source row (uint32)
     return true;
+}
+
+int tiled_geometry(const LaunchArgs& a, TiledGeometry* g) {
+    TiledSetup t;
+    const int rc = setup_tiled(a, &t);
+    if (rc != TR_OK) return rc;
+    g->rows = t.pl.R;
+    g->stages = t.pl.stages;
+    g->threads = t.pl.threads;
+    g->ctas_per_sm = t.blocks_per_sm;
+    g->grid = (int)t.grid;
+    g->odd_form = t.odd ? 1 : 0;
+    return TR_OK;
 }
 
 int launch(const LaunchArgs& a, int variant) {

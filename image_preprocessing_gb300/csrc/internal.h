@@ -66,6 +66,14 @@ bool tiled_crop_supported(const uint8_t* src, const void* dst, int N, int H, int
 // a.stream.  Returns a tr_status.
 int launch(const LaunchArgs& a, int variant);
 
+// What a tiled launch with these arguments would take (host only; occupancy
+// queries need the device): rows per band, shared-memory stages, threads per
+// CTA, CTAs per SM, grid size, and whether the odd-row form applies.
+struct TiledGeometry {
+    int rows, stages, threads, ctas_per_sm, grid, odd_form;
+};
+int tiled_geometry(const LaunchArgs& a, TiledGeometry* g);
+
 // Reads (and optionally clears) the device status word of the current device.
 int read_device_status(int* flags, bool clear);
 

@@ -250,6 +250,22 @@ int tr_fused_norm_noalloc(const uint8_t* src_u8, void* dst, int N, int H, int W,
 int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C,
                        int out_dtype, int out_layout, int* variant);
 
+/* The geometry a TILED launch with these arguments would take, through the
+ * same planning as the launch (host only, launches nothing; the CTAs-per-SM
+ * figure comes from the device's occupancy calculator, so a CUDA device is
+ * needed).  For tests and tuning.
+ *   src_u8, dst  as for tr_fused_norm; only their alignment is used.
+ *   flags        0 or TR_LAUNCH_OVERLAP_PREVIOUS (which changes the planning).
+ *   *rows        rows per band; *stages shared-memory input stages;
+ *   *ctas_per_sm resident CTAs per SM; *grid CTAs launched;
+ *   *odd_form    1 when the odd-row form applies, else 0.
+ * Errors as tr_fused_norm's argument checks; TR_ERR_NOT_SUPPORTED where the
+ * TILED kernel does not apply; TR_ERR_INVALID_ARGUMENT for N < 1 or a NULL
+ * result pointer.                                                          */
+int tr_fused_norm_geometry(const uint8_t* src_u8, const void* dst, int N, int H, int W, int C, int out_dtype,
+                           int out_layout, unsigned flags, int* rows, int* stages, int* ctas_per_sm, int* grid,
+                           int* odd_form);
+
 /* Preset mean/std (article §九).  Writes 3 floats to mean and std (unused
  * channels get mean 0, std 1) and the channel count to *channels.           */
 int tr_norm_preset(int preset, float mean[3], float std[3], int* channels);

@@ -84,6 +84,13 @@ def test_null_and_bad_constants_rejected():
     assert L.tr_fused_norm_ex(0x1000, 0x100000, 0, 2, 2, 3, M3, S3, None, 0, 0, None, 0, None, 1) == 0
     assert L.tr_fused_norm_crop_ex(0x1000, 2, 2, 6, 12, None, 0x100000, 1, 2, 2, 3, M3, S3, None, 0, 0, None, 0,
                                    None, 4) == INVALID
+    # geometry diagnostic: argument checks before any device query
+    r = [ctypes.c_int(0) for _ in range(5)]
+    refs = [ctypes.byref(x) for x in r]
+    assert L.tr_fused_norm_geometry(0x1000, 0x100000, 0, 224, 224, 3, 1, 0, 0, *refs) == INVALID        # N < 1
+    assert L.tr_fused_norm_geometry(0x1000, 0x100000, 8, 224, 224, 3, 1, 0, 2, *refs) == INVALID        # flags
+    assert L.tr_fused_norm_geometry(0x1000, 0x100000, 8, 224, 224, 3, 1, 0, 0, None, *refs[1:]) == INVALID
+    assert L.tr_fused_norm_geometry(0x1001, 0x100000, 8, 224, 224, 3, 1, 0, 0, *refs) == 2   # unaligned source
     # overlapping src and dst
     assert L.tr_fused_norm(0x1000, 0x1004, 1, 2, 2, 3, M3, S3, None, 0, 0, None) == INVALID
     # a bad kernel choice

@@ -66,15 +66,20 @@ struct Sampling {
     tr_aug_param* out = nullptr;   // device, N records
 };
 
-// The workspace of the last launch this library made on each stream (a small
-// table, oldest entry replaced): a launch asking to overlap the kernel before
-// it must not share that kernel's workspace, whose ticket counters are still
-// in use and are zeroed by its last CTA.
+// The workspace of the last launch this library made on each stream (a fixed
+// table, oldest entry replaced; nothing is allocated): a launch asking to
+// overlap the kernel before it must not share that kernel's workspace, whose
+// ticket counters are still in use and are zeroed by its last CTA.  Returns
+// true when the launch must not overlap on that account.  Once an entry has
+// been replaced, a stream missing from the table may be one whose entry was
+// dropped, so its launch is treated as sharing.
 bool note_stream_workspace(void* stream, void* workspace) {
     struct Entry { void* stream; void* ws; bool used; };
+    constexpr int kEntries = 256;
     static std::mutex mu;
-    static Entry table[64];
+    static Entry table[kEntries];
     static int next = 0;
+    static bool replaced = false;
     std::lock_guard<std::mutex> lock(mu);
     for (Entry& e : table) {
         if (e.used && e.stream == stream) {
@@ -83,9 +88,10 @@ bool note_stream_workspace(void* stream, void* workspace) {
             return same;
         }
     }
+    if (table[next].used) replaced = true;
     table[next] = Entry{stream, workspace, true};
-    next = (next + 1) % 64;
-    return false;
+    next = (next + 1) % kEntries;
+    return replaced && workspace != nullptr;
 }
 
 int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,

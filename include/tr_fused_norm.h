@@ -164,7 +164,9 @@ enum {
      * can be overlapped; after a copy, a memset or another library's kernel
      * stream order is unchanged.  A launch whose workspace equals the one of
      * this library's previous launch on the same stream is not overlapped (the
-     * flag is dropped).  A launch releases the next kernel in the stream only
+     * flag is dropped); the library remembers the last 256 streams it launched
+     * on, and once more have been used, a launch with a workspace on a stream
+     * it no longer remembers is not overlapped either.  A launch releases the next kernel in the stream only
      * once the kernel before it has completed, so no launch ever overlaps
      * more than the one kernel before it.  The GENERIC kernel (small batches,
      * strided or unaligned buffers) honours the flag the same way: one thread

@@ -49,8 +49,9 @@ struct tr_transfer_station {
 
 namespace {
 
-// A staged zone to give back once its upload has finished (one per slot:
-// a slot holds at most one batch in flight).
+// A staged zone to give back once its upload has finished.  Each submit
+// queues its own (a host function of an earlier batch may not have run yet
+// when the next batch on the same slot is queued).
 struct StagedRelease {
     tr_staging* st = nullptr;
     long long batch = 0;

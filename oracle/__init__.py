@@ -32,44 +32,46 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        path = build_oracle()
-        L = ctypes.CDLL(path)
-        u8p = ctypes.POINTER(ctypes.c_uint8)
-        f32p = ctypes.POINTER(ctypes.c_float)
-        i32p = ctypes.POINTER(ctypes.c_int32)
-        u16p = ctypes.POINTER(ctypes.c_uint16)
-        u32p = ctypes.POINTER(ctypes.c_uint32)
-        u64p = ctypes.POINTER(ctypes.c_uint64)
-        L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
-        L.oracle_f32_to_f16.restype = ctypes.c_uint16
-        L.oracle_f32_to_f16_array.argtypes = [f32p, u16p, ctypes.c_size_t]
-        L.oracle_f32_to_f16_bits_range.argtypes = [ctypes.c_uint32, ctypes.c_uint32, u16p]
-        L.oracle_norm_preset.argtypes = [ctypes.c_int, f32p, f32p, ctypes.POINTER(ctypes.c_int)]
-        L.oracle_norm_preset.restype = ctypes.c_int
-        L.oracle_fused_norm.argtypes = [u8p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                        ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
-                                        ctypes.c_int, ctypes.c_int]
-        L.oracle_fused_norm.restype = ctypes.c_int
-        L.oracle_fused_norm_crop.argtypes = [u8p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
-                                             i32p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                             ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
-                                             ctypes.c_int, ctypes.c_int]
-        L.oracle_fused_norm_crop.restype = ctypes.c_int
-        L.oracle_exp_f32_array.argtypes = [f32p, f32p, ctypes.c_size_t]
-        L.oracle_sample_aug_params_blocked.argtypes = L.oracle_sample_aug_params.argtypes
-        L.oracle_sample_aug_params_blocked.restype = ctypes.c_int
-        L.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
-        L.oracle_uniform01.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
-        L.oracle_uniform01.restype = ctypes.c_float
-        L.oracle_sample_aug_params.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
-                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
-                                               ctypes.c_int, ctypes.c_float, ctypes.c_float,
-                                               ctypes.c_float, ctypes.c_float, ctypes.c_float, i32p, u64p]
-        L.oracle_sample_aug_params.restype = ctypes.c_int
-        L.oracle_sample_aug_params_blocked.argtypes = L.oracle_sample_aug_params.argtypes
-        L.oracle_sample_aug_params_blocked.restype = ctypes.c_int
-        _lib = L
+        _lib = bind(build_oracle())
     return _lib
+
+
+def bind(path):
+    """Load a library built from fused_norm_oracle.c and declare its functions."""
+    L = ctypes.CDLL(path)
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_f16.restype = ctypes.c_uint16
+    L.oracle_f32_to_f16_array.argtypes = [f32p, u16p, ctypes.c_size_t]
+    L.oracle_f32_to_f16_bits_range.argtypes = [ctypes.c_uint32, ctypes.c_uint32, u16p]
+    L.oracle_norm_preset.argtypes = [ctypes.c_int, f32p, f32p, ctypes.POINTER(ctypes.c_int)]
+    L.oracle_norm_preset.restype = ctypes.c_int
+    L.oracle_fused_norm.argtypes = [u8p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int]
+    L.oracle_fused_norm.restype = ctypes.c_int
+    L.oracle_fused_norm_crop.argtypes = [u8p, ctypes.c_size_t, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                         i32p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, f32p, f32p, i32p, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int]
+    L.oracle_fused_norm_crop.restype = ctypes.c_int
+    L.oracle_exp_f32_array.argtypes = [f32p, f32p, ctypes.c_size_t]
+    L.oracle_philox4x32_10.argtypes = [u32p, u32p, u32p]
+    L.oracle_uniform01.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+    L.oracle_uniform01.restype = ctypes.c_float
+    L.oracle_sample_aug_params.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                           ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_float, ctypes.c_float, i32p, u64p]
+    L.oracle_sample_aug_params.restype = ctypes.c_int
+    L.oracle_sample_aug_params_blocked.argtypes = L.oracle_sample_aug_params.argtypes
+    L.oracle_sample_aug_params_blocked.restype = ctypes.c_int
+    return L
 
 
 def _ptr(a, ctype):

@@ -13,17 +13,22 @@ SRC = os.path.join(HERE, "fused_norm_oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
 
+def compile_oracle(src: str, out: str) -> str:
+    """Compile the C file `src` with the oracle's flags into the shared library `out`."""
+    cc = os.environ.get("CC", "gcc")
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build_oracle(force: bool = False) -> str:
     """Compile oracle/fused_norm_oracle.c into oracle/liboracle.so; return its path."""
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
-    cc = os.environ.get("CC", "gcc")
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [cc, "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-           "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    return compile_oracle(SRC, LIB)
 
 
 if __name__ == "__main__":

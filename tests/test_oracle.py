@@ -372,6 +372,17 @@ def test_sampler_moments_at_224():
     assert 0.08 < frac < 0.095
 
 
+@pytest.mark.parametrize("blocked", [False, True])
+def test_sampler_rates_follow_p(blocked):
+    """Flip iff u < flip_p (§五) and erase iff u < p (§十二): away from 1/2 the
+    rates tell a reversed comparison from the right one."""
+    N = 20000
+    sample = oracle.sample_aug_params_blocked if blocked else oracle.sample_aug_params
+    a, _ = sample(31, 0, N, 224, 224, flip_p=0.2, erase_p=0.3)
+    for rate, p in ((a[:, 0].mean(), 0.2), ((a[:, 3] > 0).mean(), 0.3)):
+        assert abs(rate - p) < 4 * np.sqrt(p * (1 - p) / N), (rate, p)
+
+
 # ------------------------------------------------------------- crop -------
 
 def _strided(src, row_pad, image_pad):

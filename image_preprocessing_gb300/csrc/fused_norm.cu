@@ -997,17 +997,20 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         bool ok = true;
         bool waited = !overlapped;   // the previous grid has completed
         if (recdep) {
-            int first[kMaxStages];
+            // the first S units are blockIdx.x + t * G (no array: it would
+            // live in local memory)
             for (; j < S; ++j) {
                 const int uu = (int)blockIdx.x + j * G;
                 if (uu >= p.num_units) break;
-                first[j] = uu;
                 issue_unit_uncut<C>(p, uu, j, smem);
             }
             grid_dependency_wait();
             waited = true;
             if (!(p.hints & 8)) grid_launch_dependents();
-            for (int t = 0; t < j; ++t) publish_unit(p, first[t], t, smem, unit_record(first[t]));
+            for (int t = 0; t < j; ++t) {
+                const int uu = (int)blockIdx.x + t * G;
+                publish_unit(p, uu, t, smem, unit_record(uu));
+            }
             u = next_unit(j);
             if (u < p.num_units) a = unit_record(u);
         }

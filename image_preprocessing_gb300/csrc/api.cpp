@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "stream_guard.h"
 
 namespace trfn {
 
@@ -66,32 +67,10 @@ struct Sampling {
     tr_aug_param* out = nullptr;   // device, N records
 };
 
-// The workspace of the last launch this library made on each stream (a fixed
-// table, oldest entry replaced; nothing is allocated): a launch asking to
-// overlap the kernel before it must not share that kernel's workspace, whose
-// ticket counters are still in use and are zeroed by its last CTA.  Returns
-// true when the launch must not overlap on that account.  Once an entry has
-// been replaced, a stream missing from the table may be one whose entry was
-// dropped, so its launch is treated as sharing.
+// The workspace of the last launch on each of 256 streams (stream_guard.h).
 bool note_stream_workspace(void* stream, void* workspace) {
-    struct Entry { void* stream; void* ws; bool used; };
-    constexpr int kEntries = 256;
-    static std::mutex mu;
-    static Entry table[kEntries];
-    static int next = 0;
-    static bool replaced = false;
-    std::lock_guard<std::mutex> lock(mu);
-    for (Entry& e : table) {
-        if (e.used && e.stream == stream) {
-            const bool same = (workspace != nullptr && e.ws == workspace);
-            e.ws = workspace;
-            return same;
-        }
-    }
-    if (table[next].used) replaced = true;
-    table[next] = Entry{stream, workspace, true};
-    next = (next + 1) % kEntries;
-    return replaced && workspace != nullptr;
+    static StreamWorkspaceGuard<256> guard;
+    return guard.note(stream, workspace);
 }
 
 int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, const float* mean,

@@ -67,10 +67,15 @@ MUTANTS = {
     "subnormal shift off by one": [("unsigned s = (unsigned)(-(E + 1));", "unsigned s = (unsigned)(-E);")],
     "overflow one binade late": [("if (he >= 31)", "if (he > 31)")],
     "sign dropped": [("uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);", "uint16_t sign = 0;")],
+    "NaN made infinity": [("return (uint16_t)(sign | 0x7C00u | 0x0200u | (frac >> 13));",
+                           "return (uint16_t)(sign | 0x7C00u);")],
+    # presets (§九)
+    "a preset constant": [("stdv[1] = 0.224f", "stdv[1] = 0.225f")],
     # Philox4x32-10
     "key bump dropped": [("key[1] += 0xBB67AE85u;", "key[1] += 0u;")],
     "round output words swapped": [("out[0] = hi1 ^ ctr[1] ^ key[0];", "out[0] = hi0 ^ ctr[1] ^ key[0];")],
     "nine rounds": [("for (int r = 0; r < 10; ++r)", "for (int r = 0; r < 9; ++r)")],
+    "uniform on 23 bits": [("return out[0] >> 8;", "return out[0] >> 9;")],
     # sampler (§十, §十二)
     "randint exclusive": [("(int64_t)hi - (int64_t)lo + 1", "(int64_t)hi - (int64_t)lo")],
     "flip comparison reversed": [("(rng_uniform(&g, 0.0f, 1.0f) < flip_p)", "(rng_uniform(&g, 0.0f, 1.0f) >= flip_p)")],
@@ -82,6 +87,7 @@ MUTANTS = {
     "blocked: block of 23 draws": [("const uint64_t base = offset + (uint64_t)n * ORACLE_DRAWS_PER_IMAGE;",
                                     "const uint64_t base = offset + (uint64_t)n * 23u;")],
     "exp: a Taylor term dropped": [("p = fmaf(p, r, 1.0f / 24.0f);", "p = fmaf(p, r, 0.0f);")],
+    "exp: 2^k one binade low": [("(uint32_t)((int)k + 127) << 23", "(uint32_t)((int)k + 126) << 23")],
     # crop (a window of a strided source, then the step)
     "crop ignores the flip": [("(size_t)(cx + xs) * C + c", "(size_t)(cx + x) * C + c")],
     "crop rows mirrored": [("(size_t)(cy + y) * row_stride", "(size_t)(cy + H - 1 - y) * row_stride")],
@@ -101,9 +107,12 @@ def _f16_sampled():
             ref = f.astype(np.float16).view(np.uint16)
         nan = np.isnan(f)
         assert np.array_equal(got[~nan], ref[~nan]), hex(int(first))
+        gn = got[nan]
+        assert np.all((gn & 0x7C00) == 0x7C00) and np.all((gn & 0x3FF) != 0)   # NaN stays NaN
 
 
 def _battery():
+    yield "presets", pins.test_presets_match_the_article_table
     yield "f16 rounding cases", pins.test_f16_rounding_cases
     yield "f16 per exponent (sampled)", _f16_sampled
     yield "closed form golden", pins.test_closed_form_imagenet_golden

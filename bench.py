@@ -46,6 +46,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "images/sec and achieved HBM GB/s (fraction of peak) at 256×224×224×3"
 FALLBACK_HBM_GBS = 6800.0
+SPACER_CYCLES = 2_000_000   # about 1 ms at GB300's 2.07 GHz SM clock
 
 
 def parse():
@@ -79,6 +80,9 @@ def parse():
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the 64-batch pinned-host stream (reported under 'pipeline')")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other batch workloads (16x32x32x3, 200x28x28x1, 256x224x224x3 -> f32 NHWC/NCHW) "
+                         "reported under 'per_config'")
     ap.add_argument("--no-clocks", action="store_true")
     return ap.parse_args()
 
@@ -399,7 +403,23 @@ def run_ours(args, rank, local, world, pg):
                 for k in range(rem):
                     launch(k % nsets, k, part=True)
 
+    def spacer():
+        # the GPU spins (bounded, about a millisecond) while the host queues
+        # the timed region behind it, so the region does not include the
+        # host's time to submit its first graph
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(SPACER_CYCLES)
+
     run_steps(Wm)
+    # every graph object the timed region replays runs once before it: the
+    # first replay of a graph uploads it, a one-time cost that would
+    # otherwise fall into the region (about 64 us per 20 launches)
+    with torch.cuda.stream(stream):
+        if K >= G:
+            g_full.replay()
+        if g_tail is not None:
+            g_tail.replay()
+    warm_graph_replays = int(K >= G) + int(g_tail is not None)
     torch.cuda.synchronize()
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     clocks.start()
@@ -410,26 +430,43 @@ def run_ours(args, rank, local, world, pg):
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    # five trials inside the timed region: events between graph replays
+    # five trials: events between graph replays inside the timed region when
+    # it holds at least five replays, else four repeats of the timed region
+    # after it (same graphs, same launches)
     replays = K // G
     trial_at = [replays * t // 5 for t in range(1, 5)] if replays >= 5 else []
     trial_ev = [torch.cuda.Event(enable_timing=True) for _ in trial_at]
+    spacer()
     ev0.record(stream)
     run_steps(K, g_tail, marks=list(zip(trial_at, trial_ev)))
     ev1.record(stream)
     ev1.synchronize()
     torch.cuda.synchronize()
     barrier(pg)
-    clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
-    ms_max = max_over_ranks(pg, ms, dev)
     trials = None
     if trial_ev:
         bounds = [ev0] + trial_ev + [ev1]
         steps_in = [(b - a) * G for a, b in zip([0] + trial_at, trial_at + [replays])]
         steps_in[-1] += K % G
         per = [bounds[t].elapsed_time(bounds[t + 1]) / steps_in[t] for t in range(len(steps_in))]
-        trials = {"count": len(per), "ms_per_step": per, "median_ms_per_step": float(np.median(per))}
+        trials = {"count": len(per), "ms_per_step": per, "median_ms_per_step": float(np.median(per)),
+                  "how": "five parts of the timed region"}
+    else:
+        per = [ms / K]
+        for _ in range(4):
+            e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            spacer()
+            e_a.record(stream)
+            run_steps(K, g_tail)
+            e_b.record(stream)
+            e_b.synchronize()
+            per.append(e_a.elapsed_time(e_b) / K)
+        trials = {"count": len(per), "ms_per_step": per, "median_ms_per_step": float(np.median(per)),
+                  "how": "the timed region, then four repeats of it (same graphs and launches)"}
+    trials["spread"] = float(max(per) / min(per) - 1.0)
+    clk = clocks.stop()
+    ms_max = max_over_ranks(pg, ms, dev)
     per_launch_s = (ms / 1000.0) / K
     # average algorithmic bytes per launch over the rotation actually timed
     seq = [k % nsets for k in range(K)]
@@ -467,9 +504,13 @@ def run_ours(args, rank, local, world, pg):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg)
+    headline = args.config == 3 and not S and not args.batch and not args.layout and not args.size
     pipeline = None
-    if not args.no_pipeline and args.config == 3 and not S and not args.batch and not args.layout and not args.size:
+    if not args.no_pipeline and headline:
         pipeline = run_pipeline(dev, rank, pg)
+    per_config = None
+    if not args.no_per_config and headline and world == 1:
+        per_config = run_per_config(dev, measured_peaks()[0], args.cpu_seconds / 4, not args.no_cpu)
 
     value = aggregate_images_per_s(world, N, K, ms_max)
     res = {
@@ -491,8 +532,11 @@ def run_ours(args, rank, local, world, pg):
             "flip_p": 0.5 if cfg["flip"] else 0.0, "erase_p": cfg["erase_p"],
             "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB >= 4x L2 (%.0f MB)" % (
                 nsets, nsets * set_bytes / 1e6, l2 / 1e6),
-            "launch": "CUDA graph of %d launches replayed; variant %d; %s" % (
-                G, args.variant,
+            "launch": "CUDA graph of %d launches replayed (%s); variant %d; %s" % (
+                G, "timed: %d replays + a graph of the %d remaining launches; every timed graph replayed "
+                   "once in warm-up (%d replays beyond the %d warm-up steps)" % (
+                       K // G, K % G, warm_graph_replays, Wm),
+                args.variant,
                 "consecutive launches overlap (tr_fused_norm_ex, TR_LAUNCH_OVERLAP_PREVIOUS: independent batches, "
                 "workspaces differing from one launch to the next)" if overlap["on"]
                 else "each launch waits for the previous one to complete"),
@@ -525,6 +569,8 @@ def run_ours(args, rank, local, world, pg):
         res["e2e"] = e2e
     if pipeline is not None:
         res["pipeline"] = pipeline
+    if per_config is not None:
+        res["per_config"] = per_config
     return res
 
 
@@ -622,10 +668,13 @@ def run_pipeline(dev, rank, pg):
     B, N, H, W, C = cfg["batches"], cfg["N"], cfg["H"], cfg["W"], cfg["C"]
     mean = np.array(cfg["mean"], np.float32)
     std = np.array(cfg["std"], np.float32)
-    # uniform pixels (seed 5000 + b): the copy and the kernel do not depend on
-    # pixel values, and 64 Gaussian batches take minutes to draw on the host
-    h_src = [torch.from_numpy(synth.pixels_uniform(5000 + b + 7919 * rank, N, H, W, C)).pin_memory()
-             for b in range(B)]
+    # clipped-Gaussian pixels (seed 5000 + b), drawn straight into the pinned
+    # buffers by host threads (numpy drops the GIL while it draws)
+    h_src = [torch.empty((N, H, W, C), dtype=torch.uint8).pin_memory() for _ in range(B)]
+    t_draw = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(lambda b: synth.pixels_gaussian_into(5000 + b + 7919 * rank, h_src[b].numpy()), range(B)))
+    t_draw = time.perf_counter() - t_draw
     h_par, offset = [], 0
     for b in range(B):
         recs, offset = trfn.tr_sample_aug_params(2005, offset, N, H, W, flip=True, erase=True,
@@ -691,6 +740,14 @@ def run_pipeline(dev, rank, pg):
     t_pipe = max_over_ranks(pg, e0.elapsed_time(e1) / 1e3, dev)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     h2d = img_bytes + N * 20
+    # the last two batches' outputs are still on the device (batch b wrote
+    # d_out[b & 1]): images first, middle and last of each against the oracle
+    parity = {"batches": [B - 2, B - 1], "images": [0, N // 2, N - 1], "ok": True, "max_f16_ulp": 0}
+    for b in (B - 2, B - 1):
+        one = parity_sample(dict(cfg, layout="nhwc"), [h_src[b]], [d_out[b & 1]], [h_par[b].numpy()], mean, std,
+                            trfn.OUT_F16, trfn.LAYOUT_NHWC, 1)
+        parity["ok"] = parity["ok"] and one["ok"]
+        parity["max_f16_ulp"] = max(parity["max_f16_ulp"], one["max_f16_ulp"])
     return {
         "workload": cfg["name"], "batches": B, "images_per_s": world * B * N / t_pipe,
         "ms_pipelined": t_pipe * 1e3, "h2d_gbs_lone_copy": img_bytes / t_copy / 1e9,
@@ -701,8 +758,114 @@ def run_pipeline(dev, rank, pg):
         "h2d_bytes_per_batch": h2d, "gpu_launches": int(launches),
         "path": "tr_ts_submit: pinned host u8 + records -> device slot A/B (copy stream) -> kernel "
                 "(compute stream); outputs stay on the device",
-        "pixels": "uniform (seed 5000 + b)",
+        "pixels": "rint(Normal(110, 60)) clipped to [0, 255] (seed 5000 + b), drawn in %.1f s on host threads" % t_draw,
+        "parity_sample": parity,
     }
+
+
+def run_config(k, layout_name, dev, peak):
+    """One of the other batch workloads (16x32x32x3 -> f32, 200x28x28x1 ->
+    f32, 256x224x224x3 -> f32 NHWC or NCHW): a CUDA graph of launches
+    rotating over enough buffer sets to exceed L2 four times, timed with the
+    launches overlapping the previous one (independent batches) and with each
+    waiting for the previous one; three trials each, median reported; three
+    images of the last written set against the oracle."""
+    import torch
+    import image_preprocessing_gb300 as trfn
+    from image_preprocessing_gb300 import synth
+    cfg = dict(synth.CONFIGS[k])
+    cfg["layout"] = layout_name
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    dt = trfn.OUT_F16 if cfg["out_dtype"] == "f16" else trfn.OUT_F32
+    layout = {"nhwc": trfn.LAYOUT_NHWC, "nchw": trfn.LAYOUT_NCHW, "nhwc4": trfn.LAYOUT_NHWC4}[layout_name]
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    pixels = synth.config_pixels(k)
+    recs = None
+    if cfg["flip"] or cfg["erase"]:
+        recs, _ = trfn.tr_sample_aug_params(2000 + k, 0, N, H, W, flip=cfg["flip"], erase=cfg["erase"],
+                                            erase_p=cfg["erase_p"])
+    out_shape = trfn.out_shape(N, H, W, C, layout)
+    ob = 2 if dt == trfn.OUT_F16 else 4
+    in_bytes, out_bytes = N * H * W * C, int(np.prod(out_shape)) * ob
+    in_stride, out_stride = -(-in_bytes // 256) * 256, -(-out_bytes // 256) * 256
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, int(np.ceil(4 * l2 / (in_bytes + out_bytes))))
+    G = nsets * max(1, 60 // nsets)
+    G += G % 2
+    # every set holds the same pixels at its own address
+    src_all = torch.empty((nsets, in_stride), dtype=torch.uint8, device=dev)
+    src_all[:, :in_bytes].copy_(torch.from_numpy(pixels).reshape(1, -1).to(dev).expand(nsets, -1))
+    dst_all = torch.empty((nsets, out_stride), dtype=torch.uint8, device=dev)
+    aug = torch.from_numpy(recs).to(dev) if recs is not None else None
+    s0, d0 = src_all.data_ptr(), dst_all.data_ptr()
+    stream = torch.cuda.Stream(device=dev)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev) for _ in range(2)]
+    kernel = trfn.tr_fused_norm_plan(s0, d0, N, H, W, C, dt, layout)
+
+    def launch(j, overlap):
+        trfn.tr_fused_norm(s0 + (j % nsets) * in_stride, d0 + (j % nsets) * out_stride, mean, std, aug,
+                           out_dtype=dt, layout=layout, stream=stream, shape=(N, H, W, C), workspace=wss[j % 2],
+                           overlap_previous=overlap)
+
+    with torch.cuda.stream(stream):
+        for j in range(nsets + nsets % 2):
+            launch(j, False)
+    torch.cuda.synchronize()
+    alg = algorithmic_bytes(cfg, recs)
+    res = {"workload": cfg["name"].replace("_nhwc_nchw", "_" + layout_name), "N": N, "H": H, "W": W, "C": C,
+           "out": cfg["out_dtype"] + " " + layout_name.upper(),
+           "kernel": {trfn.VARIANT_TILED: "tiled", trfn.VARIANT_GENERIC: "per-element"}.get(kernel, str(kernel)),
+           "algorithmic_bytes_per_launch": alg,
+           "l2": "%d rotating buffer sets, %.0f MB >= 4x L2" % (nsets, nsets * (in_bytes + out_bytes) / 1e6)}
+    reps = max(1, -(-240 // G))
+    for mode, overlap in (("overlapping", True), ("waiting", False)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(G):
+                launch(j, overlap)
+        with torch.cuda.stream(stream):
+            g.replay()
+        per = []
+        for _ in range(3):
+            e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(SPACER_CYCLES)
+                e_a.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e_b.record(stream)
+            e_b.synchronize()
+            per.append(e_a.elapsed_time(e_b) / (reps * G))
+        ms = float(np.median(per))
+        gbs = alg / (ms / 1e3) / 1e9
+        res[mode] = {"ms_per_step": ms, "images_per_s": N / (ms / 1e3), "achieved_gbs": gbs, "frac": gbs / peak,
+                     "trials_ms_per_step": per, "launches_timed": reps * G}
+        del g
+    torch.cuda.synchronize()
+    last = (G - 1) % nsets
+    got = dst_all[last, :out_bytes].view(torch.float16 if dt == trfn.OUT_F16 else torch.float32).view(out_shape)
+    res["parity_sample"] = parity_sample(cfg, [torch.from_numpy(pixels)], [got], [recs], mean, std, dt, layout, 1)
+    res["launch"] = "CUDA graph of %d launches, %d replay(s) per trial after one untimed replay" % (G, reps)
+    return res
+
+
+def run_per_config(dev, peak, cpu_seconds, with_cpu):
+    """The other batch workloads beside the headline, keyed by workload name;
+    for the 256x224x224x3 -> f32 validation batch also the oracle on the
+    host's cores (all of them and one)."""
+    from image_preprocessing_gb300 import synth
+    out = {}
+    for k, lay in ((1, "nhwc"), (2, "nhwc"), (4, "nhwc"), (4, "nchw")):
+        r = run_config(k, lay, dev, peak)
+        if with_cpu and k == 4:
+            cfg = dict(synth.CONFIGS[4], layout=lay)
+            v, threads, sample = oracle_images_per_s(cfg, cpu_seconds)
+            v1, _, sample1 = oracle_images_per_s(cfg, max(1.0, cpu_seconds / 2), threads=1)
+            r["cpu_baseline"] = {"value": v, "unit": "images/s", "cores": threads, "kind": "oracle",
+                                 "sample": sample, "single_core": {"value": v1, "sample": sample1}}
+        out[r["workload"]] = r
+    return out
 
 
 # ------------------------------------------------------------- oracle -----
@@ -734,7 +897,7 @@ def oracle_images_per_s(cfg, seconds, threads=None):
     threads = threads or os.cpu_count() or 1
     N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
     m = min(N, max(threads, 8))
-    src = host_batch(dict(cfg, N=N), 1000 + 3)[:m].copy()
+    src = host_batch(dict(cfg, N=m), 1000 + 3)
     recs = None
     if cfg["flip"] or cfg["erase"]:
         recs, _ = oracle.sample_aug_params(2003, 0, m, H, W, flip=cfg["flip"], erase=cfg["erase"],
@@ -815,7 +978,7 @@ def main():
         return
     res = run_ours(args, rank, local, world, pg)
     if rank == 0:
-        if not args.no_cpu:
+        if not args.no_cpu and world == 1:
             cfg = workload(args)
             v, threads, sample = oracle_images_per_s(cfg, args.cpu_seconds)
             v1, _, sample1 = oracle_images_per_s(cfg, max(1.0, args.cpu_seconds / 4), threads=1)

@@ -67,6 +67,33 @@ struct Sampling {
     tr_aug_param* out = nullptr;   // device, N records
 };
 
+}  // namespace
+
+// (x/255 - m)/s == (x - 255 m) * (1/(255 s)).  With A = 255 m rounded to an
+// integer, x - A is an exact small integer and the rest, -(255 m - A)/(255 s),
+// is at most half a scale step: every constant is formed in binary64 (255 m
+// is exact there) and rounded once to binary32.  The kernels' one FMA then
+// adds terms of the value's own size, so the result is within 3 binary32
+// ulps of the exact value whatever the mean (the product's relative error
+// is 2^-24 and |x - A| * scale <= 2 |value| when x != A), where x * scale +
+// (-m/s) would cancel two terms of up to 255 * scale.
+bool fold_constants(const float* mean, const float* stdv, int C, LaunchArgs& a) {
+    for (int c = 0; c < 4; ++c) { a.shift[c] = 0.0f; a.scale[c] = 0.0f; a.bias[c] = 0.0f; }
+    for (int c = 0; c < C; ++c) {
+        const double m = mean[c], s = stdv[c];
+        if (!std::isfinite(m) || !std::isfinite(s) || s == 0.0) return false;
+        const double am = 255.0 * m;
+        const double A = (std::fabs(am) <= 1048576.0) ? std::nearbyint(am) : 0.0;
+        a.shift[c] = (float)A;
+        a.scale[c] = (float)(1.0 / (255.0 * s));
+        a.bias[c] = (float)(-(am - A) / (255.0 * s));
+        if (!std::isfinite(a.scale[c]) || !std::isfinite(a.bias[c])) return false;
+    }
+    return true;
+}
+
+namespace {
+
 // The workspace of the last launch on each of 256 streams (stream_guard.h).
 bool note_stream_workspace(void* stream, void* workspace) {
     static StreamWorkspaceGuard<256> guard;
@@ -88,16 +115,7 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
         return TR_ERR_INVALID_ARGUMENT;
     if (mean == nullptr || stdv == nullptr) return TR_ERR_INVALID_ARGUMENT;
     LaunchArgs a;
-    for (int c = 0; c < 4; ++c) { a.scale[c] = 0.0f; a.bias[c] = 0.0f; }
-    for (int c = 0; c < C; ++c) {
-        const double m = mean[c], s = stdv[c];
-        if (!std::isfinite(m) || !std::isfinite(s) || s == 0.0) return TR_ERR_INVALID_ARGUMENT;
-        // (x/255 - m)/s == x * (1/(255 s)) + (-m/s): both constants formed in
-        // binary64 and rounded once to binary32
-        a.scale[c] = (float)(1.0 / (255.0 * s));
-        a.bias[c] = (float)(-m / s);
-        if (!std::isfinite(a.scale[c]) || !std::isfinite(a.bias[c])) return TR_ERR_INVALID_ARGUMENT;
-    }
+    if (!fold_constants(mean, stdv, C, a)) return TR_ERR_INVALID_ARGUMENT;
     if (N == 0) return TR_OK;
     if (src == nullptr || dst == nullptr) return TR_ERR_INVALID_ARGUMENT;
     const int ob = (out_dtype == TR_OUT_F16) ? 2 : 4;
@@ -296,7 +314,7 @@ int tr_fused_norm_geometry(const uint8_t* src_u8, const void* dst, int N, int H,
     if (C == 1 && out_layout == TR_LAYOUT_NCHW) out_layout = TR_LAYOUT_NHWC;   // as in the launch
     if (!tiled_supported(src_u8, dst, N, H, W, C, out_dtype, out_layout)) return TR_ERR_NOT_SUPPORTED;
     LaunchArgs a;
-    for (int c = 0; c < 4; ++c) { a.scale[c] = 0.0f; a.bias[c] = 0.0f; }
+    for (int c = 0; c < 4; ++c) { a.shift[c] = 0.0f; a.scale[c] = 0.0f; a.bias[c] = 0.0f; }
     a.src = src_u8;
     a.dst = const_cast<void*>(dst);
     a.N = N; a.H = H; a.W = W; a.C = C;

@@ -16,8 +16,8 @@
 //    chunks that lie wholly inside a wide erased span.  The other warps
 //    convert groups of 8 (C=3), 16 (C=1), 8 (C=2) or 4 (C=4) pixels: the
 //    mirrored gather is done by choosing source byte lanes with PRMT, the
-//    byte becomes 2^23 + x by the same PRMT, one exact FADD removes 2^23,
-//    one FFMA applies scale and bias.  Results go to a double-buffered
+//    byte becomes 2^23 + x by the same PRMT, one exact FADD removes 2^23 and
+//    the channel's integer shift, one FFMA applies scale and bias.  Results go to a double-buffered
 //    shared-memory output tile that one TMA bulk store per band (per plane
 //    for NCHW) writes to global memory.  With a crop source
 //    (tr_fused_norm_crop) the bands come from windows of a strided source
@@ -34,7 +34,8 @@
 //    grid has completed (TR_LAUNCH_OVERLAP_PREVIOUS).
 //  * GENERIC: one thread per output pixel, any shape, stride and alignment.
 //
-// Both kernels compute each value as fma(float(x), scale_c, bias_c) with the
+// Both kernels compute each value as fma(x - shift_c, scale_c, bias_c), the
+// subtraction exact (shift_c is 255*mean_c rounded to an integer), with the
 // same binary32 operands, so they agree bit for bit.
 //
 // Every wait in device code is bounded: a TMA stage that does not complete
@@ -223,11 +224,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ------------------------------------------------------------ arithmetic --
 
-// Byte `sel` (0..3) of `word` as a binary32 value: PRMT builds the pattern
-// 0x4B0000xx = 2^23 + x, the subtraction of 2^23 is exact.
-__device__ __forceinline__ float byte_to_float(uint32_t word, uint32_t sel) {
+// Byte `sel` (0..3) of `word` minus the channel's integer shift, as a
+// binary32 value: PRMT builds the pattern 0x4B0000xx = 2^23 + x and `base`
+// is 2^23 + shift (an integer below 2^24), so the subtraction is exact.
+__device__ __forceinline__ float byte_minus_shift(uint32_t word, uint32_t sel, float base) {
     const uint32_t bits = __byte_perm(word, 0x00004B00u, 0x5440u | sel);
-    return __fsub_rn(__uint_as_float(bits), 8388608.0f);
+    return __fsub_rn(__uint_as_float(bits), base);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -247,7 +249,7 @@ struct Group {
 // Converts one group.  Output element k is pixel k/C, channel k%C; with FLIP
 // its source is pixel P-1-k/C of the mirrored group (same channel).
 template <int C, bool FLIP>
-__device__ __forceinline__ void convert_group(const uint32_t (&w)[Group<C>::kWords],
+__device__ __forceinline__ void convert_group(const uint32_t (&w)[Group<C>::kWords], const float* base,
                                               const float* scale, const float* bias,
                                               float (&v)[Group<C>::kBytes]) {
     constexpr int P = Group<C>::P;
@@ -256,7 +258,7 @@ __device__ __forceinline__ void convert_group(const uint32_t (&w)[Group<C>::kWor
         const int i = k / C;
         const int c = k % C;
         const int sb = FLIP ? ((P - 1 - i) * C + c) : k;
-        v[k] = __fmaf_rn(byte_to_float(w[sb >> 2], sb & 3), scale[c], bias[c]);
+        v[k] = __fmaf_rn(byte_minus_shift(w[sb >> 2], sb & 3, base[c]), scale[c], bias[c]);
     }
 }
 
@@ -290,6 +292,7 @@ struct TiledParams {
                            // stores (7), erased-span rule (11, 12-15); set by the launch:
                            // overlap the previous grid (8), records written by it (9),
                            // odd-row element stores (10)
+    float base[4];         // 2^23 + shift_c (see byte_minus_shift)
     float scale[4];
     float bias[4];
 };
@@ -820,8 +823,8 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
                     w[2 * q + 1] = t.y;
                 }
             }
-            if (rec.flags & 1) convert_group<C, true>(w, p.scale, p.bias, v);
-            else convert_group<C, false>(w, p.scale, p.bias, v);
+            if (rec.flags & 1) convert_group<C, true>(w, p.base, p.scale, p.bias, v);
+            else convert_group<C, false>(w, p.base, p.scale, p.bias, v);
             if (lo < hi) {
 #pragma unroll
                 for (int k = 0; k < GB; ++k) {
@@ -1139,6 +1142,7 @@ struct GenericParams {
     int N, H, W;
     int src_H, src_W;      // source image size (H, W for compact sources)
     DivU32 div_w, div_h;   // x / W and x / H for 32-bit pixel indices
+    float shift[4];        // integer-valued: x - shift_c is exact
     float scale[4];
     float bias[4];
     int overlap;           // the launch shares no buffer with the previous grid in the stream
@@ -1196,7 +1200,8 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
 #pragma unroll
         for (int c = 0; c < OC; ++c) {
             v[c] = 0.0f;
-            if (c < C && !erased) v[c] = __fmaf_rn((float)__ldg(sp + c), p.scale[c], p.bias[c]);
+            if (c < C && !erased)
+                v[c] = __fmaf_rn(__fsub_rn((float)__ldg(sp + c), p.shift[c]), p.scale[c], p.bias[c]);
         }
         const size_t pix = ((size_t)n * p.H + y) * p.W + x;
         if (LAYOUT == TR_LAYOUT_NCHW) {
@@ -1775,7 +1780,11 @@ int launch_tiled(const LaunchArgs& a) {
     if (a.overlap_prev && !(a.records_from_prev && (crop || odd))) p.hints |= 256;
     if (a.overlap_prev && a.records_from_prev && !crop && !odd) p.hints |= 512;
     p.ws = static_cast<unsigned int*>(a.workspace);
-    for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
+    for (int c = 0; c < 4; ++c) {
+        p.base[c] = 8388608.0f + a.shift[c];   // exact: |shift| <= 2^20
+        p.scale[c] = a.scale[c];
+        p.bias[c] = a.bias[c];
+    }
 
     // The odd-row form's register realignment of group outputs lengthens a
     // band's conversion: it pays when a CTA streams many bands (6 to 13 for
@@ -1813,7 +1822,7 @@ int launch_generic(const LaunchArgs& a) {
     p.src_W = a.crop_src ? a.src_W : a.W;
     p.row_stride = a.crop_src ? (long long)a.src_row_stride : (long long)a.W * a.C;
     p.image_stride = a.crop_src ? (long long)a.src_image_stride : (long long)a.H * a.W * a.C;
-    for (int c = 0; c < 4; ++c) { p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
+    for (int c = 0; c < 4; ++c) { p.shift[c] = a.shift[c]; p.scale[c] = a.scale[c]; p.bias[c] = a.bias[c]; }
     const int threads = 256;
     p.div_w = make_div((uint32_t)a.W);
     p.div_h = make_div((uint32_t)a.H);

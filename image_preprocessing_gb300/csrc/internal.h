@@ -24,8 +24,15 @@ struct LaunchArgs {
     const uint8_t* src;
     void* dst;
     int N, H, W, C;
+    // value = (x - 255*mean_c) / (255*std_c), evaluated as
+    // fma(x - shift_c, scale_c, bias_c): shift_c is 255*mean_c rounded to an
+    // integer (0 when that is beyond 2^20), so x - shift_c is exact, and
+    // bias_c carries only the remainder; the map's terms then stay near the
+    // value itself instead of cancelling (255*mean_c = 123.68 would otherwise
+    // leave binary32 rounding errors of ulp(124) on values near 0)
+    float shift[4];   // integer-valued
     float scale[4];   // 1/(255*std_c), formed in binary64, rounded to binary32
-    float bias[4];    // -mean_c/std_c, formed in binary64, rounded to binary32
+    float bias[4];    // -(255*mean_c - shift_c)*scale_c, formed in binary64, rounded once
     const tr_aug_param* aug;
     int out_dtype;
     int out_layout;
@@ -47,6 +54,10 @@ struct LaunchArgs {
 };
 
 constexpr size_t kWorkspaceBytes = 2048;
+
+// Fills a.shift/scale/bias for channels 0..C-1 (zeros above C); false when
+// a constant is not finite or std_c is 0.
+bool fold_constants(const float* mean, const float* stdv, int C, LaunchArgs& a);
 
 // Whether the tiled kernel's aligned form applies (16-byte aligned pointers,
 // rows and NCHW output rows a multiple of 16 bytes); otherwise a supported

@@ -36,7 +36,9 @@ constexpr int kMaxDevices = 64;
 
 // Device address of g_noalloc_scratch on `dev` (made current by the caller).
 // In host code the array's name is only a host-side stand-in, so the address
-// is looked up once per device with cudaGetSymbolAddress and cached.
+// is looked up once per device with cudaGetSymbolAddress and cached.  The
+// cache is never refreshed: a device reset (cudaDeviceReset) or a teardown of
+// the primary context while the process keeps running is not supported.
 int scratch_address(int dev, void** out) {
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
@@ -92,6 +94,14 @@ extern "C" int tr_fused_norm_noalloc(const uint8_t* src_u8, void* dst, int N, in
     void* scratch = nullptr;
     rc = scratch_address(dev, &scratch);
     if (rc != TR_OK) return rc;
+    // only the tiled kernel reads the counters; the per-element kernel (small
+    // batches, unaligned buffers) ignores them, so it needs no clearing
+    int variant = TR_VARIANT_TILED;
+    rc = tr_fused_norm_plan(src_u8, dst, N, H, W, C, out_dtype, out_layout, &variant);
+    if (rc != TR_OK) return rc;
+    if (variant != TR_VARIANT_TILED)
+        return tr_fused_norm_ws(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
+                                stream, TR_VARIANT_GENERIC, nullptr);
     // the counters must start at zero: clear them in stream order
     e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -99,5 +109,5 @@ extern "C" int tr_fused_norm_noalloc(const uint8_t* src_u8, void* dst, int N, in
         return TR_ERR_CUDA;
     }
     return tr_fused_norm_ws(src_u8, dst, N, H, W, C, mean, std, aug_params, out_dtype, out_layout,
-                            stream, TR_VARIANT_AUTO, scratch);
+                            stream, TR_VARIANT_TILED, scratch);
 }

@@ -34,6 +34,19 @@ def pixels_gaussian(seed, N, H, W, C, mean=110.0, sd=60.0):
     return np.clip(np.rint(g.normal(mean, sd, size=(N, H, W, C))), 0, 255).astype(np.uint8)
 
 
+def pixels_gaussian_into(seed, out, mean=110.0, sd=60.0):
+    """The bytes of pixels_gaussian(seed, *out.shape) written into the uint8
+    array `out` (for instance a pinned host buffer), with one float64
+    temporary instead of three.  numpy releases the GIL while it draws and
+    converts, so several threads can fill several batches at once."""
+    g = np.random.default_rng(seed)
+    v = g.normal(mean, sd, size=out.shape)
+    np.rint(v, out=v)
+    np.clip(v, 0, 255, out=v)
+    out[...] = v.astype(np.uint8)
+    return out
+
+
 def coordinate_image(N, H, W, C):
     """Channel 0 holds x mod 256, channel 1 y mod 256, channel 2 n mod 256,
     channel 3 (x + 2y) mod 256: any misplaced or mirrored element changes value."""

@@ -112,9 +112,12 @@ typedef enum tr_variant {
  *               fixed by the shape, type and layout.  Must not overlap src.
  *   N,H,W,C     N >= 0 (0 = nothing to do), H >= 1, W >= 1, 1 <= C <= 4.
  *   mean, std   host arrays of C floats, read during the call.  std[c] must be
- *               finite and non-zero, mean[c] finite.  The kernels use
- *               scale = 1/(255*std) and bias = -mean/std, each formed in
- *               binary64 and rounded to binary32, in one fused multiply-add.
+ *               finite and non-zero, mean[c] finite.  The kernels compute
+ *               (x - A)*scale + bias in one fused multiply-add, with A =
+ *               255*mean rounded to an integer (so x - A is exact), scale =
+ *               1/(255*std) and bias = -(255*mean - A)*scale, each formed in
+ *               binary64 and rounded to binary32: within 3 binary32 ulps of
+ *               the exact value for any mean and std.
  *   aug_params  device array of N tr_aug_param (4-byte aligned), read in
  *               stream order; NULL means no flip and no erase for every image.
  *   out_dtype   tr_out_dtype; out_layout tr_layout.
@@ -234,9 +237,14 @@ size_t tr_workspace_bytes(void);
  * loads the library holds until the process exits), and it allocates nothing.
  *   - The first call on a device looks up that array's device address
  *     (cudaGetSymbolAddress, with the device current) and caches it; make that
- *     first call before any stream capture.
- *   - Each call clears the scratch on `stream` (an asynchronous memset) before
- *     its kernel, and the kernel leaves it zero again.  All calls on a device
+ *     first call before any stream capture.  The cached address outlives a
+ *     device reset, so resetting a device (cudaDeviceReset) or tearing down
+ *     its primary context in a process that keeps calling this is not
+ *     supported.
+ *   - Each call that takes the tiled kernel (tr_fused_norm_plan) clears the
+ *     scratch on `stream` (an asynchronous memset) before its kernel, and the
+ *     kernel leaves it zero again; a call that takes the per-element kernel
+ *     (small batches, unaligned buffers) uses no scratch and clears nothing.  All calls on a device
  *     share the one array: calls that overlap on the GPU (other streams or
  *     threads) race on it and must be ordered by the caller.
  *   - Scratch needs above the 2048-byte capacity are rejected with

@@ -243,3 +243,48 @@ def test_staged_batches_match_the_oracle(mode):
         ref = oracle.fused_norm(data[items], MEAN, STD, recs[items], out_dtype=trfn.OUT_F16)
         got = d.cpu().view(__import__("torch").int16).numpy().view(np.uint16)
         assert_parity(got, ref, trfn.OUT_F16, "staged batch %d" % b)
+
+
+def test_full_size_stream_with_a_short_last_batch_matches_the_oracle():
+    """The stream workload at full size (TransferStation §四, §四.1): four
+    256 x 224x224x3 batches of clipped-Gaussian pixels with flip and erase
+    records (Philox offsets running on across batches) go through
+    tr_ts_submit, then a short batch of 100 images through
+    tr_ts_submit_partial, which pads it with the first batch's first image and
+    record.  Every element of every batch, on the device and copied back to
+    pinned host memory, against the oracle."""
+    import concurrent.futures as cf
+    import torch
+    N, H, W, C = 256, 224, 224, 3
+    B, short = 4, 100
+    ts, _ = _station(N, H, W, C)
+    h_src = [torch.empty((N if b < B else short, H, W, C), dtype=torch.uint8).pin_memory() for b in range(B + 1)]
+    for b in range(B + 1):
+        synth.pixels_gaussian_into(5000 + b, h_src[b].numpy())
+    recs, offset = [], 0
+    for b in range(B + 1):
+        r, offset = oracle.sample_aug_params(2005, offset, h_src[b].shape[0], H, W)
+        recs.append(r)
+    h_par = [torch.from_numpy(r).pin_memory() for r in recs]
+    d_out = [torch.empty((N, H, W, C), dtype=torch.float16, device="cuda") for _ in range(B + 1)]
+    h_out = [torch.zeros((N, H, W, C), dtype=torch.float16).pin_memory() for _ in range(B + 1)]
+    for b in range(B):
+        assert ts.submit(h_src[b], d_out[b], MEAN, STD, h_params=h_par[b], h_dst=h_out[b]) == b
+    assert ts.submit_partial(h_src[B], N, d_out[B], MEAN, STD, h_params=h_par[B], h_dst=h_out[B]) == B
+    assert ts.sync(60000)
+    ts.close()
+    first_img, first_rec = h_src[0].numpy()[:1], recs[0][:1]
+    srcs = [h_src[b].numpy() for b in range(B)] + [
+        np.concatenate([h_src[B].numpy(), np.repeat(first_img, N - short, axis=0)])]
+    rs = recs[:B] + [np.concatenate([recs[B], np.repeat(first_rec, N - short, axis=0)])]
+
+    def reference(b, lo, hi):
+        return oracle.fused_norm(srcs[b][lo:hi], MEAN, STD, rs[b][lo:hi], out_dtype=trfn.OUT_F16)
+
+    step = 16
+    with cf.ThreadPoolExecutor(max_workers=8) as ex:
+        for b in range(B + 1):
+            ref = np.concatenate(list(ex.map(lambda lo: reference(b, lo, lo + step), range(0, N, step))))
+            assert_parity(_f16(d_out[b]), ref, trfn.OUT_F16, "device output of batch %d" % b)
+            assert_parity(h_out[b].view(torch.int16).numpy().view(np.uint16), ref, trfn.OUT_F16,
+                          "host copy of batch %d" % b)

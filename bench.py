@@ -80,6 +80,9 @@ def parse():
     ap.add_argument("--no-pipeline", action="store_true",
                     help="skip the 64-batch pinned-host stream (reported under 'pipeline')")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-batched", action="store_true",
+                    help="skip the launches of 1, 4 and 8 headline batches each (tr_fused_norm_batches), "
+                         "reported under 'batched_launches'")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the other batch workloads (16x32x32x3, 200x28x28x1, 256x224x224x3 -> f32 NHWC/NCHW) "
                          "reported under 'per_config'")
@@ -511,6 +514,9 @@ def run_ours(args, rank, local, world, pg):
     per_config = None
     if not args.no_per_config and headline and world == 1:
         per_config = run_per_config(dev, measured_peaks()[0], args.cpu_seconds / 4, not args.no_cpu)
+    batched = None
+    if not args.no_batched and headline and world == 1 and not (dev_sampling or fused_sampling):
+        batched = run_batched(dev, measured_peaks()[0])
 
     value = aggregate_images_per_s(world, N, K, ms_max)
     res = {
@@ -571,6 +577,8 @@ def run_ours(args, rank, local, world, pg):
         res["pipeline"] = pipeline
     if per_config is not None:
         res["per_config"] = per_config
+    if batched is not None:
+        res["batched_launches"] = batched
     return res
 
 
@@ -848,6 +856,86 @@ def run_config(k, layout_name, dev, peak):
     res["parity_sample"] = parity_sample(cfg, [torch.from_numpy(pixels)], [got], [recs], mean, std, dt, layout, 1)
     res["launch"] = "CUDA graph of %d launches, %d replay(s) per trial after one untimed replay" % (G, reps)
     return res
+
+
+def run_batched(dev, peak, Ks=(1, 4, 8)):
+    """The headline workload (256 x 224x224x3 -> f16 NHWC, flip + erase) as
+    launches of K batches each (tr_fused_norm_batches): 2*max(K) distinct
+    buffer sets, each launch taking the next K; per-batch time and roofline
+    fraction with each launch waiting for the previous one and with launches
+    overlapping; three trials each (median); the first batch of the last
+    launch against the oracle."""
+    import torch
+    import image_preprocessing_gb300 as trfn
+    from image_preprocessing_gb300 import synth
+    cfg = dict(synth.CONFIGS[3], layout="nhwc")
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    nsets = 2 * max(Ks)
+    px = synth.config_pixels(3)
+    src0 = torch.from_numpy(px).to(dev)
+    srcs = [src0.clone() for _ in range(nsets)]
+    dsts = [torch.empty((N, H, W, C), dtype=torch.float16, device=dev) for _ in range(nsets)]
+    recs, augs, offset = [], [], 0
+    for j in range(nsets):
+        r, offset = trfn.tr_sample_aug_params(2003, offset, N, H, W, erase_p=cfg["erase_p"])
+        recs.append(r)
+        augs.append(torch.from_numpy(r).to(dev))
+    alg = [algorithmic_bytes(cfg, r) for r in recs]
+    stream = torch.cuda.Stream(device=dev)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev) for _ in range(2)]
+    out = {}
+    last = None
+    for K in Ks:
+        per_cycle = nsets // K   # launches per pass over the sets
+        L = per_cycle * max(1, 32 // (per_cycle * K))   # about 32 batches per graph
+
+        def launch(i, overlap):
+            sel = [(i * K + t) % nsets for t in range(K)]
+            trfn.tr_fused_norm_batches([(srcs[j], dsts[j], augs[j]) for j in sel], mean, std,
+                                       out_dtype=trfn.OUT_F16, layout=trfn.LAYOUT_NHWC, stream=stream,
+                                       workspace=wss[i % 2], overlap_previous=overlap)
+            return sel
+
+        res = {}
+        for mode, overlap in (("waiting", False), ("overlapping", True)):
+            with torch.cuda.stream(stream):
+                for i in range(L):
+                    last = launch(i, overlap)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(L):
+                    launch(i, overlap)
+            with torch.cuda.stream(stream):
+                g.replay()
+            per = []
+            reps = 4
+            for _ in range(3):
+                e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    torch.cuda._sleep(SPACER_CYCLES)
+                    e_a.record(stream)
+                    for _ in range(reps):
+                        g.replay()
+                    e_b.record(stream)
+                e_b.synchronize()
+                per.append(e_a.elapsed_time(e_b) / (reps * L * K))
+            ms = float(np.median(per))
+            avg = float(np.mean([alg[(i * K + t) % nsets] for i in range(L) for t in range(K)]))
+            gbs = avg / (ms / 1e3) / 1e9
+            res[mode] = {"us_per_batch": ms * 1e3, "images_per_s": N / (ms / 1e3), "achieved_gbs": gbs,
+                         "frac": gbs / peak, "trials_us_per_batch": [v * 1e3 for v in per]}
+            del g
+        res["launches_per_graph"] = L
+        out["K=%d" % K] = res
+    torch.cuda.synchronize()
+    j = last[0]
+    parity = parity_sample(cfg, [srcs[j]], [dsts[j]], [recs[j]], mean, std, trfn.OUT_F16, trfn.LAYOUT_NHWC, 1)
+    out["parity_sample"] = parity
+    out["path"] = ("tr_fused_norm_batches: K batches of 256x224x224x3 -> f16 NHWC (flip + erase) per launch, "
+                   "dynamic schedule, %d rotating buffer sets" % nsets)
+    return out
 
 
 def run_per_config(dev, peak, cpu_seconds, with_cpu):

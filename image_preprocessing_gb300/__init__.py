@@ -9,7 +9,7 @@ its thin binding plus the seeded synthetic-input generators (synth).
 from .api import (LAUNCH_OVERLAP_PREVIOUS, LAYOUT_NCHW, LAYOUT_NHWC, LAYOUT_NHWC4, OUT_F16, OUT_F32, PRESETS, STAGE_FAST,
                   STAGE_REPRODUCIBLE, VARIANT_AUTO, Staging, tr_stage_zone_bytes,
                   VARIANT_GENERIC, VARIANT_TILED, TransferStation, out_shape, tr_device_status,
-                  tr_fused_norm, tr_fused_norm_crop, tr_fused_norm_geometry, tr_fused_norm_plan, tr_fused_norm_sampled, tr_launch_count, tr_norm_preset, tr_sample_aug_params,
+                  tr_fused_norm, tr_fused_norm_batches, tr_fused_norm_crop, tr_fused_norm_geometry, tr_fused_norm_plan, tr_fused_norm_sampled, tr_launch_count, tr_norm_preset, tr_sample_aug_params,
                   tr_sample_aug_params_device,
                   tr_ts_slot_bytes, tr_tune_tiled, tr_validate_aug_params, tr_workspace_bytes)
 from ._native import LIB_PATH, TrError
@@ -17,6 +17,7 @@ from ._native import LIB_PATH, TrError
 __all__ = [
     "LAUNCH_OVERLAP_PREVIOUS", "LAYOUT_NCHW", "LAYOUT_NHWC", "LAYOUT_NHWC4", "OUT_F16", "OUT_F32", "PRESETS", "VARIANT_AUTO",
     "VARIANT_GENERIC", "VARIANT_TILED", "TransferStation", "out_shape", "tr_device_status", "tr_fused_norm",
+    "tr_fused_norm_batches",
     "tr_fused_norm_crop", "tr_fused_norm_geometry", "tr_sample_aug_params_device", "tr_fused_norm_sampled",
     "tr_fused_norm_plan", "tr_launch_count", "tr_norm_preset", "tr_sample_aug_params", "tr_ts_slot_bytes",
     "tr_tune_tiled", "tr_workspace_bytes",

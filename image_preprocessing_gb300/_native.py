@@ -10,6 +10,7 @@ import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtrfn.so")
+LIB_BOUNDS_PATH = os.path.join(_HERE, "libtrfn_bounds.so")
 
 TR_OK = 0
 STATUS_NAMES = {0: "TR_OK", 1: "TR_ERR_INVALID_ARGUMENT", 2: "TR_ERR_NOT_SUPPORTED", 3: "TR_ERR_CUDA",
@@ -43,6 +44,11 @@ class StageBatch(ctypes.Structure):
                 ("count", ctypes.c_int), ("zone", ctypes.c_int)]
 
 
+class Batch(ctypes.Structure):
+    """tr_batch: one batch of a tr_fused_norm_batches call."""
+    _fields_ = [("src_u8", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("aug_params", ctypes.c_void_p)]
+
+
 class AugSampling(ctypes.Structure):
     _fields_ = [("flip_enabled", ctypes.c_int), ("flip_p", ctypes.c_float), ("erase_enabled", ctypes.c_int),
                 ("erase_p", ctypes.c_float), ("scale_lo", ctypes.c_float), ("scale_hi", ctypes.c_float),
@@ -63,6 +69,8 @@ _SIGNATURES = {
     "tr_fused_norm_ws": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _vp, _i, _i, _vp, _i, _vp, ctypes.c_uint]),
     "tr_workspace_bytes": (ctypes.c_size_t, []),
+    "tr_fused_norm_batches": (_i, [ctypes.POINTER(Batch), _i, _i, _i, _i, _i, _fp, _fp, _i, _i, _vp, _vp,
+                                   ctypes.c_uint]),
     "tr_fused_norm_sampled": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _u64, _u64, ctypes.POINTER(AugSampling), _vp,
                                    ctypes.POINTER(_u64), _i, _i, _vp, _i, _vp]),
     "tr_fused_norm_sampled_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _fp, _fp, _u64, _u64, ctypes.POINTER(AugSampling), _vp,
@@ -108,21 +116,39 @@ _SIGNATURES = {
 }
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise ImportError(
+            "%s is not built; build it with `python -m image_preprocessing_gb300.build` "
+            "or __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     """The loaded libtrfn.so (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise ImportError(
-                "libtrfn.so is not built (%s); build it with `python -m image_preprocessing_gb300.build` "
-                "or __graft_entry__.build()" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGNATURES.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+_checked = None
+
+
+def checked_lib():
+    """libtrfn_bounds.so: the same C ABI with the tiled kernel's bounds and
+    alignment checks compiled in (tr_device_status bit 1, site number in bits
+    8..15, on a failed check).  A separate library with its own device status
+    word; for tests only."""
+    global _checked
+    if _checked is None:
+        _checked = _load(LIB_BOUNDS_PATH)
+    return _checked
 
 
 def check(status, where):

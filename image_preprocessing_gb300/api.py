@@ -99,6 +99,41 @@ def tr_fused_norm(src, dst, mean, std, aug=None, out_dtype=OUT_F16, layout=LAYOU
     check(rc, "tr_fused_norm")
 
 
+def tr_fused_norm_batches(batches, mean, std, out_dtype=OUT_F16, layout=LAYOUT_NHWC, stream=None, shape=None,
+                          workspace=None, overlap_previous=False):
+    """The fused step on several batches of one shape in one launch.
+
+    batches: list of (src, dst, aug) per batch -- CUDA tensors as for
+    tr_fused_norm (aug may be None), or raw device addresses with
+    shape=(N,H,W,C), the shape of ONE batch.  workspace and overlap_previous
+    as tr_fused_norm."""
+    dt = _code(out_dtype, _DTYPES)
+    lay = _code(layout, _LAYOUTS)
+    if shape is not None:
+        N, H, W, C = shape
+    else:
+        import torch
+        src0 = batches[0][0]
+        if src0.dtype != torch.uint8 or src0.dim() != 4:
+            raise TrError(1, "tr_fused_norm_batches", "sources must be uint8 (N,H,W,C) tensors")
+        N, H, W, C = src0.shape
+        want = torch.float16 if dt == OUT_F16 else torch.float32
+        for src, dst, aug in batches:
+            if tuple(src.shape) != (N, H, W, C) or src.dtype != torch.uint8:
+                raise TrError(1, "tr_fused_norm_batches", "every source must be uint8 of one shape")
+            if dst.dtype != want or dst.numel() != int(np.prod(out_shape(N, H, W, C, lay))):
+                raise TrError(1, "tr_fused_norm_batches", "every dst must be %s of the output shape" % want)
+            if aug is not None and (aug.dtype != torch.int32 or aug.numel() != 5 * N):
+                raise TrError(1, "tr_fused_norm_batches", "aug must be int32 with N*5 elements")
+    arr = (_native.Batch * max(1, len(batches)))()
+    for k, (src, dst, aug) in enumerate(batches):
+        arr[k] = _native.Batch(_dev_ptr(src, "src"), _dev_ptr(dst, "dst"), _dev_ptr(aug, "aug"))
+    check(lib().tr_fused_norm_batches(arr, len(batches), N, H, W, C, float_array(mean), float_array(std), dt, lay,
+                                      _stream_handle(stream), _workspace_ptr(workspace, "tr_fused_norm_batches"),
+                                      LAUNCH_OVERLAP_PREVIOUS if overlap_previous else 0),
+          "tr_fused_norm_batches")
+
+
 def tr_fused_norm_sampled(src, dst, mean, std, seed, offset, records, flip=True, flip_p=0.5, erase=True,
                           erase_p=0.5, scale=(0.02, 0.33), ratio=(0.3, 3.3), out_dtype=OUT_F16, layout=LAYOUT_NHWC,
                           stream=None, variant=VARIANT_AUTO, workspace=None, overlap_previous=False):

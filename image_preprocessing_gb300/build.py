@@ -18,6 +18,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtrfn.so")
+# the same library with the tiled kernel's bounds and alignment checks
+# compiled in (-DTRFN_BOUNDS=1): a failed check sets bit 1 of the device
+# status word and skips the access; for tests, never for measurements
+LIB_BOUNDS = os.path.join(PKG, "libtrfn_bounds.so")
+CHECKED_SOURCE = "fused_norm.cu"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -31,17 +36,19 @@ def _sources():
 
 
 def _stale():
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(LIB_BOUNDS):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(LIB_BOUNDS))
     deps = _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src, checked=False):
+    obj = os.path.join(BUILD, os.path.basename(src) + (".bounds.o" if checked else ".o"))
     cmd = [_nvcc(), "-c", *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
            "-I", INCLUDE, "-I", CSRC, "-o", obj, src]
+    if checked:
+        cmd[2:2] = ["-DTRFN_BOUNDS=1"]
     if src.endswith(".cu"):
         cmd[2:2] = ["-Xptxas", "-v", "--expt-relaxed-constexpr"]
     if os.path.basename(src) == "sampler.cpp":
@@ -59,20 +66,27 @@ def build_library(force=False, verbose=False):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        results = list(ex.map(_compile, srcs))
+    checked_src = os.path.join(CSRC, CHECKED_SOURCE)
+    jobs = [(s, False) for s in srcs] + [(checked_src, True)]
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
+        results = list(ex.map(lambda j: _compile(*j), jobs))
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
-        for (obj, log), src in zip(results, srcs):
-            f.write("== %s\n%s\n" % (os.path.basename(src), log))
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [_nvcc(), "-shared", *ARCH, "-o", tmp] + [o for o, _ in results] + ["-lpthread", "-ldl", "-lrt"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError("link failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+        for (obj, log), (src, checked) in zip(results, jobs):
+            if not checked:
+                f.write("== %s\n%s\n" % (os.path.basename(src), log))
+    plain = [o for (o, _), (_, checked) in zip(results, jobs) if not checked]
+    bounds = [o for (o, _), (src, checked) in zip(results, jobs)
+              if checked or os.path.basename(src) != CHECKED_SOURCE]
+    for lib, objs in ((LIB, plain), (LIB_BOUNDS, bounds)):
+        tmp = lib + ".tmp%d" % os.getpid()
+        cmd = [_nvcc(), "-shared", *ARCH, "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("link failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
+        os.replace(tmp, lib)
     if verbose:
-        for (obj, log), src in zip(results, srcs):
-            if log.strip():
+        for (obj, log), (src, checked) in zip(results, jobs):
+            if log.strip() and not checked:
                 print("==", os.path.basename(src))
                 print(log)
     return LIB

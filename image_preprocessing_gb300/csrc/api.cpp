@@ -228,6 +228,71 @@ int tr_fused_norm_ex(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
                            stream, variant, workspace, CropSource(), Sampling(), flags);
 }
 
+int tr_fused_norm_batches(const tr_batch* batches, int K, int N, int H, int W, int C, const float* mean,
+                          const float* std, int out_dtype, int out_layout, void* stream, void* workspace,
+                          unsigned flags) {
+    if ((flags & ~(unsigned)TR_LAUNCH_OVERLAP_PREVIOUS) != 0) return TR_ERR_INVALID_ARGUMENT;
+    if (K < 0 || K > TR_MAX_BATCHES || (K > 0 && batches == nullptr)) return TR_ERR_INVALID_ARGUMENT;
+    int rc = check_shape(N, H, W, C, out_dtype, out_layout);
+    if (rc != TR_OK) return rc;
+    LaunchArgs a;
+    if (mean == nullptr || std == nullptr || !fold_constants(mean, std, C, a)) return TR_ERR_INVALID_ARGUMENT;
+    if (K == 0 || N == 0) return TR_OK;
+    if (workspace != nullptr && ((uintptr_t)workspace % 16u) != 0) return TR_ERR_INVALID_ARGUMENT;
+    if (C == 1 && out_layout == TR_LAYOUT_NCHW) out_layout = TR_LAYOUT_NHWC;   // the same bytes
+    const int ob = (out_dtype == TR_OUT_F16) ? 2 : 4;
+    const int out_ch = (out_layout == TR_LAYOUT_NHWC4) ? 4 : C;
+    const unsigned long long in_bytes = (unsigned long long)N * H * W * C;
+    const unsigned long long out_bytes = (unsigned long long)N * H * W * out_ch * ob;
+    auto overlaps = [](uintptr_t a0, unsigned long long an, uintptr_t b0, unsigned long long bn) {
+        return a0 < b0 + bn && b0 < a0 + an;
+    };
+    bool one_launch = K > 1 && (long long)K * N * H <= (1LL << 31) - 1 &&
+                      (long long)K * N * H * W * 4 <= kMaxElements && !small_batch(K * N, H, W, C, out_layout);
+    for (int k = 0; k < K; ++k) {
+        const tr_batch& b = batches[k];
+        if (b.src_u8 == nullptr || b.dst == nullptr) return TR_ERR_INVALID_ARGUMENT;
+        if (((uintptr_t)b.dst % (uintptr_t)ob) != 0) return TR_ERR_INVALID_ARGUMENT;
+        if (b.aug_params != nullptr && ((uintptr_t)b.aug_params % 4u) != 0) return TR_ERR_INVALID_ARGUMENT;
+        for (int j = 0; j < K; ++j) {
+            if (overlaps((uintptr_t)b.dst, out_bytes, (uintptr_t)batches[j].src_u8, in_bytes))
+                return TR_ERR_INVALID_ARGUMENT;
+            if (j != k && overlaps((uintptr_t)b.dst, out_bytes, (uintptr_t)batches[j].dst, out_bytes))
+                return TR_ERR_INVALID_ARGUMENT;
+        }
+        one_launch = one_launch && ((uintptr_t)b.src_u8 % 16u) == 0 && ((uintptr_t)b.dst % 16u) == 0 &&
+                     tiled_supported(b.src_u8, b.dst, N, H, W, C, out_dtype, out_layout);
+    }
+    if (one_launch) {
+        a.src = batches[0].src_u8;
+        a.dst = batches[0].dst;
+        a.N = K * N; a.H = H; a.W = W; a.C = C;
+        a.aug = nullptr;
+        a.out_dtype = out_dtype;
+        a.out_layout = out_layout;
+        a.stream = stream;
+        a.workspace = workspace;
+        a.batch_images = N;
+        for (int k = 0; k < K; ++k) {
+            a.bsrc[k] = batches[k].src_u8;
+            a.bdst[k] = batches[k].dst;
+            a.baug[k] = batches[k].aug_params;
+        }
+        const bool same_ws = note_stream_workspace(stream, workspace);
+        a.overlap_prev = (flags & TR_LAUNCH_OVERLAP_PREVIOUS) != 0 && !same_ws;
+        rc = launch(a, TR_VARIANT_TILED);
+        if (rc != TR_ERR_NOT_SUPPORTED) return rc;
+        // the tiled geometry does not fit this device: one launch per batch
+    }
+    for (int k = 0; k < K; ++k) {
+        rc = fused_norm_impl(batches[k].src_u8, batches[k].dst, N, H, W, C, mean, std, batches[k].aug_params,
+                             out_dtype, out_layout, stream, TR_VARIANT_AUTO, workspace, CropSource(), Sampling(),
+                             flags);
+        if (rc != TR_OK) return rc;
+    }
+    return TR_OK;
+}
+
 size_t tr_workspace_bytes(void) { return kWorkspaceBytes; }
 
 int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W, int C, const float* mean,

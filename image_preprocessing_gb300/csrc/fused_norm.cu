@@ -58,9 +58,36 @@
 
 namespace trfn {
 
-__device__ unsigned int g_device_status;   // bit 0: a pipeline wait timed out
+// bit 0: a pipeline wait timed out; bit 1 (checked build): a bounds or
+// alignment check failed, and g_bounds_site holds the first failing check's
+// site number (reported in bits 8..15 of tr_device_status)
+__device__ unsigned int g_device_status;
+__device__ unsigned int g_bounds_site;
 
 namespace {
+
+// The checked build (compiled with -DTRFN_BOUNDS=1, libtrfn_bounds.so) tests
+// every shared-memory and global range the tiled kernel copies, loads or
+// stores against the buffer it belongs to (and the 16-byte rules of bulk
+// copies) before the access; a failed check sets bit 1 of the status word,
+// records its site and skips the access.  A skipped copy leaves its stage
+// incomplete, so the bounded waits then end the CTA.  In the default build
+// TRFN_CHECK is the constant true and its condition is not compiled.
+#ifndef TRFN_BOUNDS
+#define TRFN_BOUNDS 0
+#endif
+#if TRFN_BOUNDS
+__device__ __noinline__ void bounds_fail(int site) {
+    atomicCAS(&g_bounds_site, 0u, (unsigned)(site & 255));
+    atomicOr(&g_device_status, 2u);
+}
+#define TRFN_CHECK(cond, site) ((cond) ? true : (bounds_fail(site), false))
+#else
+#define TRFN_CHECK(cond, site) true
+#endif
+
+// Start of the dynamic shared memory (the same bytes as the kernels' smem).
+extern __shared__ __align__(128) uint8_t trfn_dyn_smem[];
 
 constexpr int kMaxStages = 8;
 constexpr int kHeaderBytes = 384;          // mbarriers + per-stage unit records
@@ -295,7 +322,44 @@ struct TiledParams {
     float base[4];         // 2^23 + shift_c (see byte_minus_shift)
     float scale[4];
     float bias[4];
+    // several batches in one launch (tr_fused_norm_batches): images per
+    // batch, and each batch's source, output and records; image n of the
+    // launch is image n % nb of batch n / nb.  0 = one batch (src, dst, aug).
+    int nb;
+    uint32_t smem_bytes;        // dynamic shared memory of a CTA (checked build)
+    uint64_t src_batch_bytes;   // compact sources: bytes of one batch (checked build)
+    uint64_t dst_batch_bytes;   // output bytes of one batch (checked build)
+    const uint8_t* bsrc[TR_MAX_BATCHES];
+    uint8_t* bdst[TR_MAX_BATCHES];
+    const tr_aug_param* baug[TR_MAX_BATCHES];
 };
+
+// Image n of the launch: its batch's source and output base pointers and
+// its index in that batch.
+struct ImageRef {
+    const uint8_t* src;
+    uint8_t* dst;
+    int n;
+};
+
+__device__ __forceinline__ ImageRef image_ref(const TiledParams& p, int n) {
+    if (p.nb == 0) return ImageRef{p.src, p.dst, n};
+    const int k = n / p.nb;
+    return ImageRef{p.bsrc[k], p.bdst[k], n - k * p.nb};
+}
+
+// Image n's record ({0} without records).
+__device__ __forceinline__ tr_aug_param image_record(const TiledParams& p, int n) {
+    tr_aug_param r = {0, 0, 0, 0, 0};
+    if (p.nb == 0) {
+        if (p.aug != nullptr) r = p.aug[n];
+    } else {
+        const int k = n / p.nb;
+        const tr_aug_param* a = p.baug[k];
+        if (a != nullptr) r = a[n - k * p.nb];
+    }
+    return r;
+}
 
 // Per-stage record of the unit held in that stage.
 struct UnitRec {
@@ -362,9 +426,11 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
         const int xb = cx * C;
         rec->flags = flip | ((xb & ((1 << p.chunk_shift) - 1)) << 8);
         const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
+        const uint32_t box_dst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
         mbar_arrive_expect_tx(bar, (uint32_t)p.R * p.in_pitch);
-        tensor_g2s_4d(smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage, &p.tmap, 0, xb >> p.chunk_shift,
-                      cy + y_begin, b.n, bar, (p.hints & 1) ? policy_evict_last() : policy_evict_first());
+        if (TRFN_CHECK((uint64_t)p.R * p.in_pitch <= p.in_stage && (box_dst & 15u) == 0, 1))
+            tensor_g2s_4d(box_dst, &p.tmap, 0, xb >> p.chunk_shift, cy + y_begin, b.n, bar,
+                          (p.hints & 1) ? policy_evict_last() : policy_evict_first());
         return;
     }
 
@@ -373,25 +439,32 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
         // the 16-byte boundary below them, by one bulk copy; the band then
         // starts `off` bytes into the stage (consumers realign), and any
         // bytes past the source's last whole 16 are copied by this thread.
+        // (offsets from the image's batch, whose source starts 16-byte aligned)
+        const ImageRef im = image_ref(p, b.n);
         const uint64_t L = (uint64_t)p.W * C;
-        const uint64_t base = ((uint64_t)b.n * p.H + y_begin) * L;
+        const uint64_t base = ((uint64_t)im.n * p.H + y_begin) * L;
         const uint64_t end = base + (uint64_t)rows * L;
         const uint64_t a0 = base & ~15ull;
         uint64_t bulk_end = (end + 15) & ~15ull;
         if (bulk_end > p.src_floor16) bulk_end = p.src_floor16 > a0 ? p.src_floor16 : a0;
         rec->flags = flip | (int)((uint32_t)(base - a0) << 8);
         uint8_t* stage = smem + kHeaderBytes + (size_t)s * p.in_stage;
-        for (uint64_t i = bulk_end; i < end; ++i) stage[i - a0] = p.src[i];
+        for (uint64_t i = bulk_end; i < end; ++i)
+            if (TRFN_CHECK(i - a0 < p.in_stage && i < p.src_batch_bytes, 2)) stage[i - a0] = im.src[i];
         const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;   // full[s]
         const uint32_t bulk = (uint32_t)(bulk_end - a0);
         const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;   // bounded-wait test hook
         mbar_arrive_expect_tx(bar, bulk + missing);
-        if (bulk > 0) load_bytes(p, smem_u32(stage), p.src + a0, bulk, bar);
+        if (bulk > 0 && TRFN_CHECK(bulk <= p.in_stage && a0 + bulk <= p.src_batch_bytes && (bulk & 15u) == 0 &&
+                                       ((uintptr_t)(im.src + a0) & 15u) == 0 && (smem_u32(stage) & 15u) == 0,
+                                   3))
+            load_bytes(p, smem_u32(stage), im.src + a0, bulk, bar);
         return;
     }
 
     const uint32_t L = (uint32_t)p.W * C;
-    const uint8_t* g = p.src + ((size_t)b.n * p.H + y_begin) * L;
+    const ImageRef im = image_ref(p, b.n);
+    const uint8_t* g = im.src + ((size_t)im.n * p.H + y_begin) * L;
     const uint32_t sdst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
     const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;   // full[s]
     const uint32_t total = (uint32_t)rows * L;
@@ -410,9 +483,17 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     // 12..15 = v: 0 keeps 256 bytes, else (v - 1) * 128).
     const int v = (p.hints >> 12) & 15;
     const uint32_t skip_min = v == 0 ? 256u : (uint32_t)(v - 1) * 128u;
+    // (checked build) a range [at, at + n) of the band: inside the stage and
+    // the batch's source, 16-byte aligned at both ends
+    auto band_range_ok = [&](uint32_t at, uint32_t n) {
+        return (uint64_t)at + n <= total && total <= p.in_stage &&
+               (uint64_t)(g - im.src) + at + n <= p.src_batch_bytes && ((uintptr_t)(g + at) & 15u) == 0 &&
+               ((sdst + at) & 15u) == 0 && (n & 15u) == 0;
+    };
+    (void)band_range_ok;
     if (r_lo >= r_hi || a_hi <= a_lo || !allow_skip || a_hi - a_lo < skip_min) {
         mbar_arrive_expect_tx(bar, total + missing);
-        load_bytes(p, sdst, g, total, bar);
+        if (TRFN_CHECK(band_range_ok(0, total), 4)) load_bytes(p, sdst, g, total, bar);
         return;
     }
     const uint32_t skipped = (uint32_t)(r_hi - r_lo) * (a_hi - a_lo);
@@ -420,10 +501,12 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     uint32_t pos = 0;
     for (int r = r_lo; r < r_hi; ++r) {
         const uint32_t seg_end = (uint32_t)r * L + a_lo;
-        if (seg_end > pos) load_bytes(p, sdst + pos, g + pos, seg_end - pos, bar);
+        if (seg_end > pos && TRFN_CHECK(band_range_ok(pos, seg_end - pos), 5))
+            load_bytes(p, sdst + pos, g + pos, seg_end - pos, bar);
         pos = (uint32_t)r * L + a_hi;
     }
-    if (total > pos) load_bytes(p, sdst + pos, g + pos, total - pos, bar);
+    if (total > pos && TRFN_CHECK(band_range_ok(pos, total - pos), 5))
+        load_bytes(p, sdst + pos, g + pos, total - pos, bar);
 }
 
 // Early form of issue_unit for a CTA's first unit (compact sources): the
@@ -438,8 +521,13 @@ __device__ __forceinline__ void issue_unit_uncut(const TiledParams& p, int u, in
     const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
     const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;   // bounded-wait test hook
     mbar_expect_tx(bar, total + missing);
-    load_bytes(p, smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage,
-               p.src + ((size_t)b.n * p.H + b.y_begin) * L, total, bar);
+    const ImageRef im = image_ref(p, b.n);
+    const uint8_t* g = im.src + ((size_t)im.n * p.H + b.y_begin) * L;
+    const uint32_t sdst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
+    if (TRFN_CHECK(total <= p.in_stage && (uint64_t)(g - im.src) + total <= p.src_batch_bytes &&
+                       ((uintptr_t)g & 15u) == 0 && (sdst & 15u) == 0 && (total & 15u) == 0,
+                   6))
+        load_bytes(p, sdst, g, total, bar);
 }
 
 // Writes unit u's record (flip, clipped erase rectangle) for stage s and
@@ -502,6 +590,15 @@ __device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout,
     constexpr int OB = OUT_F16 ? 2 : 4;
     const int g = r * p.gpr + gx;   // the group's index in the band: its output sits at g * Q * 16
     const bool rotate = !(p.hints & 128);
+    // (checked build) the group's outputs lie in the output tile
+    if (!TRFN_CHECK(LAYOUT == TR_LAYOUT_NCHW
+                        ? (size_t)(C - 1) * p.plane_bytes + ((size_t)r * p.W + (size_t)(gx + 1) * P) * OB <=
+                                  p.out_stage &&
+                              ((size_t)r * p.W + (size_t)(gx + 1) * P) * OB <= p.plane_bytes
+                        : ((size_t)r * p.W + (size_t)(gx + 1) * P) * (LAYOUT == TR_LAYOUT_NHWC4 ? 4 : C) * OB <=
+                              p.out_stage,
+                    9))
+        return;
     if (LAYOUT == TR_LAYOUT_NHWC) {
         uint8_t* o = sout + ((size_t)r * p.W + (size_t)gx * P) * C * OB;
         if (OUT_F16) {
@@ -588,10 +685,11 @@ template <int C, int OUT_F16, int LAYOUT>
 __device__ __forceinline__ uint32_t odd_shift(const TiledParams& p, const UnitRec& rec, int c) {
     constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
     constexpr int OB = OUT_F16 ? 2 : 4;
-    size_t e;   // the band's first output element in the plane or the tensor
-    if (LAYOUT == TR_LAYOUT_NCHW) e = (((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W;
-    else e = ((size_t)rec.n * p.H + rec.y_begin) * p.W * OC;
-    return (uint32_t)((uintptr_t)(p.dst + e * OB) & 15u);
+    const ImageRef im = image_ref(p, rec.n);
+    size_t e;   // the band's first output element in the plane or the batch
+    if (LAYOUT == TR_LAYOUT_NCHW) e = (((size_t)im.n * C + c) * p.H + rec.y_begin) * p.W;
+    else e = ((size_t)im.n * p.H + rec.y_begin) * p.W * OC;
+    return (uint32_t)((uintptr_t)(im.dst + e * OB) & 15u);
 }
 
 // Writes len bytes (at least 16 - (s0 & 15), a multiple of EB) of the word
@@ -681,6 +779,14 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
     constexpr bool kStreamNHWC = LAYOUT == TR_LAYOUT_NHWC && (C * OB) % 8 != 0;
     constexpr bool kStreamNCHW = LAYOUT == TR_LAYOUT_NCHW && P * OB >= 32;
     const bool streams = !(p.hints & 1024);
+    // (checked build) the group's outputs, after the tile's alignment shift
+    // (below 16 bytes), lie in the output tile (per plane for NCHW)
+    if (!TRFN_CHECK(LAYOUT == TR_LAYOUT_NCHW
+                        ? (size_t)(C - 1) * p.plane_bytes + p.plane_bytes <= p.out_stage &&
+                              15 + ((size_t)r * p.W + (size_t)gx * P + kv) * OB <= p.plane_bytes
+                        : 15 + ((size_t)r * p.W + (size_t)gx * P + kv) * OC * OB <= p.out_stage,
+                    10))
+        return;
     if (kStreamNHWC && streams) {
         // the group's kv pixels are one run of output bytes
         constexpr int NW = P * C * OB / 4;
@@ -808,10 +914,21 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
                     sh = (at & 3u) * 8u;
                 }
                 uint32_t raw[Group<C>::kWords + 1];
+                // (checked build) the words read lie in the dynamic shared
+                // memory (a short mirrored group may start before its stage)
+                const bool rd_ok = TRFN_CHECK(reinterpret_cast<const uint8_t*>(wp) >= trfn_dyn_smem &&
+                                                  reinterpret_cast<const uint8_t*>(wp + Group<C>::kWords + 1) <=
+                                                      trfn_dyn_smem + p.smem_bytes,
+                                              8);
 #pragma unroll
-                for (int q = 0; q <= Group<C>::kWords; ++q) raw[q] = wp[q];
+                for (int q = 0; q <= Group<C>::kWords; ++q) raw[q] = rd_ok ? wp[q] : 0u;
 #pragma unroll
                 for (int q = 0; q < Group<C>::kWords; ++q) w[q] = __funnelshift_r(raw[q], raw[q + 1], sh);
+            } else if (!TRFN_CHECK(s >= sin && (size_t)(s - sin) + GB <= p.in_stage &&
+                                       ((uintptr_t)s & (GB == 16 ? 15u : 7u)) == 0,
+                                   7)) {
+#pragma unroll
+                for (int q = 0; q < Group<C>::kWords; ++q) w[q] = 0u;
             } else if (GB == 16) {
                 const uint4 t = *reinterpret_cast<const uint4*>(s);
                 w[0] = t.x; w[1] = t.y; w[2] = t.z; w[3] = t.w;
@@ -857,22 +974,30 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
         // bulk store, the unaligned first and last bytes element by element
         constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
         constexpr int NP = (LAYOUT == TR_LAYOUT_NCHW) ? C : 1;
+        const ImageRef im = image_ref(p, rec.n);
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
             size_t e;
             uint32_t bytes;
             if (LAYOUT == TR_LAYOUT_NCHW) {
-                e = (((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W;
+                e = (((size_t)im.n * C + c) * p.H + rec.y_begin) * p.W;
                 bytes = (uint32_t)rec.rows * p.W * OB;
             } else {
-                e = ((size_t)rec.n * p.H + rec.y_begin) * p.W * OC;
+                e = ((size_t)im.n * p.H + rec.y_begin) * p.W * OC;
                 bytes = (uint32_t)rec.rows * p.W * OC * OB;
             }
-            uint8_t* g = p.dst + e * OB;
+            uint8_t* g = im.dst + e * OB;
             const uint32_t sh = (uint32_t)((uintptr_t)g & 15u);
             const uint8_t* t = sout + (size_t)c * p.plane_bytes + sh;
             const uint32_t head = min(bytes, (16u - sh) & 15u);
             const uint32_t mid = (bytes - head) & ~15u;
+            // (checked build) the band's bytes lie in the batch's output and
+            // in the tile (its plane for NCHW)
+            if (!TRFN_CHECK((uint64_t)(g - im.dst) + bytes <= p.dst_batch_bytes &&
+                                (size_t)c * p.plane_bytes + sh + bytes <=
+                                    (LAYOUT == TR_LAYOUT_NCHW ? (size_t)(c + 1) * p.plane_bytes : p.out_stage),
+                            13))
+                continue;
             for (uint32_t i = 0; i < head; i += OB) {
                 if (OUT_F16) *reinterpret_cast<uint16_t*>(g + i) = *reinterpret_cast<const uint16_t*>(t + i);
                 else *reinterpret_cast<uint32_t*>(g + i) = *reinterpret_cast<const uint32_t*>(t + i);
@@ -881,23 +1006,37 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
                 if (OUT_F16) *reinterpret_cast<uint16_t*>(g + i) = *reinterpret_cast<const uint16_t*>(t + i);
                 else *reinterpret_cast<uint32_t*>(g + i) = *reinterpret_cast<const uint32_t*>(t + i);
             }
-            if (mid > 0) put(g + head, src + (uint32_t)(c * p.plane_bytes + sh + head), mid);
+            if (mid > 0 && TRFN_CHECK(((uintptr_t)(g + head) & 15u) == 0 &&
+                                          ((src + (uint32_t)(c * p.plane_bytes + sh + head)) & 15u) == 0,
+                                      14))
+                put(g + head, src + (uint32_t)(c * p.plane_bytes + sh + head), mid);
         }
         bulk_commit();
         return;
     }
+    const ImageRef im = image_ref(p, rec.n);
     if (LAYOUT == TR_LAYOUT_NCHW) {
         const uint32_t bytes = (uint32_t)rec.rows * p.W * OB;
 #pragma unroll
         for (int c = 0; c < C; ++c) {
-            uint8_t* g = p.dst + ((((size_t)rec.n * C + c) * p.H + rec.y_begin) * p.W) * OB;
-            put(g, src + (uint32_t)c * p.plane_bytes, bytes);
+            uint8_t* g = im.dst + ((((size_t)im.n * C + c) * p.H + rec.y_begin) * p.W) * OB;
+            // (checked build) inside the batch's output and the tile's plane,
+            // 16-byte aligned at both ends
+            if (TRFN_CHECK((uint64_t)(g - im.dst) + bytes <= p.dst_batch_bytes && bytes <= p.plane_bytes &&
+                               ((uintptr_t)g & 15u) == 0 && ((src + (uint32_t)c * p.plane_bytes) & 15u) == 0 &&
+                               (bytes & 15u) == 0,
+                           12))
+                put(g, src + (uint32_t)c * p.plane_bytes, bytes);
         }
     } else {
         const int ch = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
         const size_t row_bytes = (size_t)p.W * ch * OB;
-        uint8_t* g = p.dst + ((size_t)rec.n * p.H + rec.y_begin) * row_bytes;
-        put(g, src, (uint32_t)(rec.rows * row_bytes));
+        uint8_t* g = im.dst + ((size_t)im.n * p.H + rec.y_begin) * row_bytes;
+        const uint32_t bytes = (uint32_t)(rec.rows * row_bytes);
+        if (TRFN_CHECK((uint64_t)(g - im.dst) + bytes <= p.dst_batch_bytes && bytes <= p.out_stage &&
+                           ((uintptr_t)g & 15u) == 0 && (src & 15u) == 0 && (bytes & 15u) == 0,
+                       11))
+            put(g, src, bytes);
     }
     bulk_commit();
 }
@@ -969,8 +1108,7 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         // requested together, ahead of the wait for the stage they go to
         int2 org = make_int2(0, 0);
         auto unit_record = [&](int u) {
-            tr_aug_param r = {0, 0, 0, 0, 0};
-            if (p.aug != nullptr) r = p.aug[u / p.bands];
+            const tr_aug_param r = image_record(p, u / p.bands);
             if (CROP && p.crop != nullptr) {
                 org.x = p.crop[2 * (size_t)(u / p.bands)];
                 org.y = p.crop[2 * (size_t)(u / p.bands) + 1];
@@ -1767,7 +1905,21 @@ int launch_tiled(const LaunchArgs& a) {
     p.bands = pl.bands;
     p.num_units = a.N * pl.bands;
     p.gpr = odd ? (a.W + group_pixels(a.C) - 1) / group_pixels(a.C) : a.W / group_pixels(a.C);
-    p.src_floor16 = ((uint64_t)a.N * a.H * a.W * a.C) & ~15ull;
+    // the source bytes of one batch rounded down to 16 (odd-row form)
+    p.src_floor16 = ((uint64_t)(a.batch_images > 0 ? a.batch_images : a.N) * a.H * a.W * a.C) & ~15ull;
+    p.nb = a.batch_images;
+    {
+        const uint64_t n1 = (uint64_t)(a.batch_images > 0 ? a.batch_images : a.N);
+        const uint64_t oc = (a.out_layout == TR_LAYOUT_NHWC4) ? 4 : (uint64_t)a.C;
+        p.smem_bytes = (uint32_t)pl.smem;
+        p.src_batch_bytes = crop ? 0 : n1 * a.H * a.W * a.C;
+        p.dst_batch_bytes = n1 * a.H * a.W * oc * (a.out_dtype == TR_OUT_F16 ? 2 : 4);
+    }
+    for (int k = 0; k < TR_MAX_BATCHES; ++k) {
+        p.bsrc[k] = a.bsrc[k];
+        p.bdst[k] = static_cast<uint8_t*>(a.bdst[k]);
+        p.baug[k] = a.baug[k];
+    }
     p.gpr_inv = ((1ull << 32) + (uint64_t)p.gpr - 1) / (uint64_t)p.gpr;
     p.in_stage = pl.in_stage;
     p.out_stage = pl.out_stage;
@@ -1904,15 +2056,17 @@ int launch(const LaunchArgs& a, int variant) {
 }
 
 int read_device_status(int* flags, bool clear) {
-    unsigned int v = 0;
-    if (!check_cuda(cudaMemcpyFromSymbol(&v, g_device_status, sizeof v), "cudaMemcpyFromSymbol"))
+    unsigned int v = 0, site = 0;
+    if (!check_cuda(cudaMemcpyFromSymbol(&v, g_device_status, sizeof v), "cudaMemcpyFromSymbol") ||
+        !check_cuda(cudaMemcpyFromSymbol(&site, g_bounds_site, sizeof site), "cudaMemcpyFromSymbol"))
         return TR_ERR_CUDA;
     if (clear) {
         const unsigned int zero = 0;
-        if (!check_cuda(cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero), "cudaMemcpyToSymbol"))
+        if (!check_cuda(cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero), "cudaMemcpyToSymbol") ||
+            !check_cuda(cudaMemcpyToSymbol(g_bounds_site, &zero, sizeof zero), "cudaMemcpyToSymbol"))
             return TR_ERR_CUDA;
     }
-    if (flags) *flags = (int)v;
+    if (flags) *flags = (int)(v | ((site & 255u) << 8));
     return TR_OK;
 }
 

@@ -51,6 +51,14 @@ struct LaunchArgs {
     const int32_t* crop = nullptr;
     int src_H = 0, src_W = 0;
     size_t src_row_stride = 0, src_image_stride = 0;
+    // several batches in one tiled launch (tr_fused_norm_batches): N counts
+    // the images of all batches, batch_images those of one, and image n is
+    // image n % batch_images of batch n / batch_images (src, dst and aug are
+    // then batch 0's); 0 = one batch
+    int batch_images = 0;
+    const uint8_t* bsrc[TR_MAX_BATCHES] = {};
+    void* bdst[TR_MAX_BATCHES] = {};
+    const tr_aug_param* baug[TR_MAX_BATCHES] = {};
 };
 
 constexpr size_t kWorkspaceBytes = 2048;

@@ -188,6 +188,41 @@ int tr_fused_norm_ex(const uint8_t* src_u8, void* dst, int N, int H, int W, int 
                      int out_dtype, int out_layout, void* stream, int variant, void* workspace,
                      unsigned flags);
 
+/* tr_fused_norm_batches — the fused step on K batches of the same shape in
+ * one launch (the article's execute() runs once per batch, §五; a data
+ * loader hands the step one batch after another).  Each launch that waits
+ * for the previous one pays a fixed cost (grid launch, the first copies'
+ * round trip, the drain of its last bands: about 2.5 us of 19 at
+ * 256x224x224x3 -> binary16); one launch over K batches pays it once.
+ *   batches     host array of K descriptors, read during the call: batch k's
+ *               source (N*H*W*C bytes, compact NHWC uint8), output (as
+ *               tr_fused_norm's dst) and records (N, or NULL: no flip and no
+ *               erase), all device pointers.
+ *   K           0 <= K <= TR_MAX_BATCHES (0 = nothing to do).
+ *   N,H,W,C, mean, std, out_dtype, out_layout: the shape of ONE batch and
+ *               the step's settings, as tr_fused_norm.
+ *   stream, workspace, flags: as tr_fused_norm_ex (one workspace for the
+ *               launch; TR_LAUNCH_OVERLAP_PREVIOUS promises that no batch
+ *               shares a buffer with the kernel before the call).
+ * Results: batch k's output equals tr_fused_norm's on batch k, bit for bit.
+ * Every source and output must be 16-byte aligned and the batches large
+ * enough for the TILED kernel (tr_fused_norm_plan on K*N images) for the
+ * single launch; otherwise the batches are launched one after another
+ * (stream order, same results).
+ * Errors as tr_fused_norm for every batch, TR_ERR_INVALID_ARGUMENT for K
+ * outside 0..TR_MAX_BATCHES, a NULL batches array with K > 0, or any batch's
+ * output overlapping any batch's source or another batch's output.          */
+#define TR_MAX_BATCHES 16
+typedef struct tr_batch {
+    const uint8_t* src_u8;
+    void* dst;
+    const tr_aug_param* aug_params;
+} tr_batch;
+
+int tr_fused_norm_batches(const tr_batch* batches, int K, int N, int H, int W, int C, const float* mean,
+                          const float* std, int out_dtype, int out_layout, void* stream, void* workspace,
+                          unsigned flags);
+
 /* tr_fused_norm_crop — the fused step on H x W windows of a larger, strided
  * source: the crop just upstream of the step fused into its load (the
  * article's execute() takes an input stride, §五; DALI's crop_mirror_normalize,

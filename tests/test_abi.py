@@ -264,3 +264,33 @@ def test_fused_sampled_host_checks():
     # N > 0 without a records buffer
     assert L.tr_fused_norm_sampled(0x1000, 0x200000, 4, 8, 8, 3, m, s, 1, 0, ctypes.byref(good), None, None,
                                    1, 0, None, 0, None) == 1
+
+
+def test_batches_arguments_rejected_before_launch():
+    """tr_fused_norm_batches checks everything on the host first: the batch
+    count, the descriptors, every batch's pointers and that no output
+    overlaps a source or another output (no GPU is touched here)."""
+    L = _native.lib()
+    B = _native.Batch
+
+    def call(bs, K=None, N=2, H=4, W=16, C=3, dt=1, lay=0, ws=None, flags=0):
+        arr = (B * max(1, len(bs)))(*bs) if bs else None
+        return L.tr_fused_norm_batches(arr, len(bs) if K is None else K, N, H, W, C, M3, S3, dt, lay, None, ws,
+                                       flags)
+
+    img_in, img_out = 2 * 4 * 16 * 3, 2 * 4 * 16 * 3 * 2
+    good = [B(0x100000 + k * 0x10000, 0x900000 + k * 0x10000, None) for k in range(3)]
+    assert call([]) == 0                                   # K = 0: nothing to do
+    assert call(good, N=0) == 0                            # N = 0: nothing to do
+    assert call(good, K=-1) == INVALID
+    assert call(good * 6) == INVALID                       # 18 > TR_MAX_BATCHES
+    assert call([], K=2) == INVALID                        # no descriptors
+    assert call(good, C=5) == NOT_SUPPORTED
+    assert call(good, flags=2) == INVALID
+    assert call(good, ws=0x3008) == INVALID                # workspace off 16 bytes
+    assert call([good[0], B(None, 0x990000, None)]) == INVALID
+    assert call([good[0], B(0x180000, 0x990001, None)]) == INVALID   # output off its element size
+    assert call([good[0], B(0x180000, 0x990000, 0x2002)]) == INVALID  # records off int32
+    # batch 1 writes over batch 0's source; batch 1 writes into batch 0's output
+    assert call([good[0], B(0x180000, 0x100000 + img_in - 2, None)]) == INVALID
+    assert call([good[0], B(0x180000, 0x900000 + img_out - 2, None)]) == INVALID

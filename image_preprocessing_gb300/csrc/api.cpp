@@ -183,6 +183,7 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
         if (rc != TR_OK) return rc;
         a.aug = smp.out;
         a.records_from_prev = true;
+        a.spec = &smp.spec;
     }
     rc = launch(a, variant);
     if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {

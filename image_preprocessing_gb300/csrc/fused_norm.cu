@@ -54,6 +54,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "aug_sampling.cuh"
 #include "internal.h"
 
 namespace trfn {
@@ -318,7 +319,10 @@ struct TiledParams {
                            // first band (5), bounded-wait test hook (6), unrotated tile
                            // stores (7), erased-span rule (11, 12-15); set by the launch:
                            // overlap the previous grid (8), records written by it (9),
-                           // odd-row element stores (10)
+                           // odd-row element stores (10), plain order of 16-byte
+                           // odd-row NCHW plane runs (20), first records made by
+                           // the producer warp from spec (21, set by the launch
+                           // unless tr_tune_tiled bit 21)
     float base[4];         // 2^23 + shift_c (see byte_minus_shift)
     float scale[4];
     float bias[4];
@@ -329,6 +333,10 @@ struct TiledParams {
     uint32_t smem_bytes;        // dynamic shared memory of a CTA (checked build)
     uint64_t src_batch_bytes;   // compact sources: bytes of one batch (checked build)
     uint64_t dst_batch_bytes;   // output bytes of one batch (checked build)
+    // records made on the GPU by the sampler launched just before
+    // (tr_fused_norm_sampled): its settings, so that the producer warp can
+    // make a CTA's first records itself (hints bit 21)
+    SampleSpec spec;
     const uint8_t* bsrc[TR_MAX_BATCHES];
     uint8_t* bdst[TR_MAX_BATCHES];
     const tr_aug_param* baug[TR_MAX_BATCHES];
@@ -829,6 +837,49 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
         return;
     }
     if (LAYOUT == TR_LAYOUT_NCHW) {
+        // 16-byte binary16 plane runs (2 or 3 channels): the 32 lanes of a
+        // warp hold consecutive groups, 16 bytes apart, so storing element i
+        // of every lane's run at once hits each bank four times.  Each lane
+        // instead walks its run's four words starting at word (lane / 8) % 4:
+        // then every store instruction of the warp falls on 32 different
+        // banks (lanes 8 apart take different words, lanes closer than 8 lie
+        // in different 16-byte chunks).  Measured at 256x299x299, waiting
+        // launches: two channels 38.9 -> 37.2 us, three channels 55.2 ->
+        // 55.5 us (no gain); four-channel binary32 runs lost 3 % and keep
+        // the plain order.  tr_tune_tiled flags bit 20 keeps the plain order.
+        constexpr bool kRotate16 = (P * OB == 16) && OUT_F16;
+        if (kRotate16 && !(p.hints & 1048576)) {
+            const uint32_t q = (threadIdx.x >> 3) & 3u;
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) +
+                             ((size_t)r * p.W + (size_t)gx * P) * OB;
+                uint32_t w[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    if constexpr (OUT_F16 != 0) w[m] = pack_half2(v[(2 * m) * C + c], v[(2 * m + 1) * C + c]);
+                    else w[m] = __float_as_uint(v[m * C + c]);
+                }
+                // rotate: w[m] <- word (m + q) % 4 (two select stages, registers only)
+                uint32_t t[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) t[m] = (q & 1u) ? w[(m + 1) & 3] : w[m];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) w[m] = (q & 2u) ? t[(m + 2) & 3] : t[m];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t wi = (m + q) & 3u;   // the word of the run w[m] holds
+                    uint8_t* at = o + 4u * wi;
+                    if constexpr (OUT_F16 != 0) {
+                        if ((int)(2 * wi) < kv) *reinterpret_cast<uint16_t*>(at) = (uint16_t)(w[m] & 0xFFFFu);
+                        if ((int)(2 * wi + 1) < kv) *reinterpret_cast<uint16_t*>(at + 2) = (uint16_t)(w[m] >> 16);
+                    } else {
+                        if ((int)wi < kv) *reinterpret_cast<uint32_t*>(at) = w[m];
+                    }
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int c = 0; c < C; ++c) {
             uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) +
@@ -1041,6 +1092,34 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
     bulk_commit();
 }
 
+// The records the sampler grid is writing are readable only once it has
+// completed, which is after the kernel before it in the stream.  For a CTA's
+// first S units the producer warp makes the records itself instead, with the
+// sampler's steps (the same bits): lane 0 requests the S bands whole, then
+// the warp samples each unit's record (a lane per draw) and lane 0 publishes
+// it, so those bands convert while that kernel drains.  Later units' records
+// are read from the sampler's output after the wait.  Kept out of line so the
+// kernel's main path does not carry it.  Returns the number of units started.
+template <int C>
+__device__ __noinline__ int first_units_self_sampled(const TiledParams& p, uint8_t* smem, int S, int G) {
+    const int lane = (int)threadIdx.x;
+    int j = 0;
+    if (lane == 0) {
+        for (; j < S; ++j) {
+            const int uu = (int)blockIdx.x + j * G;
+            if (uu >= p.num_units) break;
+            issue_unit_uncut<C>(p, uu, j, smem);
+        }
+    }
+    j = __shfl_sync(0xffffffffu, j, 0);
+    for (int t = 0; t < j; ++t) {
+        const int uu = (int)blockIdx.x + t * G;
+        const tr_aug_param r = sample_record_warp(p.spec, uu / p.bands, lane);
+        if (lane == 0) publish_unit(p, uu, t, smem, r);
+    }
+    return j;
+}
+
 // Scheduling workspace: kTicketGroups ticket counters, each on its own
 // 128-byte line, then the count of finished CTAs.  With g = min(kTicketGroups,
 // gridDim.x) groups, CTA b draws from counter b % g, which hands out the
@@ -1062,7 +1141,13 @@ constexpr int kDoneWord = kTicketGroups * kTicketStride;
 // (An explicit minimum of one CTA per SM lets ptxas use up to 63 registers
 // here, against 61 without it, and measured 0.9 % faster at 256x224x224x3.)
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
-__global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ TiledParams p) {
+constexpr int tiled_min_blocks() {
+    return (ODD && LAYOUT == TR_LAYOUT_NCHW && Group<C>::P * (OUT_F16 ? 2 : 4) == 16) ? 4 : 1;
+}
+
+template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
+__global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CROP, ODD>()))
+    tiled_kernel(const __grid_constant__ TiledParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
     const uint32_t full0 = smem_u32(smem);
@@ -1098,8 +1183,10 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
 
     if (threadIdx.x < 32) {
         // The producer: lane 0 waits on barriers, issues copies, takes
-        // tickets and loads the records; the other lanes leave.
-        if (threadIdx.x != 0) return;
+        // tickets and loads the records; the other lanes leave (with hints
+        // bit 21 they first help to sample the CTA's first records).
+        const bool self_sample = !CROP && !ODD && overlapped && (p.hints & 512) && (p.hints & 2097152);
+        if (threadIdx.x != 0 && !self_sample) return;
         const int G = gridDim.x;
         const int ngroups = min(kTicketGroups, G);   // every group must have a CTA
         const int group = (int)blockIdx.x % ngroups;
@@ -1137,7 +1224,15 @@ __global__ void __launch_bounds__(256, 1) tiled_kernel(const __grid_constant__ T
         int j = 0;
         bool ok = true;
         bool waited = !overlapped;   // the previous grid has completed
-        if (recdep) {
+        if (recdep && self_sample) {
+            j = first_units_self_sampled<C>(p, smem, S, G);
+            if (threadIdx.x != 0) return;
+            grid_dependency_wait();
+            waited = true;
+            if (!(p.hints & 8)) grid_launch_dependents();
+            u = next_unit(j);
+            if (u < p.num_units) a = unit_record(u);
+        } else if (recdep) {
             // the first S units are blockIdx.x + t * G (no array: it would
             // live in local memory)
             for (; j < S; ++j) {
@@ -1925,12 +2020,20 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
-    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000);
+    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000 | 1048576);
     // copies may start before the previous grid completes; records that grid
     // wrote are read after it (compact aligned sources; the crop and
     // odd-row forms then wait for it before they touch memory)
     if (a.overlap_prev && !(a.records_from_prev && (crop || odd))) p.hints |= 256;
     if (a.overlap_prev && a.records_from_prev && !crop && !odd) p.hints |= 512;
+    // the sampler's settings are known: the first records are made in the
+    // kernel (tr_tune_tiled flags bit 21 reads them from the sampler instead)
+    if (a.spec != nullptr) {
+        p.spec = *a.spec;
+        if (!(tflags & 2097152)) p.hints |= 2097152;
+    } else {
+        p.spec = SampleSpec();
+    }
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) {
         p.base[c] = 8388608.0f + a.shift[c];   // exact: |shift| <= 2^20

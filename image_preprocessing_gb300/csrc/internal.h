@@ -45,6 +45,9 @@ struct LaunchArgs {
     // device sampler): with overlap_prev the tiled kernel requests its first
     // bands before that kernel has completed and reads the records after
     bool records_from_prev = false;
+    // with records_from_prev: the sampler's settings (the tiled kernel then
+    // makes a CTA's first records itself, bit-identical), or null
+    const SampleSpec* spec = nullptr;
     // windows of a strided source (tr_fused_norm_crop); otherwise a compact
     // NHWC source of H x W images
     bool crop_src = false;

@@ -632,7 +632,18 @@ int tr_device_status(int* flags, int clear);
  *                    each group's output bytes moved to the tile's 16-byte
  *                    frame in registers and written with 16-byte stores,
  *                    2/4/8-byte stores only at its ends), bit 17 uses that
- *                    realignment however few bands a CTA gets;
+ *                    realignment however few bands a CTA gets; bit 20 makes
+ *                    the odd-row form store 16-byte binary16 NCHW plane runs
+ *                    (2 or 3 channels) in plain element order (default: each
+ *                    lane starts at word (lane / 8) % 4 of its run, so a
+ *                    warp's stores fall on distinct banks);
+ *                    records made on the GPU in the same call
+ *                    (tr_fused_norm_sampled_ex with TR_LAUNCH_OVERLAP_PREVIOUS):
+ *                    bit 21 makes each CTA read its first bands' records from
+ *                    the sampler's output once the sampler has completed
+ *                    (default: its producer warp makes them with the
+ *                    sampler's steps, the same bits, so those bands convert
+ *                    while the kernel before drains);
  *                    crop sources: bit 8 reads 16-byte chunks even where 32-byte
  *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion;
  *                    compact sources: erased source spans are left out of a

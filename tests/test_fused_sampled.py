@@ -110,12 +110,26 @@ def test_bad_arguments_launch_nothing():
 @pytest.mark.parametrize("shape,dt,layout", [((64, 224, 224, 3), trfn.OUT_F16, trfn.LAYOUT_NHWC),
                                              ((32, 224, 224, 3), trfn.OUT_F32, trfn.LAYOUT_NCHW),
                                              ((24, 299, 299, 3), trfn.OUT_F16, trfn.LAYOUT_NHWC)])   # odd-row form
-def test_overlapped_sampled_launches(shape, dt, layout):
+@pytest.mark.parametrize("first_records", ["made_in_kernel", "read_from_sampler"])
+def test_overlapped_sampled_launches(shape, dt, layout, first_records):
     """tr_fused_norm_sampled_ex with TR_LAUNCH_OVERLAP_PREVIOUS: a large
     launch, then consecutive sampled batches with their own source, output
     and records, workspaces alternating.  Each sampler writes while the
     kernel before it drains, each fused kernel requests its first bands
-    before its sampler is done: records and outputs equal the oracle's."""
+    before its sampler is done; by default its producer warp makes those
+    bands' records itself with the sampler's steps (tr_tune_tiled flags bit
+    21 reads them from the sampler's output instead).  Records and outputs
+    equal the oracle's either way."""
+    import torch
+    if first_records == "read_from_sampler":
+        trfn.tr_tune_tiled(flags=1 << 21)
+    try:
+        _overlapped_sampled_chain(shape, dt, layout)
+    finally:
+        trfn.tr_tune_tiled()
+
+
+def _overlapped_sampled_chain(shape, dt, layout):
     import torch
     N, H, W, C = shape
     K = 6

@@ -46,7 +46,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "images/sec and achieved HBM GB/s (fraction of peak) at 256×224×224×3"
 FALLBACK_HBM_GBS = 6800.0
-SPACER_CYCLES = 2_000_000   # about 1 ms at GB300's 2.07 GHz SM clock
+SPACER_CYCLES = 200_000   # about 0.1 ms at GB300's 2.07 GHz SM clock
 
 
 def parse():

@@ -177,13 +177,11 @@ int fused_norm_impl(const uint8_t* src, void* dst, int N, int H, int W, int C, c
     const bool same_ws = note_stream_workspace(stream, workspace);
     a.overlap_prev = (flags & TR_LAUNCH_OVERLAP_PREVIOUS) != 0 && !same_ws;
     if (smp.on) {
-        // the records first, into smp.out, then the kernel reads them in
-        // stream order (its prologue overlaps the sampler)
-        rc = launch_sampler(smp.spec, N, smp.out, stream, a.overlap_prev);
-        if (rc != TR_OK) return rc;
-        a.aug = smp.out;
-        a.records_from_prev = true;
+        // records made on the GPU: by the tiled kernel itself where it can,
+        // else by the sampler first (launch() decides)
+        a.aug = nullptr;
         a.spec = &smp.spec;
+        a.records_out = smp.out;
     }
     rc = launch(a, variant);
     if (rc == TR_ERR_NOT_SUPPORTED && variant == TR_VARIANT_TILED && !forced) {

@@ -320,9 +320,8 @@ struct TiledParams {
                            // stores (7), erased-span rule (11, 12-15); set by the launch:
                            // overlap the previous grid (8), records written by it (9),
                            // odd-row element stores (10), plain order of 16-byte
-                           // odd-row NCHW plane runs (20), first records made by
-                           // the producer warp from spec (21, set by the launch
-                           // unless tr_tune_tiled bit 21)
+                           // odd-row NCHW plane runs (20), a sampled launch's first
+                           // records made by the producer warp (22)
     float base[4];         // 2^23 + shift_c (see byte_minus_shift)
     float scale[4];
     float bias[4];
@@ -333,14 +332,22 @@ struct TiledParams {
     uint32_t smem_bytes;        // dynamic shared memory of a CTA (checked build)
     uint64_t src_batch_bytes;   // compact sources: bytes of one batch (checked build)
     uint64_t dst_batch_bytes;   // output bytes of one batch (checked build)
-    // records made on the GPU by the sampler launched just before
-    // (tr_fused_norm_sampled): its settings, so that the producer warp can
-    // make a CTA's first records itself (hints bit 21)
+    // records made on the GPU (tr_fused_norm_sampled): the sampler's
+    // settings, with which the kernel makes its CTAs' first records
     SampleSpec spec;
     const uint8_t* bsrc[TR_MAX_BATCHES];
     uint8_t* bdst[TR_MAX_BATCHES];
     const tr_aug_param* baug[TR_MAX_BATCHES];
 };
+
+// What a tiled launch covers, fixed at compile time so that each form
+// carries only its own code: one batch whose records are read (or absent),
+// several batches of one shape (tr_fused_norm_batches), or one batch whose
+// records a sampler grid is writing while the launch starts, of which the
+// kernel makes its CTAs' first ones itself (tr_fused_norm_sampled).
+constexpr int kModeBatch = 0;
+constexpr int kModeBatches = 1;
+constexpr int kModeSampled = 2;
 
 // Image n of the launch: its batch's source and output base pointers and
 // its index in that batch.
@@ -350,21 +357,26 @@ struct ImageRef {
     int n;
 };
 
+template <int MODE>
 __device__ __forceinline__ ImageRef image_ref(const TiledParams& p, int n) {
-    if (p.nb == 0) return ImageRef{p.src, p.dst, n};
-    const int k = n / p.nb;
-    return ImageRef{p.bsrc[k], p.bdst[k], n - k * p.nb};
+    if constexpr (MODE == kModeBatches) {
+        const int k = n / p.nb;
+        return ImageRef{p.bsrc[k], p.bdst[k], n - k * p.nb};
+    } else {
+        return ImageRef{p.src, p.dst, n};
+    }
 }
 
 // Image n's record ({0} without records).
+template <int MODE>
 __device__ __forceinline__ tr_aug_param image_record(const TiledParams& p, int n) {
     tr_aug_param r = {0, 0, 0, 0, 0};
-    if (p.nb == 0) {
-        if (p.aug != nullptr) r = p.aug[n];
-    } else {
+    if constexpr (MODE == kModeBatches) {
         const int k = n / p.nb;
         const tr_aug_param* a = p.baug[k];
         if (a != nullptr) r = a[n - k * p.nb];
+    } else {
+        if (p.aug != nullptr) r = p.aug[n];
     }
     return r;
 }
@@ -405,7 +417,7 @@ __device__ __forceinline__ void load_bytes(const TiledParams& p, uint32_t dst, c
 // allowed and worth a copy) the 16-byte chunks that lie wholly inside the
 // erased source span of the erased
 // rows.
-template <int C, bool CROP, bool ODD>
+template <int C, bool CROP, bool ODD, int MODE>
 __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, uint8_t* smem,
                                            const tr_aug_param& a, bool allow_skip, int2 origin) {
     const Band b = band_of(p, u);
@@ -448,7 +460,7 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
         // starts `off` bytes into the stage (consumers realign), and any
         // bytes past the source's last whole 16 are copied by this thread.
         // (offsets from the image's batch, whose source starts 16-byte aligned)
-        const ImageRef im = image_ref(p, b.n);
+        const ImageRef im = image_ref<MODE>(p, b.n);
         const uint64_t L = (uint64_t)p.W * C;
         const uint64_t base = ((uint64_t)im.n * p.H + y_begin) * L;
         const uint64_t end = base + (uint64_t)rows * L;
@@ -471,7 +483,7 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
     }
 
     const uint32_t L = (uint32_t)p.W * C;
-    const ImageRef im = image_ref(p, b.n);
+    const ImageRef im = image_ref<MODE>(p, b.n);
     const uint8_t* g = im.src + ((size_t)im.n * p.H + y_begin) * L;
     const uint32_t sdst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
     const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;   // full[s]
@@ -521,7 +533,7 @@ __device__ __forceinline__ void issue_unit(const TiledParams& p, int u, int s, u
 // whole band is requested before the unit's record has arrived; only the
 // expected byte count is posted, so the stage cannot complete before
 // publish_unit has written the record and arrived.
-template <int C>
+template <int C, int MODE>
 __device__ __forceinline__ void issue_unit_uncut(const TiledParams& p, int u, int s, uint8_t* smem) {
     const Band b = band_of(p, u);
     const uint32_t L = (uint32_t)p.W * C;
@@ -529,7 +541,7 @@ __device__ __forceinline__ void issue_unit_uncut(const TiledParams& p, int u, in
     const uint32_t bar = smem_u32(smem) + 8u * (uint32_t)s;
     const uint32_t missing = ((p.hints & 64) && u == 0) ? 16u : 0u;   // bounded-wait test hook
     mbar_expect_tx(bar, total + missing);
-    const ImageRef im = image_ref(p, b.n);
+    const ImageRef im = image_ref<MODE>(p, b.n);
     const uint8_t* g = im.src + ((size_t)im.n * p.H + b.y_begin) * L;
     const uint32_t sdst = smem_u32(smem + kHeaderBytes) + (uint32_t)s * p.in_stage;
     if (TRFN_CHECK(total <= p.in_stage && (uint64_t)(g - im.src) + total <= p.src_batch_bytes &&
@@ -689,11 +701,11 @@ __device__ __forceinline__ void store_group(const TiledParams& p, uint8_t* sout,
 // band's global alignment (it starts at the band's global address mod 16,
 // per plane for NCHW), so its bulk store can cover the 16-byte aligned
 // middle; groups are written element by element, only their kv valid pixels.
-template <int C, int OUT_F16, int LAYOUT>
+template <int C, int OUT_F16, int LAYOUT, int MODE>
 __device__ __forceinline__ uint32_t odd_shift(const TiledParams& p, const UnitRec& rec, int c) {
     constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
     constexpr int OB = OUT_F16 ? 2 : 4;
-    const ImageRef im = image_ref(p, rec.n);
+    const ImageRef im = image_ref<MODE>(p, rec.n);
     size_t e;   // the band's first output element in the plane or the batch
     if (LAYOUT == TR_LAYOUT_NCHW) e = (((size_t)im.n * C + c) * p.H + rec.y_begin) * p.W;
     else e = ((size_t)im.n * p.H + rec.y_begin) * p.W * OC;
@@ -769,7 +781,7 @@ __device__ __forceinline__ void put_stream(uint8_t* tile, uint32_t s0, uint32_t 
     }
 }
 
-template <int C, int OUT_F16, int LAYOUT>
+template <int C, int OUT_F16, int LAYOUT, int MODE>
 __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* sout, const UnitRec& rec, int r,
                                                 int gx, int kv, const float (&v)[Group<C>::kBytes]) {
     constexpr int P = Group<C>::P;
@@ -798,7 +810,7 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
     if (kStreamNHWC && streams) {
         // the group's kv pixels are one run of output bytes
         constexpr int NW = P * C * OB / 4;
-        const uint32_t s0 = odd_shift<C, OUT_F16, LAYOUT>(p, rec, 0) + ((uint32_t)r * p.W + (uint32_t)gx * P) * (C * OB);
+        const uint32_t s0 = odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, 0) + ((uint32_t)r * p.W + (uint32_t)gx * P) * (C * OB);
         const uint32_t len = (uint32_t)kv * (C * OB);
         if ((s0 & 15u) + len >= 16u) {
             uint32_t w[NW];
@@ -818,7 +830,7 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
         const uint32_t len = (uint32_t)kv * OB;
 #pragma unroll
         for (int c = 0; c < C; ++c) {
-            const uint32_t s0 = odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) + at;
+            const uint32_t s0 = odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, c) + at;
             uint8_t* plane = sout + (size_t)c * p.plane_bytes;
             if ((s0 & 15u) + len >= 16u) {
                 uint32_t w[NW];
@@ -852,7 +864,7 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
             const uint32_t q = (threadIdx.x >> 3) & 3u;
 #pragma unroll
             for (int c = 0; c < C; ++c) {
-                uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) +
+                uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, c) +
                              ((size_t)r * p.W + (size_t)gx * P) * OB;
                 uint32_t w[4];
 #pragma unroll
@@ -882,7 +894,7 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
         }
 #pragma unroll
         for (int c = 0; c < C; ++c) {
-            uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT>(p, rec, c) +
+            uint8_t* o = sout + (size_t)c * p.plane_bytes + odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, c) +
                          ((size_t)r * p.W + (size_t)gx * P) * OB;
 #pragma unroll
             for (int i = 0; i < P; ++i)
@@ -893,7 +905,7 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
         // that long and aligned, else element by element (runs of 4-byte
         // stores for 6-byte binary16 pixels measured slower)
         constexpr int PB = OC * OB;
-        uint8_t* o = sout + odd_shift<C, OUT_F16, LAYOUT>(p, rec, 0) + ((size_t)r * p.W + (size_t)gx * P) * PB;
+        uint8_t* o = sout + odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, 0) + ((size_t)r * p.W + (size_t)gx * P) * PB;
 #pragma unroll
         for (int i = 0; i < P; ++i) {
             if (i < kv) {
@@ -923,7 +935,7 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
     }
 }
 
-template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
+template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD, int MODE>
 __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
                                              uint8_t* sout, const UnitRec& rec, int tid, int nthr) {
     constexpr int P = Group<C>::P;
@@ -1001,12 +1013,12 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
                 }
             }
         }
-        if (ODD) store_group_odd<C, OUT_F16, LAYOUT>(p, sout, rec, r, gx, kv, v);
+        if (ODD) store_group_odd<C, OUT_F16, LAYOUT, MODE>(p, sout, rec, r, gx, kv, v);
         else store_group<C, OUT_F16, LAYOUT>(p, sout, r, gx, v);
     }
 }
 
-template <int C, int OUT_F16, int LAYOUT, bool ODD>
+template <int C, int OUT_F16, int LAYOUT, bool ODD, int MODE>
 __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* sout,
                                            const UnitRec& rec) {
     constexpr int OB = OUT_F16 ? 2 : 4;
@@ -1025,7 +1037,7 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
         // bulk store, the unaligned first and last bytes element by element
         constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
         constexpr int NP = (LAYOUT == TR_LAYOUT_NCHW) ? C : 1;
-        const ImageRef im = image_ref(p, rec.n);
+        const ImageRef im = image_ref<MODE>(p, rec.n);
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
             size_t e;
@@ -1065,7 +1077,7 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
         bulk_commit();
         return;
     }
-    const ImageRef im = image_ref(p, rec.n);
+    const ImageRef im = image_ref<MODE>(p, rec.n);
     if (LAYOUT == TR_LAYOUT_NCHW) {
         const uint32_t bytes = (uint32_t)rec.rows * p.W * OB;
 #pragma unroll
@@ -1092,34 +1104,6 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
     bulk_commit();
 }
 
-// The records the sampler grid is writing are readable only once it has
-// completed, which is after the kernel before it in the stream.  For a CTA's
-// first S units the producer warp makes the records itself instead, with the
-// sampler's steps (the same bits): lane 0 requests the S bands whole, then
-// the warp samples each unit's record (a lane per draw) and lane 0 publishes
-// it, so those bands convert while that kernel drains.  Later units' records
-// are read from the sampler's output after the wait.  Kept out of line so the
-// kernel's main path does not carry it.  Returns the number of units started.
-template <int C>
-__device__ __noinline__ int first_units_self_sampled(const TiledParams& p, uint8_t* smem, int S, int G) {
-    const int lane = (int)threadIdx.x;
-    int j = 0;
-    if (lane == 0) {
-        for (; j < S; ++j) {
-            const int uu = (int)blockIdx.x + j * G;
-            if (uu >= p.num_units) break;
-            issue_unit_uncut<C>(p, uu, j, smem);
-        }
-    }
-    j = __shfl_sync(0xffffffffu, j, 0);
-    for (int t = 0; t < j; ++t) {
-        const int uu = (int)blockIdx.x + t * G;
-        const tr_aug_param r = sample_record_warp(p.spec, uu / p.bands, lane);
-        if (lane == 0) publish_unit(p, uu, t, smem, r);
-    }
-    return j;
-}
-
 // Scheduling workspace: kTicketGroups ticket counters, each on its own
 // 128-byte line, then the count of finished CTAs.  With g = min(kTicketGroups,
 // gridDim.x) groups, CTA b draws from counter b % g, which hands out the
@@ -1127,6 +1111,99 @@ __device__ __noinline__ int first_units_self_sampled(const TiledParams& p, uint8
 constexpr int kTicketGroups = 8;
 constexpr int kTicketStride = 32;   // uint32 words between counters (128 bytes)
 constexpr int kDoneWord = kTicketGroups * kTicketStride;
+
+// The producer's last steps (lane 0), after it has issued `j` fills: the
+// wait for the previous grid if it has not been taken, the release of the
+// next one, the status or the workspace reset by the last CTA to finish, and
+// the wait for the bands in flight (bounded).  Fill k's phase is the latest
+// of its stage only if no later fill used the stage: after a normal end the
+// end mark took stage j % S, so fill j - S is done and superseded.
+__device__ __forceinline__ void producer_finish(const TiledParams& p, uint32_t full0, int j, int S, bool ok,
+                                                bool waited) {
+    if (!waited) grid_dependency_wait();
+    grid_launch_dependents();
+    if (!ok) {
+        atomicOr(&g_device_status, kStatusTimeout);
+    } else if (p.ws != nullptr) {
+        __threadfence();
+        if (atomicAdd(p.ws + kDoneWord, 1u) == gridDim.x - 1) {
+            for (int g = 0; g < kTicketGroups; ++g) p.ws[g * kTicketStride] = 0;
+            p.ws[kDoneWord] = 0;
+            __threadfence();
+        }
+    }
+    for (int k = max(0, ok ? j - S + 1 : j - S); k < j; ++k) {
+        if (!mbar_wait_bounded(full0 + 8u * (k % S), (uint32_t)(k / S) & 1u)) {
+            atomicOr(&g_device_status, kStatusTimeout);
+            break;
+        }
+    }
+}
+
+// Records made on the GPU in the same call (tr_fused_norm_sampled with
+// TR_LAUNCH_OVERLAP_PREVIOUS, compact source with 16-byte aligned rows): the
+// sampler grid launched just before writes them all, but they are readable
+// only once it has completed, which is after the kernel before it in the
+// stream.  So a CTA's first S records are made in the kernel, with the
+// sampler's steps (a lane per Philox draw, the decisions on every lane with
+// the draws shuffled in: the same bits), and those bands convert while the
+// kernel before drains; later units' records are read from the sampler's
+// output after the wait.  Consumer warps 1..S make the first S records in
+// parallel while the first copies are in flight (they have nothing to
+// convert yet); named barrier 2 orders each publication after the producer
+// has posted the stage's byte count.  Where a CTA has fewer consumer warps
+// than stages, or tr_tune_tiled flags bit 22 asks for it, the producer warp
+// makes them one after another instead.
+__device__ __forceinline__ bool first_records_by_consumers(const TiledParams& p) {
+    return p.stages <= (int)(blockDim.x >> 5) - 1 && !(p.hints & 4194304);
+}
+
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Consumer warp w (0-based): the record of the CTA's w-th unit, published on
+// stage w once the producer has posted the band's bytes.
+__device__ __forceinline__ void consumer_first_record(const TiledParams& p, uint8_t* smem, int w) {
+    const int lane = (int)(threadIdx.x & 31u);
+    const int uu = (int)blockIdx.x + w * (int)gridDim.x;
+    tr_aug_param r = {0, 0, 0, 0, 0};
+    if (uu < p.num_units) r = sample_record_warp(p.spec, uu / p.bands, lane);
+    named_barrier_sync(2, (uint32_t)(p.stages + 1) * 32u);
+    if (uu < p.num_units && lane == 0) publish_unit(p, uu, w, smem, r);
+}
+
+// The producer warp's start in such a launch (all 32 lanes): lane 0
+// requests the first S bands whole, then the records are made (by the
+// consumers, or here).  Returns the number of bands requested.
+template <int C>
+__device__ __forceinline__ int first_bands_sampled(const TiledParams& p, uint8_t* smem) {
+    const int lane = (int)threadIdx.x;
+    const int S = p.stages;
+    const int G = (int)gridDim.x;
+    int j = 0;
+    if (lane == 0) {
+        for (; j < S; ++j) {
+            const int uu = (int)blockIdx.x + j * G;
+            if (uu >= p.num_units) break;
+            issue_unit_uncut<C, kModeSampled>(p, uu, j, smem);
+        }
+    }
+    j = __shfl_sync(0xffffffffu, j, 0);
+    if (first_records_by_consumers(p)) {
+        named_barrier_arrive(2, (uint32_t)(S + 1) * 32u);
+    } else {
+        for (int t = 0; t < j; ++t) {
+            const int uu = (int)blockIdx.x + t * G;
+            const tr_aug_param r = sample_record_warp(p.spec, uu / p.bands, lane);
+            if (lane == 0) publish_unit(p, uu, t, smem, r);
+        }
+    }
+    return j;
+}
 
 // Warp 0 is the producer: its lane 0 fills stage s = j % S with the CTA's
 // j-th unit once the consumers have released the stage (empty[s]), counting
@@ -1145,7 +1222,7 @@ constexpr int tiled_min_blocks() {
     return (ODD && LAYOUT == TR_LAYOUT_NCHW && Group<C>::P * (OUT_F16 ? 2 : 4) == 16) ? 4 : 1;
 }
 
-template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
+template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD, int MODE>
 __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CROP, ODD>()))
     tiled_kernel(const __grid_constant__ TiledParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1183,10 +1260,11 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
 
     if (threadIdx.x < 32) {
         // The producer: lane 0 waits on barriers, issues copies, takes
-        // tickets and loads the records; the other lanes leave (with hints
-        // bit 21 they first help to sample the CTA's first records).
-        const bool self_sample = !CROP && !ODD && overlapped && (p.hints & 512) && (p.hints & 2097152);
-        if (threadIdx.x != 0 && !self_sample) return;
+        // tickets and loads the records; the other lanes leave (after the
+        // first records of a sampled launch).
+        int j = 0;
+        if constexpr (MODE == kModeSampled) j = first_bands_sampled<C>(p, smem);
+        if (threadIdx.x != 0) return;
         const int G = gridDim.x;
         const int ngroups = min(kTicketGroups, G);   // every group must have a CTA
         const int group = (int)blockIdx.x % ngroups;
@@ -1195,7 +1273,7 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         // requested together, ahead of the wait for the stage they go to
         int2 org = make_int2(0, 0);
         auto unit_record = [&](int u) {
-            const tr_aug_param r = image_record(p, u / p.bands);
+            const tr_aug_param r = image_record<MODE>(p, u / p.bands);
             if (CROP && p.crop != nullptr) {
                 org.x = p.crop[2 * (size_t)(u / p.bands)];
                 org.y = p.crop[2 * (size_t)(u / p.bands) + 1];
@@ -1221,12 +1299,11 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         // 256x224x224x3 than waiting for the record
         const bool early0 = !CROP && !ODD && !recdep && !(p.hints & 32) && u < p.num_units;
         if (!early0 && !recdep && u < p.num_units) a = unit_record(u);
-        int j = 0;
         bool ok = true;
         bool waited = !overlapped;   // the previous grid has completed
-        if (recdep && self_sample) {
-            j = first_units_self_sampled<C>(p, smem, S, G);
-            if (threadIdx.x != 0) return;
+        if (MODE == kModeSampled) {
+            // the first S bands and their records are under way; the rest
+            // of the records are the sampler's, readable after the wait
             grid_dependency_wait();
             waited = true;
             if (!(p.hints & 8)) grid_launch_dependents();
@@ -1238,7 +1315,7 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
             for (; j < S; ++j) {
                 const int uu = (int)blockIdx.x + j * G;
                 if (uu >= p.num_units) break;
-                issue_unit_uncut<C>(p, uu, j, smem);
+                issue_unit_uncut<C, MODE>(p, uu, j, smem);
             }
             grid_dependency_wait();
             waited = true;
@@ -1263,13 +1340,13 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
                 break;
             }
             if (j == 0 && early0) {
-                issue_unit_uncut<C>(p, u, s, smem);
+                issue_unit_uncut<C, MODE>(p, u, s, smem);
                 a = unit_record(u);
                 publish_unit(p, u, s, smem, a);
             } else {
                 // a CTA's first S bands are copied whole (measured faster:
                 // they are the ramp every launch starts with)
-                issue_unit<C, CROP, ODD>(p, u, s, smem, a, (p.hints & 2048) || j >= S, org);
+                issue_unit<C, CROP, ODD, MODE>(p, u, s, smem, a, (p.hints & 2048) || j >= S, org);
             }
             // the next unit and its record: requested now, used after the
             // next empty wait
@@ -1282,33 +1359,14 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
                 if (!(p.hints & 8)) grid_launch_dependents();
             }
         }
-        {
-            if (!waited) grid_dependency_wait();
-            grid_launch_dependents();
-            if (!ok) {
-                atomicOr(&g_device_status, kStatusTimeout);
-            } else if (p.ws != nullptr) {
-                __threadfence();
-                if (atomicAdd(p.ws + kDoneWord, 1u) == (unsigned)G - 1) {
-                    for (int g = 0; g < kTicketGroups; ++g) p.ws[g * kTicketStride] = 0;
-                    p.ws[kDoneWord] = 0;
-                    __threadfence();
-                }
-            }
-            // The bands in flight must land before this thread leaves
-            // (bounded).  Fill k's phase is the latest of its stage only if no
-            // later fill used the stage: after a normal end the end mark took
-            // stage j % S, so fill j - S is done and superseded.
-            for (int k = max(0, ok ? j - S + 1 : j - S); k < j; ++k) {
-                if (!mbar_wait_bounded(full0 + 8u * (k % S), (uint32_t)(k / S) & 1u)) {
-                    atomicOr(&g_device_status, kStatusTimeout);
-                    break;
-                }
-            }
-        }
+        producer_finish(p, full0, j, S, ok, waited);
         return;
     }
 
+    if constexpr (MODE == kModeSampled) {
+        const int w = (int)(threadIdx.x >> 5) - 1;
+        if (first_records_by_consumers(p) && w < S) consumer_first_record(p, smem, w);
+    }
     const int tid = threadIdx.x - 32;
     const int nthr = blockDim.x - 32;
     const bool storer = (tid == 0);
@@ -1318,7 +1376,7 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         const bool ok = mbar_wait_bounded(full0 + 8u * s, (uint32_t)(i / S) & 1u);
         const UnitRec rec = recs[s];
         uint8_t* ob = sout + (size_t)(i & 1) * p.out_stage;
-        if (ok) compute_unit<C, OUT_F16, LAYOUT, CROP, ODD>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
+        if (ok) compute_unit<C, OUT_F16, LAYOUT, CROP, ODD, MODE>(p, sin + (size_t)s * p.in_stage, ob, rec, tid, nthr);
         fence_proxy_async_smem();
         // The store issued last iteration reads the other output tile, which
         // the next iteration overwrites: it must be done reading first.
@@ -1327,7 +1385,7 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         if (rec.rows == 0) break;   // the producer's end mark
         if (storer) {
             mbar_arrive(empty0 + 8u * s);
-            store_unit<C, OUT_F16, LAYOUT, ODD>(p, ob, rec);
+            store_unit<C, OUT_F16, LAYOUT, ODD, MODE>(p, ob, rec);
         }
     }
     if (storer) {
@@ -1498,35 +1556,41 @@ DeviceInfo device_info(int dev) {
 using TiledFn = void (*)(TiledParams);
 using GenericFn = void (*)(GenericParams);
 
-template <int C, int F16, bool CROP, bool ODD>
+template <int C, int F16, bool CROP, bool ODD, int MODE>
 TiledFn pick_tiled_layout(int layout) {
     switch (layout) {
-    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC, CROP, ODD>;
-    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW, CROP, ODD>;
-    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4, CROP, ODD>;
+    case TR_LAYOUT_NHWC: return tiled_kernel<C, F16, TR_LAYOUT_NHWC, CROP, ODD, MODE>;
+    case TR_LAYOUT_NCHW: return tiled_kernel<C, F16, TR_LAYOUT_NCHW, CROP, ODD, MODE>;
+    default: return tiled_kernel<C, F16, TR_LAYOUT_NHWC4, CROP, ODD, MODE>;
     }
 }
 
-template <int C, bool CROP, bool ODD>
+template <int C, bool CROP, bool ODD, int MODE>
 TiledFn pick_tiled_dtype(int f16, int layout) {
-    return f16 ? pick_tiled_layout<C, 1, CROP, ODD>(layout) : pick_tiled_layout<C, 0, CROP, ODD>(layout);
+    return f16 ? pick_tiled_layout<C, 1, CROP, ODD, MODE>(layout) : pick_tiled_layout<C, 0, CROP, ODD, MODE>(layout);
 }
 
-template <bool CROP, bool ODD>
+template <bool CROP, bool ODD, int MODE>
 TiledFn pick_tiled_c(int C, int f16, int layout) {
     switch (C) {
-    case 1: return pick_tiled_dtype<1, CROP, ODD>(f16, layout);
-    case 2: return pick_tiled_dtype<2, CROP, ODD>(f16, layout);
-    case 3: return pick_tiled_dtype<3, CROP, ODD>(f16, layout);
-    default: return pick_tiled_dtype<4, CROP, ODD>(f16, layout);
+    case 1: return pick_tiled_dtype<1, CROP, ODD, MODE>(f16, layout);
+    case 2: return pick_tiled_dtype<2, CROP, ODD, MODE>(f16, layout);
+    case 3: return pick_tiled_dtype<3, CROP, ODD, MODE>(f16, layout);
+    default: return pick_tiled_dtype<4, CROP, ODD, MODE>(f16, layout);
     }
 }
 
 // odd: compact sources whose rows (or NCHW output rows, or the output
-// pointer) are not 16-byte aligned
-TiledFn pick_tiled(int C, int f16, int layout, bool crop, bool odd) {
-    if (crop) return pick_tiled_c<true, false>(C, f16, layout);
-    return odd ? pick_tiled_c<false, true>(C, f16, layout) : pick_tiled_c<false, false>(C, f16, layout);
+// pointer) are not 16-byte aligned.  Several batches: compact sources only;
+// records made in the kernel: compact sources with aligned rows only.
+TiledFn pick_tiled(int C, int f16, int layout, bool crop, bool odd, int mode) {
+    if (crop) return pick_tiled_c<true, false, kModeBatch>(C, f16, layout);
+    if (mode == kModeSampled) return pick_tiled_c<false, false, kModeSampled>(C, f16, layout);
+    if (mode == kModeBatches)
+        return odd ? pick_tiled_c<false, true, kModeBatches>(C, f16, layout)
+                   : pick_tiled_c<false, false, kModeBatches>(C, f16, layout);
+    return odd ? pick_tiled_c<false, true, kModeBatch>(C, f16, layout)
+               : pick_tiled_c<false, false, kModeBatch>(C, f16, layout);
 }
 
 template <int C, int F16>
@@ -1904,7 +1968,10 @@ int setup_tiled(const LaunchArgs& a, TiledSetup* t) {
     // compact sources whose rows, NCHW output rows or output pointer are
     // not 16-byte aligned take the odd-row form of the kernel
     const bool odd = !crop && !tiled_aligned(a.src, a.dst, a.W, a.C, f16, a.out_layout);
-    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop, odd);
+    const int mode = a.sample_in_kernel ? kModeSampled : a.batch_images > 0 ? kModeBatches : kModeBatch;
+    if (mode == kModeSampled && (crop || odd || !a.overlap_prev || !a.records_from_prev))
+        return TR_ERR_NOT_SUPPORTED;
+    const TiledFn fn = pick_tiled(a.C, f16, a.out_layout, crop, odd, mode);
     TiledPlan pl;
     if (crop) {
         pl = plan_tiled_crop(a.H, a.W, a.C, f16, a.out_layout, di.smem_optin, di.smem_per_sm, di.smem_reserved,
@@ -2020,20 +2087,14 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
-    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000 | 1048576);
+    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000 | 1048576 | 4194304);
     // copies may start before the previous grid completes; records that grid
     // wrote are read after it (compact aligned sources; the crop and
     // odd-row forms then wait for it before they touch memory)
     if (a.overlap_prev && !(a.records_from_prev && (crop || odd))) p.hints |= 256;
     if (a.overlap_prev && a.records_from_prev && !crop && !odd) p.hints |= 512;
-    // the sampler's settings are known: the first records are made in the
-    // kernel (tr_tune_tiled flags bit 21 reads them from the sampler instead)
-    if (a.spec != nullptr) {
-        p.spec = *a.spec;
-        if (!(tflags & 2097152)) p.hints |= 2097152;
-    } else {
-        p.spec = SampleSpec();
-    }
+    // first records made in the kernel: the sampler's settings
+    p.spec = a.sample_in_kernel ? *a.spec : SampleSpec();
     p.ws = static_cast<unsigned int*>(a.workspace);
     for (int c = 0; c < 4; ++c) {
         p.base[c] = 8388608.0f + a.shift[c];   // exact: |shift| <= 2^20
@@ -2154,6 +2215,25 @@ int tiled_geometry(const LaunchArgs& a, TiledGeometry* g) {
 }
 
 int launch(const LaunchArgs& a, int variant) {
+    if (a.spec != nullptr && !a.records_from_prev) {
+        // Records made on the GPU: the sampler writes them first, and the
+        // kernel reads them in stream order.  A tiled launch in its aligned
+        // compact form that overlaps the kernel before it also makes its
+        // CTAs' first records itself (the same bits), so that it need not
+        // wait for the sampler, hence for that kernel, before converting
+        // (tr_tune_tiled flags bit 21 turns this off).
+        int rc = launch_sampler(*a.spec, a.N, a.records_out, a.stream, a.overlap_prev);
+        if (rc != TR_OK) return rc;
+        LaunchArgs b = a;
+        b.aug = a.records_out;
+        b.records_from_prev = true;
+        const int f16 = (a.out_dtype == TR_OUT_F16);
+        b.sample_in_kernel = variant == TR_VARIANT_TILED && a.overlap_prev && !a.crop_src && a.batch_images == 0 &&
+                             tiled_aligned(a.src, a.dst, a.W, a.C, f16, a.out_layout) &&
+                             !(g_flags.load(std::memory_order_relaxed) & 2097152);
+        if (!b.sample_in_kernel) b.spec = nullptr;
+        return launch(b, variant);
+    }
     if (variant == TR_VARIANT_TILED) return launch_tiled(a);
     return launch_generic(a);
 }

@@ -45,9 +45,13 @@ struct LaunchArgs {
     // device sampler): with overlap_prev the tiled kernel requests its first
     // bands before that kernel has completed and reads the records after
     bool records_from_prev = false;
-    // with records_from_prev: the sampler's settings (the tiled kernel then
-    // makes a CTA's first records itself, bit-identical), or null
+    // records to be made on the GPU (tr_fused_norm_sampled): the sampler's
+    // settings and the N records' destination; launch() runs the sampler
+    // first and the kernel on its output (records_from_prev), an overlapped
+    // tiled launch making its CTAs' first records itself (sample_in_kernel)
     const SampleSpec* spec = nullptr;
+    tr_aug_param* records_out = nullptr;
+    bool sample_in_kernel = false;
     // windows of a strided source (tr_fused_norm_crop); otherwise a compact
     // NHWC source of H x W images
     bool crop_src = false;

@@ -391,9 +391,13 @@ int tr_fused_norm_sampled(const uint8_t* src_u8, void* dst, int N, int H, int W,
  * With TR_LAUNCH_OVERLAP_PREVIOUS the caller promises that the kernel before
  * this call in the stream uses none of src, dst, d_records and workspace: the
  * sampler then writes the records while that kernel drains, and the fused
- * kernel requests its first bands at once and reads the records once the
- * sampler (which itself completes only after the previous kernel) is done.
- * The crop and odd-row forms wait for the sampler before they touch memory. */
+ * kernel requests its first bands at once.  Its records become readable only
+ * when the sampler has completed, which is after the previous kernel; so in
+ * the TILED kernel's aligned form each CTA makes the records of its first
+ * bands itself (consumer warps, in parallel, with the sampler's steps: the
+ * same bits) and converts them while the previous kernel drains, and reads
+ * the later records from the sampler's output.  The crop and odd-row forms
+ * wait for the sampler before they touch memory.                           */
 int tr_fused_norm_sampled_ex(const uint8_t* src_u8, void* dst, int N, int H, int W, int C,
                              const float* mean, const float* std, uint64_t seed, uint64_t offset,
                              const tr_aug_sampling* sampling, tr_aug_param* d_records, uint64_t* next_offset,
@@ -641,9 +645,11 @@ int tr_device_status(int* flags, int clear);
  *                    (tr_fused_norm_sampled_ex with TR_LAUNCH_OVERLAP_PREVIOUS):
  *                    bit 21 makes each CTA read its first bands' records from
  *                    the sampler's output once the sampler has completed
- *                    (default: its producer warp makes them with the
- *                    sampler's steps, the same bits, so those bands convert
- *                    while the kernel before drains);
+ *                    (default: the CTA makes them with the sampler's steps,
+ *                    the same bits, so those bands convert while the kernel
+ *                    before drains), bit 22 has the producer warp make them
+ *                    one after another (default: one consumer warp each, in
+ *                    parallel);
  *                    crop sources: bit 8 reads 16-byte chunks even where 32-byte
  *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion;
  *                    compact sources: erased source spans are left out of a

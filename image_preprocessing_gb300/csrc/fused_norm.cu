@@ -1020,7 +1020,7 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
 
 template <int C, int OUT_F16, int LAYOUT, bool ODD, int MODE>
 __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* sout,
-                                           const UnitRec& rec) {
+                                           const UnitRec& rec, int lane) {
     constexpr int OB = OUT_F16 ? 2 : 4;
     const uint32_t src = smem_u32(sout);
     // Output lines go to L2 evict-first by default (a streamed result); a
@@ -1034,7 +1034,10 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
     };
     if (ODD) {
         // per plane (NCHW) or for the band: the 16-byte aligned middle by a
-        // bulk store, the unaligned first and last bytes element by element
+        // bulk store (lane 0), the unaligned first and last bytes element by
+        // element, spread over the storer's warp (up to 14 elements a plane:
+        // one thread storing them all kept the other consumers waiting at
+        // the next band's barrier)
         constexpr int OC = (LAYOUT == TR_LAYOUT_NHWC4) ? 4 : C;
         constexpr int NP = (LAYOUT == TR_LAYOUT_NCHW) ? C : 1;
         const ImageRef im = image_ref<MODE>(p, rec.n);
@@ -1061,20 +1064,19 @@ __device__ __forceinline__ void store_unit(const TiledParams& p, const uint8_t* 
                                     (LAYOUT == TR_LAYOUT_NCHW ? (size_t)(c + 1) * p.plane_bytes : p.out_stage),
                             13))
                 continue;
-            for (uint32_t i = 0; i < head; i += OB) {
+            const uint32_t nh = head / OB, ne = nh + (bytes - head - mid) / OB;
+            for (uint32_t k = (uint32_t)lane; k < ne; k += 32u) {
+                const uint32_t i = k < nh ? k * OB : head + mid + (k - nh) * OB;
                 if (OUT_F16) *reinterpret_cast<uint16_t*>(g + i) = *reinterpret_cast<const uint16_t*>(t + i);
                 else *reinterpret_cast<uint32_t*>(g + i) = *reinterpret_cast<const uint32_t*>(t + i);
             }
-            for (uint32_t i = head + mid; i < bytes; i += OB) {
-                if (OUT_F16) *reinterpret_cast<uint16_t*>(g + i) = *reinterpret_cast<const uint16_t*>(t + i);
-                else *reinterpret_cast<uint32_t*>(g + i) = *reinterpret_cast<const uint32_t*>(t + i);
-            }
-            if (mid > 0 && TRFN_CHECK(((uintptr_t)(g + head) & 15u) == 0 &&
-                                          ((src + (uint32_t)(c * p.plane_bytes + sh + head)) & 15u) == 0,
-                                      14))
+            if (lane == 0 && mid > 0 &&
+                TRFN_CHECK(((uintptr_t)(g + head) & 15u) == 0 &&
+                               ((src + (uint32_t)(c * p.plane_bytes + sh + head)) & 15u) == 0,
+                           14))
                 put(g + head, src + (uint32_t)(c * p.plane_bytes + sh + head), mid);
         }
-        bulk_commit();
+        if (lane == 0) bulk_commit();
         return;
     }
     const ImageRef im = image_ref<MODE>(p, rec.n);
@@ -1370,6 +1372,9 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
     const int tid = threadIdx.x - 32;
     const int nthr = blockDim.x - 32;
     const bool storer = (tid == 0);
+    // the odd-row form's stores take the storer's whole warp (element stores
+    // at the bands' unaligned edges); lane 0 issues the bulk stores
+    const bool store_warp = ODD ? (tid < 32) : storer;
     bool aborted = false;
     for (int i = 0;; ++i) {
         const int s = i % S;
@@ -1383,9 +1388,9 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         if (storer) bulk_wait_read<0>();
         if (named_barrier_or((uint32_t)nthr, !ok)) { aborted = true; break; }
         if (rec.rows == 0) break;   // the producer's end mark
-        if (storer) {
-            mbar_arrive(empty0 + 8u * s);
-            store_unit<C, OUT_F16, LAYOUT, ODD, MODE>(p, ob, rec);
+        if (store_warp) {
+            if (storer) mbar_arrive(empty0 + 8u * s);
+            store_unit<C, OUT_F16, LAYOUT, ODD, MODE>(p, ob, rec, tid);
         }
     }
     if (storer) {

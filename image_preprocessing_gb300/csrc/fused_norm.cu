@@ -307,6 +307,7 @@ struct TiledParams {
     int num_units;         // N * bands
     int gpr;               // groups per row, W / P
     uint64_t gpr_inv;      // ceil(2^32 / gpr): g / gpr == (g * gpr_inv) >> 32 for g, gpr < 2^16
+    uint64_t wc_inv;       // ceil(2^32 / (W*C)): e / (W*C) the same way, for e * W*C < 2^31
     uint64_t src_floor16;  // rows not a multiple of 16 bytes: the source's bytes rounded down to 16
     uint32_t in_stage;     // bytes per input stage (R*W*C, multiple of 16)
     uint32_t out_stage;    // bytes per output stage
@@ -320,7 +321,8 @@ struct TiledParams {
                            // stores (7), erased-span rule (11, 12-15); set by the launch:
                            // overlap the previous grid (8), records written by it (9),
                            // odd-row element stores (10), plain order of 16-byte
-                           // odd-row NCHW plane runs (20), a sampled launch's first
+                           // odd-row NCHW plane runs (20), odd-row NHWC groups aligned
+                           // to the output tile (24), a sampled launch's first
                            // records made by the producer warp (22)
     float base[4];         // 2^23 + shift_c (see byte_minus_shift)
     float scale[4];
@@ -935,11 +937,167 @@ __device__ __forceinline__ void store_group_odd(const TiledParams& p, uint8_t* s
     }
 }
 
+// The odd-row form's NHWC output with 1 or 3 channels (hints bit 24).  A
+// band's output is one run of rows*W*C elements, element e at tile offset
+// sh + e*OB, where sh (below 16) follows the band's global alignment, and the
+// unflipped source byte of element e is the band's byte e.  Pixel-aligned
+// groups (8 pixels, 24 elements, or 16 grayscale pixels) therefore start at
+// arbitrary bytes of the tile, and their outputs had to be moved into its
+// 16-byte frame in registers (19 % of the kernel's time at 256x299x299x3 ->
+// f16).  Here group g takes the elements [g*GE - psi, g*GE - psi + GE), psi
+// in [0, GE) chosen per band so that every group starts both on a pixel
+// (psi = 0 mod C) and on a 16-byte boundary of the tile (psi = (sh/OB) mod
+// (16/OB)); GE is a multiple of both.  A group's outputs leave as aligned
+// 16-byte stores, its conversion is the pixel groups' own (convert_group),
+// and only the source side changes: unflipped, the group's GE source bytes
+// are contiguous even across rows; flipped within one row, they are the
+// mirrored run of its P pixels; flipped across two rows, the two rows'
+// mirrored runs, the first row's pixels in the run's upper bytes.  Elements
+// before the band start fall before sh and elements past its end into the
+// tile's slack: neither is stored to global memory.
+
+// NWD words of the bytes starting at q (any alignment): aligned 4-byte loads
+// and funnel shifts.
+template <int NWD>
+__device__ __forceinline__ void load_bytes_at(const uint8_t* q, uint32_t (&w)[NWD]) {
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>((uintptr_t)q & ~(uintptr_t)3);
+    const uint32_t sh = (uint32_t)((uintptr_t)q & 3u) * 8u;
+    uint32_t raw[NWD + 1];
+#pragma unroll
+    for (int i = 0; i <= NWD; ++i) raw[i] = wp[i];
+#pragma unroll
+    for (int i = 0; i < NWD; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
+// Checked-build guard of a shared-memory read of `bytes` at q.
+__device__ __forceinline__ bool smem_read_ok(const TiledParams& p, const uint8_t* q, int bytes, int site) {
+    (void)p; (void)q; (void)bytes; (void)site;
+    return TRFN_CHECK(q >= trfn_dyn_smem && q + bytes <= trfn_dyn_smem + p.smem_bytes, site);
+}
+
+template <int C, int OUT_F16>
+__device__ __forceinline__ void odd_nhwc_group(const TiledParams& p, const uint8_t* sin, uint8_t* tile0,
+                                               const uint8_t* tile_end, const UnitRec& rec, int g, int psi,
+                                               int E, int off_in) {
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    constexpr int P = Group<C>::P;
+    constexpr int GE = P * C;                    // elements (source bytes) of a group
+    constexpr int NW = GE / 4;
+    constexpr int NCH = GE * OB / 16;            // 16-byte output chunks
+    constexpr int EPC = 16 / OB;                 // elements per chunk
+    const int WC = p.W * C;
+    const int e0 = g * GE - psi;
+    // row of the last element, or the band's last row when the group runs
+    // past the band (those elements are not stored)
+    const int r1 = min((int)(((uint64_t)(uint32_t)(e0 + GE - 1) * p.wc_inv) >> 32), rec.rows - 1);
+    const int split = r1 * WC - e0;              // elements k < split lie in row r1 - 1
+    const int split_px = split > 0 ? split / C : 0;   // pixels of the group in row r1 - 1
+    const bool flip = (rec.flags & 1) != 0;
+    uint32_t w[NW];
+    if (!flip) {
+        const uint8_t* q = sin + off_in + e0;
+        if (smem_read_ok(p, q, 4 * (NW + 1), 15)) load_bytes_at<NW>(q, w);
+        else for (int i = 0; i < NW; ++i) w[i] = 0u;
+    } else {
+        // row r1's mirrored run: the group's pixels x = e/C - r1*W (the first
+        // ones negative when the group starts in row r1 - 1) take the row's
+        // pixels W-1-x, i.e. the P pixels from W - x0 - P on, reversed
+        const int x0b = (e0 - r1 * WC) / C;   // exact: e0 - r1*WC is a multiple of C
+        const uint8_t* qb = sin + off_in + r1 * WC + C * (p.W - x0b - P);
+        if (smem_read_ok(p, qb, 4 * (NW + 1), 16)) load_bytes_at<NW>(qb, w);
+        else for (int i = 0; i < NW; ++i) w[i] = 0u;
+        if (split_px > 0 && r1 > 0) {
+            // the pixels k < split_px lie in row r1 - 1 (x = x0b + W + k):
+            // its mirrored run fills the run's bytes from C*(P - split_px) on
+            uint32_t wa[NW];
+            const uint8_t* qa = qb - WC - C * p.W;   // row r1 - 1, first pixel x0b + W
+            if (smem_read_ok(p, qa, 4 * (NW + 1), 17)) load_bytes_at<NW>(qa, wa);
+            else for (int i = 0; i < NW; ++i) wa[i] = 0u;
+            const int thr = C * (P - split_px);   // bytes [thr, GE) from row r1 - 1
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                const int m = thr - 4 * i;      // bytes of word i from row r1
+                if (m <= 0) w[i] = wa[i];
+                else if (m < 4) w[i] = __byte_perm(w[i], wa[i], m == 1 ? 0x7650u : m == 2 ? 0x7610u : 0x7210u);
+            }
+        }
+    }
+    float v[GE];
+    if (flip) convert_group<C, true>(w, p.base, p.scale, p.bias, v);
+    else convert_group<C, false>(w, p.base, p.scale, p.bias, v);
+    // erased pixels: those of row r1 - 1 ([0, split_px)) and of row r1
+    if (rec.erow_lo < rec.erow_hi) {
+        const int ya = rec.y_begin + r1 - 1, yb = ya + 1;
+        const int xa = (e0 - (r1 - 1) * WC) / C;   // pixel x of group pixel 0 in row r1 - 1 (if any)
+        const int xb = (e0 - r1 * WC) / C;         // ... in row r1 (negative when it starts before)
+        int lo_a = 0, hi_a = 0, lo_b = 0, hi_b = 0;
+        if (split_px > 0 && ya >= rec.erow_lo && ya < rec.erow_hi) {
+            lo_a = max(rec.ecol_lo - xa, 0);
+            hi_a = min(rec.ecol_hi - xa, split_px);
+        }
+        if (yb >= rec.erow_lo && yb < rec.erow_hi) {
+            lo_b = max(rec.ecol_lo - xb, split_px);
+            hi_b = min(rec.ecol_hi - xb, P);
+        }
+        if (lo_a < hi_a || lo_b < hi_b) {
+#pragma unroll
+            for (int k = 0; k < GE; ++k) {
+                const int i = k / C;
+                if ((i >= lo_a && i < hi_a) || (i >= lo_b && i < hi_b)) v[k] = 0.0f;
+            }
+        }
+    }
+    uint8_t* o = tile0 + (size_t)g * GE * OB;
+#pragma unroll
+    for (int qc = 0; qc < NCH; ++qc) {
+        if (e0 + qc * EPC >= E) break;   // past the band (the tile's slack holds a chunk's overhang)
+        if (e0 + (qc + 1) * EPC <= 0) continue;   // wholly before the band (outside the tile)
+        uint4 ch;
+        if (OUT_F16) {
+            ch.x = pack_half2(v[8 * qc + 0], v[8 * qc + 1]);
+            ch.y = pack_half2(v[8 * qc + 2], v[8 * qc + 3]);
+            ch.z = pack_half2(v[8 * qc + 4], v[8 * qc + 5]);
+            ch.w = pack_half2(v[8 * qc + 6], v[8 * qc + 7]);
+        } else {
+            ch = make_uint4(__float_as_uint(v[4 * qc + 0]), __float_as_uint(v[4 * qc + 1]),
+                            __float_as_uint(v[4 * qc + 2]), __float_as_uint(v[4 * qc + 3]));
+        }
+        if (TRFN_CHECK(o + 16 * (qc + 1) <= tile_end && ((uintptr_t)(o + 16 * qc) & 15u) == 0, 18))
+            reinterpret_cast<uint4*>(o)[qc] = ch;
+    }
+}
+
+template <int C, int OUT_F16>
+__device__ __forceinline__ void odd_nhwc_band(const TiledParams& p, const uint8_t* sin, uint8_t* sout,
+                                              const UnitRec& rec, int tid, int nthr, uint32_t sh) {
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    constexpr int GE = Group<C>::P * C;
+    constexpr int EPC = 16 / OB;
+    const int phi = (int)((sh / OB) % EPC);
+    int psi = phi;   // psi = phi mod EPC and psi = 0 mod C, in [0, GE)
+    while (psi % C != 0) psi += EPC;
+    const int E = rec.rows * p.W * C;
+    const int off_in = rec.flags >> 8;
+    uint8_t* tile0 = sout + (sh - (uint32_t)phi * OB) - (psi - phi) * OB;
+    const uint8_t* tile_end = sout + p.out_stage;
+    const int ng = (E + psi + GE - 1) / GE;
+    for (int g = tid; g < ng; g += nthr) odd_nhwc_group<C, OUT_F16>(p, sin, tile0, tile_end, rec, g, psi, E, off_in);
+}
+
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD, int MODE>
 __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
                                              uint8_t* sout, const UnitRec& rec, int tid, int nthr) {
     constexpr int P = Group<C>::P;
     constexpr int GB = Group<C>::kBytes;
+    if constexpr (ODD && LAYOUT == TR_LAYOUT_NHWC && (C == 1 || C == 3)) {
+        if (p.hints & 16777216) {
+            // (the producer's end mark, rows = 0, carries no other valid
+            // field: nothing of it is read)
+            if (rec.rows > 0)
+                odd_nhwc_band<C, OUT_F16>(p, sin, sout, rec, tid, nthr, odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, 0));
+            return;
+        }
+    }
     const int L = p.W * C;
     const int groups = rec.rows * p.gpr;
     for (int g = tid; g < groups; g += nthr) {
@@ -1221,7 +1379,10 @@ __device__ __forceinline__ int first_bands_sampled(const TiledParams& p, uint8_t
 // here, against 61 without it, and measured 0.9 % faster at 256x224x224x3.)
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
 constexpr int tiled_min_blocks() {
-    return (ODD && LAYOUT == TR_LAYOUT_NCHW && Group<C>::P * (OUT_F16 ? 2 : 4) == 16) ? 4 : 1;
+    return ((ODD && LAYOUT == TR_LAYOUT_NCHW && Group<C>::P * (OUT_F16 ? 2 : 4) == 16) ||
+            (ODD && LAYOUT == TR_LAYOUT_NHWC && (C == 1 || C == 3)))
+               ? 4
+               : 1;
 }
 
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD, int MODE>
@@ -1815,9 +1976,12 @@ TiledPlan plan_tiled_r(int H, int W, int C, int f16, int layout, int smem_limit,
     for (;;) {
         const size_t in_stage = round_up((size_t)R * pitch + slack, 128);
         const size_t plane = odd ? round_up((size_t)R * W * ob + 16, 16) : (size_t)R * W * ob;
+        // odd rows: 16 bytes for the tile to follow the band's alignment,
+        // and 16 more for the overhang of the last 16-byte chunk of the
+        // aligned-output groups
         const size_t out_stage = !odd ? round_up((size_t)R * out_row, 128)
                                  : layout == TR_LAYOUT_NCHW ? round_up((size_t)C * plane, 128)
-                                                            : round_up((size_t)R * out_row + 16, 128);
+                                                            : round_up((size_t)R * out_row + 32, 128);
         const size_t smem = kHeaderBytes + stages * in_stage + 2 * out_stage;
         if (in_stage < (1u << 20) && smem <= (size_t)smem_limit && R <= 256) {
             pl.ok = true;
@@ -2088,6 +2252,7 @@ int launch_tiled(const LaunchArgs& a) {
         p.baug[k] = a.baug[k];
     }
     p.gpr_inv = ((1ull << 32) + (uint64_t)p.gpr - 1) / (uint64_t)p.gpr;
+    p.wc_inv = ((1ull << 32) + (uint64_t)a.W * a.C - 1) / ((uint64_t)a.W * a.C);
     p.in_stage = pl.in_stage;
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
@@ -2116,6 +2281,22 @@ int launch_tiled(const LaunchArgs& a) {
     // slower).  Those launches keep the element stores (tr_tune_tiled flags
     // bit 17 asks for the realignment regardless).
     if (odd && t.waves < kStreamMinBandsPerCta && !(tflags & 131072)) p.hints |= 1024;
+    // odd-row NHWC output with 1 or 3 channels, where each CTA streams
+    // enough bands for the register realignment above: groups aligned to the
+    // output tile instead (each row at least one group long; element indices
+    // small enough for the one-multiply row division).  GB300, waiting /
+    // overlapping launches: 256x299x299x3 -> f16 43.5 / 39.8 -> 37.3 / 34.5
+    // us, 256x227x227x3 28.5 / 24.6 -> 25.3 / 22.1, 256x299x299 grayscale
+    // 22.9 / 17.8 -> 20.3 / 15.9, binary32 the same; batches of 28x28
+    // images (element stores) were 6-8 % slower with it.  tr_tune_tiled
+    // flags bit 23 keeps the pixel-aligned groups.
+    {
+        const uint64_t wc = (uint64_t)a.W * a.C;
+        const uint64_t ge = (uint64_t)group_pixels(a.C) * a.C;
+        if (odd && a.out_layout == TR_LAYOUT_NHWC && (a.C == 1 || a.C == 3) && !(p.hints & 1024) && wc >= ge &&
+            ((uint64_t)pl.R * wc + ge) * wc < (1ull << 31) && !(tflags & 8388608))
+            p.hints |= 16777216;
+    }
 
     if (!check_cuda(launch_pdl((const void*)t.fn, (unsigned)t.grid, pl.threads, pl.smem, a.stream, &p),
                     "tiled kernel launch"))

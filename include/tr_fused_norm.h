@@ -636,7 +636,11 @@ int tr_device_status(int* flags, int clear);
  *                    each group's output bytes moved to the tile's 16-byte
  *                    frame in registers and written with 16-byte stores,
  *                    2/4/8-byte stores only at its ends), bit 17 uses that
- *                    realignment however few bands a CTA gets; bit 20 makes
+ *                    realignment however few bands a CTA gets (for NHWC
+ *                    output with 1 or 3 channels the groups are then laid on
+ *                    the output tile's 16-byte frame instead, a pixel and a
+ *                    chunk boundary at once, so no realignment is needed;
+ *                    bit 23 keeps the realigned pixel groups); bit 20 makes
  *                    the odd-row form store 16-byte binary16 NCHW plane runs
  *                    (2 or 3 channels) in plain element order (default: each
  *                    lane starts at word (lane / 8) % 4 of its run, so a

@@ -436,8 +436,9 @@ def test_odd_row_tiled_form(shape):
 def test_odd_row_full_size(dt, layout):
     """256 x 299x299x3 (Inception-sized rows of 897 bytes) through AUTO: the
     odd-row form with its default stores at a size where each CTA streams
-    many bands (register-realigned stores for binary16/binary32 NHWC and
-    binary32 NCHW), whole output against the oracle, guard bytes intact."""
+    many bands (groups laid on the output tile's 16-byte frame for binary16
+    and binary32 NHWC, register-realigned stores for binary32 NCHW), whole
+    output against the oracle, guard bytes intact."""
     N, H, W, C = 256, 299, 299, 3
     src = synth.pixels_uniform(299, N, H, W, C)
     aug, _ = oracle.sample_aug_params(2990, 0, N, H, W)
@@ -447,10 +448,12 @@ def test_odd_row_full_size(dt, layout):
 
 @pytest.mark.parametrize("shape", [(2, 17, 299, 3), (3, 9, 10, 1), (7, 3, 33, 3), (3, 2, 15, 4), (2, 11, 13, 2)])
 def test_odd_row_output_stores_same_bits(shape):
-    """The odd-row form's two ways of writing its output tile (16-byte
-    stores of register-realigned group outputs, forced by tr_tune_tiled flags
-    bit 17; element stores, bit 10) give the same bits in every layout and
-    type, with the output pointer on and off 16."""
+    """The odd-row form's ways of writing its output tile give the same bits
+    in every layout and type, with the output pointer on and off 16: groups
+    laid on the tile's 16-byte frame (NHWC with 1 or 3 channels) or 16-byte
+    stores of register-realigned group outputs (the rest), forced at any size
+    by tr_tune_tiled flags bit 17; the realigned pixel groups for every
+    layout (bits 17 and 23); element stores (bit 10)."""
     N, H, W, C = shape
     src = synth.coordinate_image(N, H, W, C)
     mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
@@ -460,7 +463,7 @@ def test_odd_row_output_stores_same_bits(shape):
         for layout in (NHWC, NCHW, NHWC4):
             for dst_off in (0, 2 if dt == F16 else 4, 6 if dt == F16 else 12):
                 outs = []
-                for fl in (STREAMS, 1024):
+                for fl in (STREAMS, STREAMS | (1 << 23), 1024):
                     try:
                         trfn.tr_tune_tiled(0, 0, 0, fl)
                         got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED, dst_offset=dst_off)
@@ -468,6 +471,7 @@ def test_odd_row_output_stores_same_bits(shape):
                         trfn.tr_tune_tiled(0, 0, 0, 0)
                     outs.append(got)
                 assert np.array_equal(outs[0], outs[1]), (dt, layout, dst_off)
+                assert np.array_equal(outs[0], outs[2]), (dt, layout, dst_off)
     assert trfn.tr_device_status() == 0
 
 

@@ -1318,6 +1318,27 @@ __device__ __forceinline__ bool first_records_by_consumers(const TiledParams& p)
     return p.stages <= (int)(blockDim.x >> 5) - 1 && !(p.hints & 4194304);
 }
 
+// Where the consumer warps number at least 2S, warps S+1..2S make the records
+// of the CTA's units S..2S-1 at the same time, into the unit-record slots
+// S..2S-1 that the stage ring leaves free, and arrive on the barrier slot of
+// stage S (also outside the ring).  The CTA's first 2S units are then static,
+// and once the producer's wait for the sampler (hence for the kernel before
+// it) returns, its next S bands are requested without a read of the
+// sampler's output on the way (tr_tune_tiled flags bit 25 keeps S).  The
+// wait itself stays after the first S bands: taken later, it also releases
+// the next kernel in the stream later, which measured slower.
+// Returns the count of units whose records the kernel makes.
+__device__ __forceinline__ int sampled_prefix(const TiledParams& p) {
+    const int S = p.stages;
+    const bool twice = first_records_by_consumers(p) && 2 * S <= (int)(blockDim.x >> 5) - 1 &&
+                       2 * S <= kMaxStages && !(p.hints & 33554432);
+    return twice ? 2 * S : S;
+}
+
+__device__ __forceinline__ tr_aug_param* later_record_slot(uint8_t* smem, int j) {
+    return reinterpret_cast<tr_aug_param*>(smem + kRecOffset + (size_t)j * sizeof(UnitRec));
+}
+
 __device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -1334,6 +1355,19 @@ __device__ __forceinline__ void consumer_first_record(const TiledParams& p, uint
     if (uu < p.num_units) r = sample_record_warp(p.spec, uu / p.bands, lane);
     named_barrier_sync(2, (uint32_t)(p.stages + 1) * 32u);
     if (uu < p.num_units && lane == 0) publish_unit(p, uu, w, smem, r);
+}
+
+// Consumer warp w, S <= w < 2S: the record of the CTA's w-th unit, left in
+// slot w for the producer.
+__device__ __forceinline__ void consumer_later_record(const TiledParams& p, uint8_t* smem, int w) {
+    const int lane = (int)(threadIdx.x & 31u);
+    const int uu = (int)blockIdx.x + w * (int)gridDim.x;
+    tr_aug_param r = {0, 0, 0, 0, 0};
+    if (uu < p.num_units) r = sample_record_warp(p.spec, uu / p.bands, lane);
+    if (lane == 0) {
+        *later_record_slot(smem, w) = r;
+        mbar_arrive(smem_u32(smem) + 8u * (uint32_t)p.stages);
+    }
 }
 
 // The producer warp's start in such a launch (all 32 lanes): lane 0
@@ -1401,6 +1435,9 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
             mbar_init(full0 + 8u * s, 1);
             mbar_init(empty0 + 8u * s, 1);
         }
+        if constexpr (MODE == kModeSampled) {
+            if (sampled_prefix(p) > S) mbar_init(full0 + 8u * S, (uint32_t)(sampled_prefix(p) - S));
+        }
         fence_mbar_init();
     }
     __syncthreads();
@@ -1431,7 +1468,10 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         const int G = gridDim.x;
         const int ngroups = min(kTicketGroups, G);   // every group must have a CTA
         const int group = (int)blockIdx.x % ngroups;
-        const int n_dyn = max(0, p.num_units - S * G);   // units handed out by tickets
+        // the CTA's first SP units are static: S, or 2S in a sampled launch
+        // whose consumers make that many records
+        const int SP = (MODE == kModeSampled) ? sampled_prefix(p) : S;
+        const int n_dyn = max(0, p.num_units - SP * G);   // units handed out by tickets
         // unit u's record and, for crop sources, its image's window origin:
         // requested together, ahead of the wait for the stage they go to
         int2 org = make_int2(0, 0);
@@ -1443,12 +1483,12 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
             }
             return r;
         };
-        // the CTA's jn-th unit: static for the first S (or without a
+        // the CTA's jn-th unit: static for the first SP (or without a
         // workspace), else from this CTA's ticket counter
         auto next_unit = [&](int jn) {
-            if (p.ws == nullptr || jn < S) return (int)blockIdx.x + jn * G;
+            if (p.ws == nullptr || jn < SP) return (int)blockIdx.x + jn * G;
             const int k = group + (int)atomicAdd(p.ws + group * kTicketStride, 1u) * ngroups;
-            return k < n_dyn ? S * G + k : p.num_units;
+            return k < n_dyn ? SP * G + k : p.num_units;
         };
         int u = blockIdx.x;
         tr_aug_param a = {0, 0, 0, 0, 0};
@@ -1465,13 +1505,23 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         bool ok = true;
         bool waited = !overlapped;   // the previous grid has completed
         if (MODE == kModeSampled) {
-            // the first S bands and their records are under way; the rest
-            // of the records are the sampler's, readable after the wait
+            // the first S bands and their records are under way; units S..SP-1
+            // take the records the consumers make, the rest the sampler's,
+            // readable after the wait
+            u = next_unit(j);
+            const bool made = j < SP && u < p.num_units;
+            if (made) {
+                if (mbar_wait_bounded(full0 + 8u * S, 0u)) {
+                    a = *later_record_slot(smem, j);
+                } else {
+                    atomicOr(&g_device_status, kStatusTimeout);
+                    u = p.num_units;
+                }
+            }
             grid_dependency_wait();
             waited = true;
             if (!(p.hints & 8)) grid_launch_dependents();
-            u = next_unit(j);
-            if (u < p.num_units) a = unit_record(u);
+            if (!made && u < p.num_units) a = unit_record(u);
         } else if (recdep) {
             // the first S units are blockIdx.x + t * G (no array: it would
             // live in local memory)
@@ -1514,12 +1564,19 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
             // the next unit and its record: requested now, used after the
             // next empty wait
             u = next_unit(j + 1);
-            if (u < p.num_units) a = unit_record(u);
-            if (!waited && j + 1 >= S) {
-                // overlapped launch: its first S bands are in flight
-                grid_dependency_wait();
-                waited = true;
-                if (!(p.hints & 8)) grid_launch_dependents();
+            if constexpr (MODE == kModeSampled) {
+                // a record the consumers made (their barrier was passed
+                // above), else the sampler's (the wait was taken above)
+                if (j + 1 < SP) a = *later_record_slot(smem, j + 1);
+                else if (u < p.num_units) a = unit_record(u);
+            } else {
+                if (u < p.num_units) a = unit_record(u);
+                if (!waited && j + 1 >= S) {
+                    // overlapped launch: its first S bands are in flight
+                    grid_dependency_wait();
+                    waited = true;
+                    if (!(p.hints & 8)) grid_launch_dependents();
+                }
             }
         }
         producer_finish(p, full0, j, S, ok, waited);
@@ -1528,7 +1585,10 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
 
     if constexpr (MODE == kModeSampled) {
         const int w = (int)(threadIdx.x >> 5) - 1;
-        if (first_records_by_consumers(p) && w < S) consumer_first_record(p, smem, w);
+        if (first_records_by_consumers(p)) {
+            if (w < S) consumer_first_record(p, smem, w);
+            else if (w < sampled_prefix(p)) consumer_later_record(p, smem, w);
+        }
     }
     const int tid = threadIdx.x - 32;
     const int nthr = blockDim.x - 32;
@@ -2257,7 +2317,8 @@ int launch_tiled(const LaunchArgs& a) {
     p.out_stage = pl.out_stage;
     p.plane_bytes = pl.plane_bytes;
     p.stages = pl.stages;
-    p.hints = g_flags.load(std::memory_order_relaxed) & (255 | 1024 | 2048 | 0xF000 | 1048576 | 4194304);
+    p.hints = g_flags.load(std::memory_order_relaxed) &
+              (255 | 1024 | 2048 | 0xF000 | 1048576 | 4194304 | 33554432);
     // copies may start before the previous grid completes; records that grid
     // wrote are read after it (compact aligned sources; the crop and
     // odd-row forms then wait for it before they touch memory)

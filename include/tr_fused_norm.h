@@ -653,7 +653,11 @@ int tr_device_status(int* flags, int clear);
  *                    the same bits, so those bands convert while the kernel
  *                    before drains), bit 22 has the producer warp make them
  *                    one after another (default: one consumer warp each, in
- *                    parallel);
+ *                    parallel), bit 25 makes only the records of a CTA's
+ *                    first S bands (default: its first 2S where it has 2S
+ *                    consumer warps, so that once its wait for the sampler
+ *                    returns, its next S bands need no read of the sampler's
+ *                    output);
  *                    crop sources: bit 8 reads 16-byte chunks even where 32-byte
  *                    chunks fit, bit 9 asks TMA for 128-byte L2 promotion;
  *                    compact sources: erased source spans are left out of a

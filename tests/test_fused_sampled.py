@@ -110,19 +110,22 @@ def test_bad_arguments_launch_nothing():
 @pytest.mark.parametrize("shape,dt,layout", [((64, 224, 224, 3), trfn.OUT_F16, trfn.LAYOUT_NHWC),
                                              ((32, 224, 224, 3), trfn.OUT_F32, trfn.LAYOUT_NCHW),
                                              ((24, 299, 299, 3), trfn.OUT_F16, trfn.LAYOUT_NHWC)])   # odd-row form
-@pytest.mark.parametrize("first_records", ["made_in_kernel", "read_from_sampler"])
+@pytest.mark.parametrize("first_records", ["made_in_kernel", "first_S_made_in_kernel", "read_from_sampler"])
 def test_overlapped_sampled_launches(shape, dt, layout, first_records):
     """tr_fused_norm_sampled_ex with TR_LAUNCH_OVERLAP_PREVIOUS: a large
     launch, then consecutive sampled batches with their own source, output
     and records, workspaces alternating.  Each sampler writes while the
     kernel before it drains, each fused kernel requests its first bands
-    before its sampler is done; by default its producer warp makes those
-    bands' records itself with the sampler's steps (tr_tune_tiled flags bit
-    21 reads them from the sampler's output instead).  Records and outputs
-    equal the oracle's either way."""
+    before its sampler is done; by default its consumer warps make the
+    records of a CTA's first 2S bands (S where there are fewer than 2S
+    consumer warps: 4-stage plans) with the sampler's steps (tr_tune_tiled
+    flags bit 25 keeps S, bit 21 reads them all from the sampler's output
+    instead).  Records and outputs equal the oracle's every way."""
     import torch
     if first_records == "read_from_sampler":
         trfn.tr_tune_tiled(flags=1 << 21)
+    elif first_records == "first_S_made_in_kernel":
+        trfn.tr_tune_tiled(flags=1 << 25)
     try:
         _overlapped_sampled_chain(shape, dt, layout)
     finally:

@@ -82,7 +82,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-batched", action="store_true",
                     help="skip the launches of 1, 4 and 8 headline batches each (tr_fused_norm_batches), "
-                         "reported under 'batched_launches'")
+                         "reported under 'batched_launches', the headline batches with their records sampled in "
+                         "the same call ('fused_sampling') and the 299x299 odd-row batches ('odd_rows')")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the other batch workloads (16x32x32x3, 200x28x28x1, 256x224x224x3 -> f32 NHWC/NCHW) "
                          "reported under 'per_config'")
@@ -515,9 +516,11 @@ def run_ours(args, rank, local, world, pg):
     per_config = None
     if not args.no_per_config and headline and world == 1:
         per_config = run_per_config(dev, measured_peaks()[0], args.cpu_seconds / 4, not args.no_cpu)
-    batched = None
+    batched = sampled = odd_rows = None
     if not args.no_batched and headline and world == 1 and not (dev_sampling or fused_sampling):
         batched = run_batched(dev, measured_peaks()[0])
+        sampled = run_sampled(dev, measured_peaks()[0])
+        odd_rows = run_odd_rows(dev, measured_peaks()[0])
 
     value = aggregate_images_per_s(world, N, K, ms_max)
     res = {
@@ -580,6 +583,10 @@ def run_ours(args, rank, local, world, pg):
         res["per_config"] = per_config
     if batched is not None:
         res["batched_launches"] = batched
+    if sampled is not None:
+        res["fused_sampling"] = sampled
+    if odd_rows is not None:
+        res["odd_rows"] = odd_rows
     return res
 
 
@@ -936,6 +943,152 @@ def run_batched(dev, peak, Ks=(1, 4, 8)):
     out["parity_sample"] = parity
     out["path"] = ("tr_fused_norm_batches: K batches of 256x224x224x3 -> f16 NHWC (flip + erase) per launch, "
                    "dynamic schedule, %d rotating buffer sets" % nsets)
+    return out
+
+
+def time_graph_modes(stream, launch, G, reps, per_launch_units=1):
+    """Median milliseconds per unit (a launch, or per_launch_units batches of
+    it) of a CUDA graph of G launches, replayed reps times per trial, three
+    trials, with the launches overlapping the previous one and with each
+    waiting for it: {mode: (median, trials)}.  launch(k, overlap) issues
+    launch k on stream; one untimed replay precedes the trials."""
+    import torch
+    out = {}
+    for mode, overlap in (("overlapping", True), ("waiting", False)):
+        with torch.cuda.stream(stream):
+            for k in range(G):
+                launch(k, overlap)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(G):
+                launch(k, overlap)
+        with torch.cuda.stream(stream):
+            g.replay()
+        per = []
+        for _ in range(3):
+            e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                torch.cuda._sleep(SPACER_CYCLES)
+                e_a.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e_b.record(stream)
+            e_b.synchronize()
+            per.append(e_a.elapsed_time(e_b) / (reps * G * per_launch_units))
+        out[mode] = (float(np.median(per)), per)
+        del g
+    torch.cuda.synchronize()
+    return out
+
+
+def run_sampled(dev, peak):
+    """The headline workload with its records drawn on the GPU in the same
+    call (tr_fused_norm_sampled: the sampler grid, then the fused kernel,
+    whose CTAs make their first records themselves when the call overlaps
+    the previous one): per-batch time and roofline fraction overlapping and
+    waiting; the records and three images of the last written set against
+    the oracle."""
+    import torch
+    import image_preprocessing_gb300 as trfn
+    from image_preprocessing_gb300 import synth
+    cfg = dict(synth.CONFIGS[3], layout="nhwc")
+    N, H, W, C = cfg["N"], cfg["H"], cfg["W"], cfg["C"]
+    mean = np.array(cfg["mean"], np.float32)
+    std = np.array(cfg["std"], np.float32)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nsets = max(2, int(np.ceil(4 * l2 / (N * H * W * C * 3))))
+    src0 = torch.from_numpy(synth.config_pixels(3)).to(dev)
+    srcs = [src0.clone() for _ in range(nsets)]
+    dsts = [torch.empty((N, H, W, C), dtype=torch.float16, device=dev) for _ in range(nsets)]
+    recs = [torch.zeros((N, 5), dtype=torch.int32, device=dev) for _ in range(nsets)]
+    stream = torch.cuda.Stream(device=dev)
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev) for _ in range(2)]
+    G = nsets * max(1, 60 // nsets)
+    G += G % 2
+
+    def launch(k, overlap):
+        j = k % nsets
+        trfn.tr_fused_norm_sampled(srcs[j], dsts[j], mean, std, 4000 + j, 0, recs[j], flip=cfg["flip"],
+                                   erase=cfg["erase"], erase_p=cfg["erase_p"], out_dtype=trfn.OUT_F16,
+                                   layout=trfn.LAYOUT_NHWC, stream=stream, workspace=wss[k % 2],
+                                   overlap_previous=overlap)
+
+    t = time_graph_modes(stream, launch, G, max(1, -(-240 // G)))
+    got_recs = [r.cpu().numpy() for r in recs]   # the records the sampler wrote (bytes of the erased spans)
+    alg = float(np.mean([algorithmic_bytes(cfg, got_recs[k % nsets]) for k in range(G)]))
+    out = {"workload": cfg["name"] + "_records_sampled_in_call", "algorithmic_bytes_per_launch": alg,
+           "l2": "%d rotating buffer sets >= 4x L2" % nsets}
+    for mode, (ms, per) in t.items():
+        gbs = alg / (ms / 1e3) / 1e9
+        out[mode] = {"us_per_batch": ms * 1e3, "images_per_s": N / (ms / 1e3), "achieved_gbs": gbs,
+                     "frac": gbs / peak, "trials_us_per_batch": [v * 1e3 for v in per]}
+    import oracle
+    j = (G - 1) % nsets
+    ref_recs = oracle.sample_aug_params_blocked(4000 + j, 0, N, H, W, flip=cfg["flip"], erase=cfg["erase"],
+                                                erase_p=cfg["erase_p"])[0]
+    par = parity_sample(cfg, [srcs[j]], [dsts[j]], [ref_recs], mean, std, trfn.OUT_F16, trfn.LAYOUT_NHWC, 1)
+    par["records_equal"] = bool(np.array_equal(got_recs[j], ref_recs))
+    par["ok"] = par["ok"] and par["records_equal"]
+    out["parity_sample"] = par
+    out["path"] = ("tr_fused_norm_sampled: records sampled on the GPU (Philox4x32-10 counters) and the fused step "
+                   "in one call, graph of %d calls" % G)
+    return out
+
+
+def run_odd_rows(dev, peak):
+    """256 x 299x299x3 -> f16 NHWC and NCHW, flip + erase: source rows of 897
+    bytes and NCHW output rows of 598, the tiled kernel's odd-row form; per
+    batch overlapping and waiting, three images of the last set against the
+    oracle."""
+    import torch
+    import image_preprocessing_gb300 as trfn
+    from image_preprocessing_gb300 import synth
+    out = {}
+    N, H, W, C = 256, 299, 299, 3
+    for layout_name in ("nhwc", "nchw"):
+        cfg = dict(synth.CONFIGS[3], H=H, W=W, layout=layout_name)
+        cfg["name"] = "n256_299x299x3_f16_%s_flip_erase" % layout_name
+        layout = trfn.LAYOUT_NHWC if layout_name == "nhwc" else trfn.LAYOUT_NCHW
+        mean = np.array(cfg["mean"], np.float32)
+        std = np.array(cfg["std"], np.float32)
+        shape = trfn.out_shape(N, H, W, C, layout)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        nsets = max(2, int(np.ceil(4 * l2 / (N * H * W * C * 3))))
+        px = synth.pixels_uniform(1299, N, H, W, C)
+        src0 = torch.from_numpy(px).to(dev)
+        srcs = [src0.clone() for _ in range(nsets)]
+        dsts = [torch.empty(shape, dtype=torch.float16, device=dev) for _ in range(nsets)]
+        recs_all, augs, offset = [], [], 0
+        for j in range(nsets):
+            r, offset = trfn.tr_sample_aug_params(2299, offset, N, H, W, erase_p=cfg["erase_p"])
+            recs_all.append(r)
+            augs.append(torch.from_numpy(r).to(dev))
+        stream = torch.cuda.Stream(device=dev)
+        wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device=dev) for _ in range(2)]
+        G = nsets * max(1, 60 // nsets)
+        G += G % 2
+
+        def launch(k, overlap):
+            j = k % nsets
+            trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=trfn.OUT_F16, layout=layout,
+                               stream=stream, workspace=wss[k % 2], overlap_previous=overlap)
+
+        t = time_graph_modes(stream, launch, G, max(1, -(-120 // G)))
+        alg = float(np.mean([algorithmic_bytes(cfg, recs_all[k % nsets]) for k in range(G)]))
+        geo = trfn.tr_fused_norm_geometry(N, H, W, C, out_dtype=trfn.OUT_F16, layout=layout, overlap_previous=True)
+        r = {"workload": cfg["name"], "algorithmic_bytes_per_launch": alg,
+             "kernel": "tiled, odd-row form" if geo.get("odd_form") else "tiled", "geometry": geo,
+             "l2": "%d rotating buffer sets >= 4x L2" % nsets}
+        for mode, (ms, per) in t.items():
+            gbs = alg / (ms / 1e3) / 1e9
+            r[mode] = {"us_per_batch": ms * 1e3, "images_per_s": N / (ms / 1e3), "achieved_gbs": gbs,
+                       "frac": gbs / peak, "trials_us_per_batch": [v * 1e3 for v in per]}
+        j = (G - 1) % nsets
+        r["parity_sample"] = parity_sample(cfg, [srcs[j]], [dsts[j]], [recs_all[j]], mean, std, trfn.OUT_F16,
+                                           layout, 1)
+        out[cfg["name"]] = r
+        del srcs, dsts
+        torch.cuda.empty_cache()
     return out
 
 

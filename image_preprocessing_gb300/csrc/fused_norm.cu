@@ -1592,10 +1592,15 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
     }
     const int tid = threadIdx.x - 32;
     const int nthr = blockDim.x - 32;
-    const bool storer = (tid == 0);
+    // The storer is the first thread of the last consumer warp: where a
+    // band's groups leave the consumers' last stride partly empty, the
+    // empty slots fall on the last warps (groups go to consumer threads in
+    // order), so the store work goes to a warp with less conversion work.
+    const int store_base = nthr - 32;
+    const bool storer = (tid == store_base);
     // the odd-row form's stores take the storer's whole warp (element stores
-    // at the bands' unaligned edges); lane 0 issues the bulk stores
-    const bool store_warp = ODD ? (tid < 32) : storer;
+    // at the bands' unaligned edges); its first lane issues the bulk stores
+    const bool store_warp = ODD ? (tid >= store_base) : storer;
     bool aborted = false;
     for (int i = 0;; ++i) {
         const int s = i % S;
@@ -1611,7 +1616,7 @@ __global__ void __launch_bounds__(256, (tiled_min_blocks<C, OUT_F16, LAYOUT, CRO
         if (rec.rows == 0) break;   // the producer's end mark
         if (store_warp) {
             if (storer) mbar_arrive(empty0 + 8u * s);
-            store_unit<C, OUT_F16, LAYOUT, ODD, MODE>(p, ob, rec, tid);
+            store_unit<C, OUT_F16, LAYOUT, ODD, MODE>(p, ob, rec, tid - store_base);
         }
     }
     if (storer) {

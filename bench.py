@@ -666,11 +666,35 @@ def run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg):
     ob = 2 if dt == 1 else 4
     h2d = N * H * W * C + (N * 20 if h_par[0] is not None else 0)
     d2h = int(np.prod(out_shape)) * ob
+    # the bound the station runs against: the same steps' copies alone (the
+    # batch in on the copy stream, the result out on the d2h stream, both
+    # directions at once), no kernel
+    img = N * H * W * C
+    reps = 16
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    main = torch.cuda.current_stream(dev)
+    e_a.record(main)
+    s_copy.wait_stream(main)
+    s_d2h.wait_stream(main)
+    for k in range(reps):
+        with torch.cuda.stream(s_copy):
+            slots[k % 2][:img].copy_(h_src[k % nh].view(-1), non_blocking=True)
+        with torch.cuda.stream(s_d2h):
+            h_out[k % 2].copy_(d_out[k % 2], non_blocking=True)
+    main.wait_stream(s_copy)
+    main.wait_stream(s_d2h)
+    e_b.record(main)
+    e_b.synchronize()
+    copies_s = e_a.elapsed_time(e_b) / 1e3 / reps
     return {"value": world * N * K / sec, "unit": "images/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
             "path": "tr_ts_submit: pinned host u8 + records -> device slot A/B (copy stream) -> kernel "
                     "(compute stream) -> pinned host output (d2h stream)",
-            "link_gbs": (h2d + d2h) * K / sec / 1e9}
+            "link_gbs": (h2d + d2h) * K / sec / 1e9,
+            "copies_alone": {"us_per_step": copies_s * 1e6, "link_gbs": (img + d2h) / copies_s / 1e9,
+                             "frac": copies_s / (sec / K),
+                             "how": "the step's uint8 batch in and result out, both directions at once, %d steps, "
+                                    "no kernel" % reps}}
 
 
 def run_pipeline(dev, rank, pg):

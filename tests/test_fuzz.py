@@ -1,0 +1,120 @@
+"""Seeded random cases, each compared with the oracle element by element with
+guard bytes around the output: shapes with ragged edges (odd rows, one-row
+and one-pixel images, rows shorter than a group), every channel count,
+output type and layout, offset source and output pointers, the three kernel
+choices, tile geometries (band height, stages, CTAs per SM) and
+tr_tune_tiled flags, all drawn from one seed.  The tiled cases run once more
+through the checked build (libtrfn_bounds.so), which tests every range the
+tiled kernel copies, loads or stores and must leave its status word clear;
+that test comes first, so a range the planner got wrong shows up there as a
+status bit rather than as an access outside a buffer.
+(Integration tests as layers of determinism and correctness: "(25)
+integration tests" article, §一-§二.)"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import image_preprocessing_gb300 as trfn
+from image_preprocessing_gb300 import _native, synth
+from parity_util import assert_parity, check_case
+
+pytestmark = pytest.mark.gpu
+
+F32, F16 = trfn.OUT_F32, trfn.OUT_F16
+NHWC, NCHW, NHWC4 = trfn.LAYOUT_NHWC, trfn.LAYOUT_NCHW, trfn.LAYOUT_NHWC4
+AUTO, TILED, GENERIC = trfn.VARIANT_AUTO, trfn.VARIANT_TILED, trfn.VARIANT_GENERIC
+
+SEED = 20261202
+CASES = 300
+# tr_tune_tiled flag bits that change how the kernels work, not what they
+# compute (bit 6, the bounded-wait test hook, is left out)
+FLAG_BITS = (0, 1, 2, 3, 4, 5, 7, 10, 11, 16, 17, 18, 19, 20, 23)
+
+
+def _case(i):
+    rng = np.random.default_rng(SEED + i)
+    N = int(rng.integers(1, 9))
+    H = int(rng.integers(1, 72))
+    W = int(rng.integers(1, 140))
+    C = int(rng.integers(1, 5))
+    dt = F16 if rng.random() < 0.5 else F32
+    layout = (NHWC, NCHW, NHWC4)[int(rng.integers(0, 3))]
+    variant = (AUTO, TILED, GENERIC)[int(rng.integers(0, 3))]
+    ob = 2 if dt == F16 else 4
+    flags = 0
+    for b in rng.choice(FLAG_BITS, size=int(rng.integers(0, 4)), replace=False):
+        flags |= 1 << int(b)
+    if rng.random() < 0.3:
+        flags |= int(rng.integers(0, 16)) << 12   # erased-span threshold
+    return dict(
+        src=synth.pixels_uniform(SEED + i, N, H, W, C),
+        aug=synth.random_records(SEED + i, N, H, W, allow_outside=True) if rng.random() < 0.8 else None,
+        mean=rng.uniform(0.0, 1.0, C).astype(np.float32),
+        # |v| <= 5: the binary32 bar (2e-6 absolute) is then above 3 ulps
+        std=rng.uniform(0.2, 0.6, C).astype(np.float32),
+        dt=dt, layout=layout, variant=variant,
+        src_offset=0 if variant == TILED else int(rng.choice([0, 0, 1, 3, 16])),
+        dst_offset=int(rng.choice([0, 0, ob, 3 * ob, 16])),
+        tune=(int(rng.choice([0, 0, 16, 48, 200, 1000, 4096])), int(rng.choice([0, 0, 2, 3, 4, 8])),
+              int(rng.choice([0, 0, 1, 2, 3])), flags),
+        workspace=bool(rng.random() < 0.5))
+
+
+def _checked_status(L):
+    v = ctypes.c_int(0)
+    assert L.tr_device_status(ctypes.byref(v), 1) == 0
+    return v.value
+
+
+def test_random_tiled_cases_pass_the_checked_build():
+    import torch
+    L = _native.checked_lib()
+    _checked_status(L)
+    guard = 64
+    for i in range(CASES):
+        c = _case(i)
+        src = c["src"]
+        N, H, W, C = src.shape
+        shape = trfn.out_shape(N, H, W, C, c["layout"])
+        ob = 2 if c["dt"] == F16 else 4
+        nbytes = int(np.prod(shape)) * ob
+        s_buf = torch.from_numpy(np.ascontiguousarray(src).reshape(-1)).cuda()
+        d_buf = torch.full((nbytes + 2 * guard + c["dst_offset"],), 0xAB, dtype=torch.uint8, device="cuda")
+        a = torch.from_numpy(c["aug"]).cuda() if c["aug"] is not None else None
+        ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") if c["workspace"] else None
+        assert L.tr_tune_tiled(*c["tune"]) == 0
+        try:
+            rc = L.tr_fused_norm_ws(s_buf.data_ptr(), d_buf.data_ptr() + guard + c["dst_offset"], N, H, W, C,
+                                    _native.float_array(c["mean"]), _native.float_array(c["std"]),
+                                    a.data_ptr() if a is not None else None, c["dt"], c["layout"], None, TILED,
+                                    ws.data_ptr() if ws is not None else None)
+            assert rc == 0, L.tr_last_error_message()
+            torch.cuda.synchronize()
+        finally:
+            L.tr_tune_tiled(0, 0, 0, 0)
+        host = d_buf.cpu().numpy()
+        body = host[guard + c["dst_offset"]:guard + c["dst_offset"] + nbytes]
+        got = body.view(np.uint16 if c["dt"] == F16 else np.float32).reshape(shape)
+        ref = oracle.fused_norm(src, c["mean"], c["std"], c["aug"], out_dtype=c["dt"], layout=c["layout"])
+        assert_parity(got, ref, c["dt"], "checked build, case %d" % i)
+        rest = np.concatenate([host[:guard + c["dst_offset"]], host[guard + c["dst_offset"] + nbytes:]])
+        assert np.all(rest == 0xAB), "case %d wrote outside its output" % i
+        assert _checked_status(L) == 0, "case %d: a bounds check failed" % i
+
+
+@pytest.mark.parametrize("i", range(CASES))
+def test_random_case_matches_the_oracle(i):
+    import torch
+    c = _case(i)
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") if c["workspace"] else None
+    trfn.tr_tune_tiled(*c["tune"])
+    try:
+        check_case(c["src"], c["mean"], c["std"], c["aug"], c["dt"], c["layout"], variant=c["variant"],
+                   src_offset=c["src_offset"], dst_offset=c["dst_offset"], workspace=ws)
+    finally:
+        trfn.tr_tune_tiled()
+    if ws is not None:
+        assert int(ws.count_nonzero()) == 0, "the scheduling workspace was not returned to zero"
+    assert trfn.tr_device_status() == 0

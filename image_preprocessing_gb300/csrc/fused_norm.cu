@@ -978,7 +978,7 @@ __device__ __forceinline__ bool smem_read_ok(const TiledParams& p, const uint8_t
 template <int C, int OUT_F16>
 __device__ __forceinline__ void odd_nhwc_group(const TiledParams& p, const uint8_t* sin, uint8_t* tile0,
                                                const uint8_t* tile_end, const UnitRec& rec, int g, int psi,
-                                               int E, int off_in) {
+                                               int E, int off_in, bool band_erased) {
     constexpr int OB = OUT_F16 ? 2 : 4;
     constexpr int P = Group<C>::P;
     constexpr int GE = P * C;                    // elements (source bytes) of a group
@@ -987,12 +987,17 @@ __device__ __forceinline__ void odd_nhwc_group(const TiledParams& p, const uint8
     constexpr int EPC = 16 / OB;                 // elements per chunk
     const int WC = p.W * C;
     const int e0 = g * GE - psi;
-    // row of the last element, or the band's last row when the group runs
-    // past the band (those elements are not stored)
-    const int r1 = min((int)(((uint64_t)(uint32_t)(e0 + GE - 1) * p.wc_inv) >> 32), rec.rows - 1);
-    const int split = r1 * WC - e0;              // elements k < split lie in row r1 - 1
-    const int split_px = split > 0 ? split / C : 0;   // pixels of the group in row r1 - 1
     const bool flip = (rec.flags & 1) != 0;
+    // the row of the group's last element (or the band's last row when the
+    // group runs past the band: those elements are not stored) and the
+    // group's pixels in the row before it; needed only where the band is
+    // flipped or meets the erased rows (both uniform over the band)
+    int r1 = 0, split_px = 0;
+    if (flip || band_erased) {
+        r1 = min((int)(((uint64_t)(uint32_t)(e0 + GE - 1) * p.wc_inv) >> 32), rec.rows - 1);
+        const int split = r1 * WC - e0;          // elements k < split lie in row r1 - 1
+        split_px = split > 0 ? split / C : 0;
+    }
     uint32_t w[NW];
     if (!flip) {
         const uint8_t* q = sin + off_in + e0;
@@ -1026,7 +1031,7 @@ __device__ __forceinline__ void odd_nhwc_group(const TiledParams& p, const uint8
     if (flip) convert_group<C, true>(w, p.base, p.scale, p.bias, v);
     else convert_group<C, false>(w, p.base, p.scale, p.bias, v);
     // erased pixels: those of row r1 - 1 ([0, split_px)) and of row r1
-    if (rec.erow_lo < rec.erow_hi) {
+    if (band_erased) {
         const int ya = rec.y_begin + r1 - 1, yb = ya + 1;
         const int xa = (e0 - (r1 - 1) * WC) / C;   // pixel x of group pixel 0 in row r1 - 1 (if any)
         const int xb = (e0 - r1 * WC) / C;         // ... in row r1 (negative when it starts before)
@@ -1081,7 +1086,11 @@ __device__ __forceinline__ void odd_nhwc_band(const TiledParams& p, const uint8_
     uint8_t* tile0 = sout + (sh - (uint32_t)phi * OB) - (psi - phi) * OB;
     const uint8_t* tile_end = sout + p.out_stage;
     const int ng = (E + psi + GE - 1) / GE;
-    for (int g = tid; g < ng; g += nthr) odd_nhwc_group<C, OUT_F16>(p, sin, tile0, tile_end, rec, g, psi, E, off_in);
+    // whether any of the band's rows is erased (then per group below)
+    const bool band_erased = rec.erow_lo < rec.erow_hi && rec.erow_lo < rec.y_begin + rec.rows &&
+                             rec.erow_hi > rec.y_begin;
+    for (int g = tid; g < ng; g += nthr)
+        odd_nhwc_group<C, OUT_F16>(p, sin, tile0, tile_end, rec, g, psi, E, off_in, band_erased);
 }
 
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD, int MODE>

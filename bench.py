@@ -652,16 +652,22 @@ def run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg):
     steps(0, 4)
     assert ts.sync(60000)
     K = args.e2e_steps
-    barrier(pg)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    steps(4, K)
-    ok = ts.sync(120000)
-    torch.cuda.synchronize()
-    t1 = time.perf_counter()
+    # three runs of K steps; the median is reported (host memory and its link
+    # are shared with the machine's other jobs, so a single run can catch
+    # their traffic)
+    runs = []
+    for t in range(3):
+        barrier(pg)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        steps(4 + t * K, K)
+        ok = ts.sync(120000)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        assert ok, "transfer station did not finish"
+        runs.append(max_over_ranks(pg, t1 - t0, dev))
     ts.close()
-    assert ok, "transfer station did not finish"
-    sec = max_over_ranks(pg, t1 - t0, dev)
+    sec = float(np.median(runs))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     ob = 2 if dt == 1 else 4
     h2d = N * H * W * C + (N * 20 if h_par[0] is not None else 0)
@@ -688,6 +694,8 @@ def run_e2e(args, cfg, dev, mean, std, dt, layout, tdt, out_shape, rank, pg):
     copies_s = e_a.elapsed_time(e_b) / 1e3 / reps
     return {"value": world * N * K / sec, "unit": "images/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
+            "runs_images_per_s": [world * N * K / r for r in runs],
+            "how": "median of three runs of %d steps" % K,
             "path": "tr_ts_submit: pinned host u8 + records -> device slot A/B (copy stream) -> kernel "
                     "(compute stream) -> pinned host output (d2h stream)",
             "link_gbs": (h2d + d2h) * K / sec / 1e9,
@@ -704,8 +712,9 @@ def run_pipeline(dev, rank, pg):
     device; the copy of batch k+1 (copy stream) overlaps the kernel on batch
     k (compute stream).  Outputs stay on the device (two alternating output
     buffers).  Reports images/s from the first copy to the last kernel (CUDA
-    events), a lone 38.5 MB pinned copy, the kernel alone, and the overlap
-    efficiency (T_copy + T_kernel) / T_pipelined over the 64 batches."""
+    events; the median of three passes), a lone 38.5 MB pinned copy, the
+    kernel alone, and the overlap efficiency (T_copy + T_kernel) /
+    T_pipelined over the 64 batches."""
     import torch
     import image_preprocessing_gb300 as trfn
     from image_preprocessing_gb300 import synth
@@ -741,15 +750,19 @@ def run_pipeline(dev, rank, pg):
         for b in range(B):
             slots[b & 1][:img_bytes].copy_(h_src[b].view(-1), non_blocking=True)
     torch.cuda.synchronize()
-    # a lone pinned host-to-device copy of one batch (8 batches, averaged)
-    e0, e1 = events()
-    with torch.cuda.stream(s_copy):
-        e0.record(s_copy)
-        for b in range(8):
-            slots[b & 1][:img_bytes].copy_(h_src[b].view(-1), non_blocking=True)
-        e1.record(s_copy)
-    e1.synchronize()
-    t_copy = e0.elapsed_time(e1) / 8 / 1e3
+    # a lone pinned host-to-device copy of one batch (8 batches, averaged;
+    # the median of three such runs)
+    lone = []
+    for _ in range(3):
+        e0, e1 = events()
+        with torch.cuda.stream(s_copy):
+            e0.record(s_copy)
+            for b in range(8):
+                slots[b & 1][:img_bytes].copy_(h_src[b].view(-1), non_blocking=True)
+            e1.record(s_copy)
+        e1.synchronize()
+        lone.append(e0.elapsed_time(e1) / 8 / 1e3)
+    t_copy = float(np.median(lone))
     # the kernel alone on a slot, dynamically scheduled as in the station (16
     # launches, averaged)
     d_par = h_par[0].to(dev)
@@ -770,19 +783,24 @@ def run_pipeline(dev, rank, pg):
     for b in range(2):   # warm-up: the station's first batch also saves its filler
         ts.submit(h_src[b], d_out[b & 1], mean, std, h_params=h_par[b], out_dtype=trfn.OUT_F16)
     assert ts.sync(60000)
-    barrier(pg)
-    torch.cuda.synchronize()
-    e0, e1 = events()
-    e0.record(s_copy)
-    launches = trfn.tr_launch_count()
-    for b in range(B):
-        ts.submit(h_src[b], d_out[b & 1], mean, std, h_params=h_par[b], out_dtype=trfn.OUT_F16)
-    e1.record(s_comp)
-    launches = trfn.tr_launch_count() - launches
-    e1.synchronize()
-    assert ts.sync(60000)
+    # the stream of B batches, three times; the median is reported (host
+    # memory and its link are shared with the machine's other jobs)
+    passes = []
+    for _ in range(3):
+        barrier(pg)
+        torch.cuda.synchronize()
+        e0, e1 = events()
+        e0.record(s_copy)
+        launches = trfn.tr_launch_count()
+        for b in range(B):
+            ts.submit(h_src[b], d_out[b & 1], mean, std, h_params=h_par[b], out_dtype=trfn.OUT_F16)
+        e1.record(s_comp)
+        launches = trfn.tr_launch_count() - launches
+        e1.synchronize()
+        assert ts.sync(60000)
+        passes.append(max_over_ranks(pg, e0.elapsed_time(e1) / 1e3, dev))
     ts.close()
-    t_pipe = max_over_ranks(pg, e0.elapsed_time(e1) / 1e3, dev)
+    t_pipe = float(np.median(passes))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     h2d = img_bytes + N * 20
     # the last two batches' outputs are still on the device (batch b wrote
@@ -795,6 +813,7 @@ def run_pipeline(dev, rank, pg):
         parity["max_f16_ulp"] = max(parity["max_f16_ulp"], one["max_f16_ulp"])
     return {
         "workload": cfg["name"], "batches": B, "images_per_s": world * B * N / t_pipe,
+        "passes_images_per_s": [world * B * N / t for t in passes], "how": "median of three passes",
         "ms_pipelined": t_pipe * 1e3, "h2d_gbs_lone_copy": img_bytes / t_copy / 1e9,
         "us_copy_per_batch": t_copy * 1e6, "us_kernel_per_batch": t_kernel * 1e6,
         "overlap_efficiency": B * (t_copy + t_kernel) / t_pipe,

@@ -1713,6 +1713,20 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
             n = (int)(row / p.H);
             y = (int)(row - (long long)n * p.H);
         }
+        int cy = 0, cx = 0;
+        if (p.crop != nullptr) {
+            cy = min(max(p.crop[2 * (size_t)n], 0), p.src_H - p.H);
+            cx = min(max(p.crop[2 * (size_t)n + 1], 0), p.src_W - p.W);
+        }
+        const uint8_t* row = p.src + (size_t)n * p.image_stride + (size_t)(cy + y) * p.row_stride + (size_t)cx * C;
+        // the pixel and its mirror in the same row are requested with the
+        // record, so the record's latency does not come before the pixel's
+        uint8_t here[C], mirror[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            here[c] = __ldg(row + (size_t)x * C + c);
+            mirror[c] = p.aug != nullptr ? __ldg(row + (size_t)(p.W - 1 - x) * C + c) : here[c];
+        }
         bool flip = false, erased = false;
         if (p.aug != nullptr) {
             const tr_aug_param a = p.aug[n];
@@ -1720,19 +1734,13 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
             erased = a.h > 0 && a.w > 0 && y >= a.y0 && (long long)y < (long long)a.y0 + a.h && x >= a.x0 &&
                      (long long)x < (long long)a.x0 + a.w;
         }
-        int cy = 0, cx = 0;
-        if (p.crop != nullptr) {
-            cy = min(max(p.crop[2 * (size_t)n], 0), p.src_H - p.H);
-            cx = min(max(p.crop[2 * (size_t)n + 1], 0), p.src_W - p.W);
-        }
-        const int xs = flip ? (p.W - 1 - x) : x;
-        const uint8_t* sp = p.src + (size_t)n * p.image_stride + (size_t)(cy + y) * p.row_stride + (size_t)(cx + xs) * C;
         float v[OC];
 #pragma unroll
-        for (int c = 0; c < OC; ++c) {
-            v[c] = 0.0f;
-            if (c < C && !erased)
-                v[c] = __fmaf_rn(__fsub_rn((float)__ldg(sp + c), p.shift[c]), p.scale[c], p.bias[c]);
+        for (int c = 0; c < OC; ++c) v[c] = 0.0f;
+        if (!erased) {
+#pragma unroll
+            for (int c = 0; c < C; ++c)
+                v[c] = __fmaf_rn(__fsub_rn((float)(flip ? mirror[c] : here[c]), p.shift[c]), p.scale[c], p.bias[c]);
         }
         const size_t pix = ((size_t)n * p.H + y) * p.W + x;
         if (LAYOUT == TR_LAYOUT_NCHW) {

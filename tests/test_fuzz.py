@@ -118,3 +118,61 @@ def test_random_case_matches_the_oracle(i):
     if ws is not None:
         assert int(ws.count_nonzero()) == 0, "the scheduling workspace was not returned to zero"
     assert trfn.tr_device_status() == 0
+
+
+SAMPLED_CASES = 32
+# tr_tune_tiled flag bits of the one-call sampled form: first records read
+# from the sampler (21), made by the producer warp (22), only the first S
+# made (25)
+SAMPLED_BITS = (21, 22, 25)
+
+
+@pytest.mark.parametrize("i", range(SAMPLED_CASES))
+def test_random_overlapped_sampled_chains_match_the_oracle(i):
+    """Chains of three one-call sampled launches (records drawn on the GPU
+    in the same call), each overlapping the one before, on random shapes
+    (rows mostly 16-byte multiples, where the fused kernel makes a CTA's
+    first records itself), stage counts and flags: every batch's records
+    equal the oracle's sampler bit for bit and its output the oracle's."""
+    import torch
+    rng = np.random.default_rng(SEED + 7000 + i)
+    C = int(rng.integers(1, 5))
+    W = int(rng.integers(1, 12)) * (16 // np.gcd(16, C)) if rng.random() < 0.8 else int(rng.integers(1, 140))
+    H = int(rng.integers(1, 90))
+    N = int(rng.integers(1, 70))
+    dt = F16 if rng.random() < 0.5 else F32
+    layout = (NHWC, NCHW, NHWC4)[int(rng.integers(0, 3))]
+    flags = 0
+    for b in rng.choice(SAMPLED_BITS, size=int(rng.integers(0, 2)), replace=False):
+        flags |= 1 << int(b)
+    stages = int(rng.choice([0, 0, 2, 3, 4]))
+    mean = rng.uniform(0.0, 1.0, C).astype(np.float32)
+    std = rng.uniform(0.2, 0.6, C).astype(np.float32)
+    K = 3
+    srcs = [synth.pixels_uniform(SEED + 100 * i + k, N, H, W, C) for k in range(K)]
+    tdt = torch.float16 if dt == F16 else torch.float32
+    dsts = [torch.full(trfn.out_shape(N, H, W, C, layout), 3.0, dtype=tdt, device="cuda") for _ in range(K)]
+    recs = [torch.full((N, 5), -7, dtype=torch.int32, device="cuda") for _ in range(K)]
+    wss = [torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") for _ in range(2)]
+    d_src = [torch.from_numpy(x).cuda() for x in srcs]
+    st = torch.cuda.Stream()
+    trfn.tr_tune_tiled(0, stages, 0, flags)
+    try:
+        with torch.cuda.stream(st):
+            for k in range(K):
+                trfn.tr_fused_norm_sampled(d_src[k], dsts[k], mean, std, 900 + i, 24 * N * k, recs[k],
+                                           out_dtype=dt, layout=layout, stream=st, workspace=wss[k % 2],
+                                           overlap_previous=True)
+        torch.cuda.synchronize()
+    finally:
+        trfn.tr_tune_tiled()
+    for k in range(K):
+        ref_rec, _ = oracle.sample_aug_params_blocked(900 + i, 24 * N * k, N, H, W)
+        assert np.array_equal(recs[k].cpu().numpy(), ref_rec), "case %d batch %d records" % (i, k)
+        got = dsts[k].cpu()
+        got = got.view(torch.int16).numpy().view(np.uint16) if dt == F16 else got.numpy()
+        ref = oracle.fused_norm(srcs[k], mean, std, ref_rec, out_dtype=dt, layout=layout)
+        assert_parity(got, ref, dt, "case %d batch %d" % (i, k))
+    for ws in wss:
+        assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0

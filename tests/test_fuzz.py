@@ -176,3 +176,43 @@ def test_random_overlapped_sampled_chains_match_the_oracle(i):
     for ws in wss:
         assert int(ws.count_nonzero()) == 0
     assert trfn.tr_device_status() == 0
+
+
+BATCHES_CASES = 24
+
+
+@pytest.mark.parametrize("i", range(BATCHES_CASES))
+def test_random_batches_per_launch_match_the_oracle(i):
+    """tr_fused_norm_batches on random K (1..16), shapes (odd rows
+    included), types, layouts, records and schedules, waiting or overlapping
+    the launch before: every batch against the oracle."""
+    import torch
+    rng = np.random.default_rng(SEED + 9000 + i)
+    K = int(rng.integers(1, 17))
+    C = int(rng.integers(1, 5))
+    N, H, W = int(rng.integers(1, 40)), int(rng.integers(1, 60)), int(rng.integers(1, 100))
+    dt = F16 if rng.random() < 0.5 else F32
+    layout = (NHWC, NCHW, NHWC4)[int(rng.integers(0, 3))]
+    mean = rng.uniform(0.0, 1.0, C).astype(np.float32)
+    std = rng.uniform(0.2, 0.6, C).astype(np.float32)
+    tdt = torch.float16 if dt == F16 else torch.float32
+    host, batches = [], []
+    for k in range(K):
+        src = synth.pixels_uniform(SEED + 50 * i + k, N, H, W, C)
+        aug = synth.random_records(SEED + 50 * i + k, N, H, W, allow_outside=True) if rng.random() < 0.8 else None
+        host.append((src, aug))
+        batches.append((torch.from_numpy(src).cuda(),
+                        torch.full(trfn.out_shape(N, H, W, C, layout), 3.0, dtype=tdt, device="cuda"),
+                        torch.from_numpy(aug).cuda() if aug is not None else None))
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") if rng.random() < 0.5 else None
+    trfn.tr_fused_norm_batches(batches, mean, std, out_dtype=dt, layout=layout, workspace=ws,
+                               overlap_previous=bool(ws is not None and rng.random() < 0.5))
+    torch.cuda.synchronize()
+    for k, ((src, aug), (_, dst, _)) in enumerate(zip(host, batches)):
+        got = dst.cpu()
+        got = got.view(torch.int16).numpy().view(np.uint16) if dt == F16 else got.numpy()
+        ref = oracle.fused_norm(src, mean, std, aug, out_dtype=dt, layout=layout)
+        assert_parity(got, ref, dt, "case %d batch %d" % (i, k))
+    if ws is not None:
+        assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0

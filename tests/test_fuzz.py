@@ -216,3 +216,60 @@ def test_random_batches_per_launch_match_the_oracle(i):
     if ws is not None:
         assert int(ws.count_nonzero()) == 0
     assert trfn.tr_device_status() == 0
+
+
+CROP_CASES = 32
+
+
+@pytest.mark.parametrize("i", range(CROP_CASES))
+def test_random_crop_windows_match_the_oracle(i):
+    """tr_fused_norm_crop on random windows of random strided sources: row
+    and image strides padded by multiples of 16 bytes half the time (the
+    tensor-copy path where the shape allows it) and by any count otherwise,
+    origins anywhere (clamped into the source), random records, types,
+    layouts, kernel choices and schedules: against the oracle's crop form."""
+    import torch
+    rng = np.random.default_rng(SEED + 11000 + i)
+    C = int(rng.integers(1, 5))
+    N = int(rng.integers(1, 9))
+    H, W = int(rng.integers(1, 48)), int(rng.integers(1, 80))
+    SH, SW = H + int(rng.integers(0, 24)), W + int(rng.integers(0, 40))
+    if rng.random() < 0.5:
+        SW = -(-SW * C // 16) * 16 // C if (-(-SW * C // 16) * 16) % C == 0 else SW
+        row_pad, image_pad = 16 * int(rng.integers(0, 3)), 16 * int(rng.integers(0, 3))
+    else:
+        row_pad, image_pad = int(rng.integers(0, 20)), int(rng.integers(0, 40))
+    dt = F16 if rng.random() < 0.5 else F32
+    layout = (NHWC, NCHW, NHWC4)[int(rng.integers(0, 3))]
+    variant = (AUTO, GENERIC)[int(rng.integers(0, 2))]
+    mean = rng.uniform(0.0, 1.0, C).astype(np.float32)
+    std = rng.uniform(0.2, 0.6, C).astype(np.float32)
+    src = synth.pixels_uniform(SEED + i, N, SH, SW, C)
+    row_stride = SW * C + row_pad
+    image_stride = SH * row_stride + image_pad
+    buf = np.full(N * image_stride, 0xEE, np.uint8)
+    for n in range(N):
+        for y in range(SH):
+            o = n * image_stride + y * row_stride
+            buf[o:o + SW * C] = src[n, y].reshape(-1)
+    crop = np.stack([rng.integers(-4, SH - H + 5, N), rng.integers(-4, SW - W + 5, N)], axis=1).astype(np.int32)
+    clamped = np.stack([np.clip(crop[:, 0], 0, SH - H), np.clip(crop[:, 1], 0, SW - W)], axis=1).astype(np.int32)
+    aug = synth.random_records(SEED + 11000 + i, N, H, W, allow_outside=True) if rng.random() < 0.8 else None
+    ws = torch.zeros(trfn.tr_workspace_bytes(), dtype=torch.uint8, device="cuda") if rng.random() < 0.5 else None
+    d_buf = torch.zeros(buf.size + 64, dtype=torch.uint8, device="cuda")
+    d_buf[:buf.size].copy_(torch.from_numpy(buf))
+    tdt = torch.float16 if dt == F16 else torch.float32
+    out = torch.empty(trfn.out_shape(N, H, W, C, layout), dtype=tdt, device="cuda")
+    trfn.tr_fused_norm_crop(d_buf.data_ptr(), SH, SW, row_stride, image_stride, out, N, H, W, C, mean, std,
+                            crop=torch.from_numpy(crop).cuda(),
+                            aug=torch.from_numpy(aug).cuda() if aug is not None else None,
+                            out_dtype=dt, layout=layout, variant=variant, workspace=ws)
+    torch.cuda.synchronize()
+    got = out.cpu()
+    got = got.view(torch.int16).numpy().view(np.uint16) if dt == F16 else got.numpy()
+    ref = oracle.fused_norm_crop(buf, image_stride, row_stride, SH, SW, N, H, W, C, mean, std, clamped, aug,
+                                 out_dtype=dt, layout=layout)
+    assert_parity(got, ref, dt, "case %d" % i)
+    if ws is not None:
+        assert int(ws.count_nonzero()) == 0
+    assert trfn.tr_device_status() == 0

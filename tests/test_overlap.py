@@ -3,6 +3,8 @@ TR_LAUNCH_OVERLAP_PREVIOUS): consecutive batches with their own buffers and
 workspaces alternating between two, eagerly and inside a CUDA graph, aligned
 and odd-row forms, against the oracle; stream order for later work; the flag
 dropped when a launch reuses the previous launch's workspace."""
+import os
+
 import numpy as np
 import pytest
 
@@ -210,7 +212,7 @@ def test_small_launches_never_run_ahead_of_a_large_one():
 
 
 def test_random_overlapped_chains_match_waiting_launches():
-    """About ten seconds of random chains of overlapped launches (sizes from
+    """About ten seconds (TRFN_CHAIN_SECONDS) of random chains of overlapped launches (sizes from
     2 to 512 images, aligned and odd-row forms, every layout, both types,
     host-made records and records drawn on the GPU in the same call,
     workspaces alternating, eager and replayed from graphs): every output and
@@ -243,7 +245,8 @@ def test_random_overlapped_chains_match_waiting_launches():
     st = torch.cuda.Stream()
     torch.cuda.synchronize()
     t0, chains = time.time(), 0
-    while time.time() - t0 < 10.0:
+    seconds = float(os.environ.get("TRFN_CHAIN_SECONDS", "10"))   # longer stress runs set it
+    while time.time() - t0 < seconds:
         order = rng.permutation(len(bufs)).tolist() + rng.integers(0, len(bufs), 4).tolist()
         seq = [order[0]] + [b for a, b in zip(order, order[1:]) if a != b]   # no buffer twice in a row
 

@@ -302,7 +302,11 @@ int tr_fused_norm_plan(const uint8_t* src_u8, const void* dst, int N, int H, int
  *   src_u8, dst  as for tr_fused_norm; only their alignment is used.
  *   flags        0 or TR_LAUNCH_OVERLAP_PREVIOUS (which changes the planning).
  *   *rows        rows per band; *stages shared-memory input stages;
- *   *ctas_per_sm resident CTAs per SM; *grid CTAs launched;
+ *   *ctas_per_sm resident CTAs per SM; *grid CTAs launched by the static
+ *                schedule (no workspace: the bands spread evenly over the
+ *                fewest CTAs that fit); with a workspace the launch takes
+ *                ctas_per_sm times the SM count, or one CTA per band if
+ *                there are fewer bands;
  *   *odd_form    1 when the odd-row form applies, else 0.
  * Errors as tr_fused_norm's argument checks; TR_ERR_NOT_SUPPORTED where the
  * TILED kernel does not apply; TR_ERR_INVALID_ARGUMENT for N < 1 or a NULL

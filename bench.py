@@ -1124,6 +1124,10 @@ def run_odd_rows(dev, peak):
         t = time_graph_modes(stream, launch, G, max(1, -(-120 // G)))
         alg = float(np.mean([algorithmic_bytes(cfg, recs_all[k % nsets]) for k in range(G)]))
         geo = trfn.tr_fused_norm_geometry(N, H, W, C, out_dtype=trfn.OUT_F16, layout=layout, overlap_previous=True)
+        # geometry's grid is the static schedule's; these launches carry a
+        # workspace, so they take every resident slot (or one CTA per band)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        geo["grid_launched"] = min(N * -(-H // geo["rows"]), geo["ctas_per_sm"] * sms)
         r = {"workload": cfg["name"], "algorithmic_bytes_per_launch": alg,
              "kernel": "tiled, odd-row form" if geo.get("odd_form") else "tiled", "geometry": geo,
              "l2": "%d rotating buffer sets >= 4x L2" % nsets}

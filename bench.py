@@ -545,8 +545,7 @@ def run_ours(args, rank, local, world, pg):
             "workload": cfg["workload"], "N": N, "H": H, "W": W, "C": C, "in": "u8 NHWC",
             "out": cfg["out_dtype"] + " " + cfg["layout"].upper(),
             "flip_p": 0.5 if cfg["flip"] else 0.0, "erase_p": cfg["erase_p"],
-            "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB >= 4x L2 (%.0f MB)" % (
-                nsets, nsets * set_bytes / 1e6, l2 / 1e6),
+            "l2": l2_note(K, nsets, set_bytes, l2),
             "launch": "CUDA graph of %d launches replayed (%s); variant %d; %s" % (
                 G, "timed: %d replays + a graph of the %d remaining launches; every timed graph replayed "
                    "three times in warm-up (%d replays beyond the %d warm-up steps), and %d launches of the "
@@ -593,6 +592,20 @@ def run_ours(args, rank, local, world, pg):
     if odd_rows is not None:
         res["odd_rows"] = odd_rows
     return res
+
+
+def l2_note(K, nsets, set_bytes, l2):
+    """How the timed region stands against L2: its K launches walk the
+    rotating sets in order, so they touch min(K, nsets) of them.  Below 4x L2
+    of distinct bytes the region's inputs are L2-resident (small workloads at
+    small step counts; `per_config` times those over every set)."""
+    touched = min(K, nsets) * set_bytes
+    if touched >= 4 * l2:
+        return "inputs larger than L2: %d rotating buffer sets, %.0f MB >= 4x L2 (%.0f MB)" % (
+            nsets, nsets * set_bytes / 1e6, l2 / 1e6)
+    return ("L2-resident: the timed region's %d launches touch %d of the %d rotating buffer sets, "
+            "%.0f MB < 4x L2 (%.0f MB); per_config times the small workloads over every set" % (
+                K, min(K, nsets), nsets, touched / 1e6, l2 / 1e6))
 
 
 def parity_sample(cfg, srcs, dsts, recs_all, mean, std, dt, layout, nsets, crops=None):

@@ -52,3 +52,14 @@ def test_reference_arm_on_an_overridden_size():
     assert line["config"]["workload"].startswith("n16_33x35x3_")
     assert (line["config"]["H"], line["config"]["W"]) == (33, 35)
     assert line["value"] > 0
+
+
+def test_l2_note_counts_the_sets_the_timed_region_touches():
+    l2 = 136 * 2**20
+    # the headline: 20 launches over five 115.6 MB sets touch all of them
+    assert bench.l2_note(20, 5, 115_605_504, l2).startswith("inputs larger than L2: 5 rotating")
+    # 40 launches of a 0.94 MB workload touch 40 of 692 sets: L2-resident
+    note = bench.l2_note(40, 692, 940_800, l2)
+    assert note.startswith("L2-resident") and "40 of the 692" in note
+    # the same workload over every set is not
+    assert bench.l2_note(692, 692, 940_800, l2).startswith("inputs larger than L2")

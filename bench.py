@@ -1169,8 +1169,11 @@ def run_per_config(dev, peak, cpu_seconds, with_cpu):
             cfg = dict(synth.CONFIGS[4], layout=lay)
             v, threads, sample = oracle_images_per_s(cfg, cpu_seconds)
             v1, _, sample1 = oracle_images_per_s(cfg, max(1.0, cpu_seconds / 2), threads=1)
+            per_image = r["algorithmic_bytes_per_launch"] / r["N"]
             r["cpu_baseline"] = {"value": v, "unit": "images/s", "cores": threads, "kind": "oracle",
-                                 "sample": sample, "single_core": {"value": v1, "sample": sample1}}
+                                 "algorithmic_gbs": v * per_image / 1e9, "sample": sample,
+                                 "single_core": {"value": v1, "algorithmic_gbs": v1 * per_image / 1e9,
+                                                 "sample": sample1}}
         out[r["workload"]] = r
     return out
 
@@ -1289,8 +1292,12 @@ def main():
             cfg = workload(args)
             v, threads, sample = oracle_images_per_s(cfg, args.cpu_seconds)
             v1, _, sample1 = oracle_images_per_s(cfg, max(1.0, args.cpu_seconds / 4), threads=1)
+            # the GPU line's mean algorithmic bytes per image (its sampled rectangles)
+            per_image = res["roofline"]["algorithmic_bytes_per_launch"] / res["config"]["N"]
             res["cpu_baseline"] = {"value": v, "unit": "images/s", "cores": threads, "kind": "oracle",
-                                   "sample": sample, "single_core": {"value": v1, "sample": sample1},
+                                   "algorithmic_gbs": v * per_image / 1e9, "sample": sample,
+                                   "single_core": {"value": v1, "algorithmic_gbs": v1 * per_image / 1e9,
+                                                   "sample": sample1},
                                    "cpu_model": cpu_model()}
         print(json.dumps(res), flush=True)
     if pg is not None:

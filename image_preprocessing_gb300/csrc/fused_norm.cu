@@ -1093,6 +1093,163 @@ __device__ __forceinline__ void odd_nhwc_band(const TiledParams& p, const uint8_
         odd_nhwc_group<C, OUT_F16>(p, sin, tile0, tile_end, rec, g, psi, E, off_in, band_erased);
 }
 
+// NCHW output of the odd-row form (2 or 3 channels), windows laid on the
+// plane tiles' 16-byte frames.  A 16-byte chunk holds EPC = 16 / OB
+// elements (8 binary16, 4 binary32).  Plane c's tile holds the band's
+// rows*W elements from byte sh_c on, so its chunks start at the band's
+// pixels EPC*k - phi_c (phi_c = sh_c / OB).  An image's planes lie H*W
+// elements apart: phi_c = phi_0 + c*D (mod EPC) with D = (H*W) mod EPC.
+// For D = 0 or 1 (every odd square size: 227, 299, ...) the
+// WP = EPC + (C-1)*D consecutive pixels from EPC*g - phi_0 - (C-1)*D on
+// hold, for every plane c, the plane's chunk that starts at window pixel
+// (C-1-c)*D (the band's pixel EPC*g - phi_0 - c*D).  Lane g converts each
+// channel of its window once (the window's source bytes are contiguous like
+// a tile-aligned NHWC group's, with the same flip and erase handling) and
+// writes C aligned 16-byte chunks: no element stores and no realignment of
+// the output.
+template <int C, int OUT_F16, int D>
+struct NchwWindow {
+    static constexpr int EPC = OUT_F16 ? 8 : 4;      // elements per 16-byte chunk
+    static constexpr int WP = EPC + (C - 1) * D;    // window pixels
+    static constexpr int GEW = WP * C;              // its source bytes
+    static constexpr int NWW = (GEW + 3) / 4;       // its words
+};
+
+// Plane c's chunk of window g: its EPC pixels are window pixels (C-1-c)*D
+// on (FLIP: their bytes in the mirrored run), erased ones written as +0.
+template <int C, int OUT_F16, int D, bool FLIP>
+__device__ __forceinline__ void odd_nchw_chunks(const TiledParams& p, const uint32_t (&w)[NchwWindow<C, OUT_F16, D>::NWW],
+                                                const uint8_t* sout, uint8_t* const (&tile)[C], int g, int pw,
+                                                int E, int lo_a, int hi_a, int lo_b, int hi_b) {
+    constexpr int EPC = NchwWindow<C, OUT_F16, D>::EPC;
+    constexpr int WP = NchwWindow<C, OUT_F16, D>::WP;
+    // every plane's chunk lies in the band unless the window meets an end
+    const bool inner = pw >= 0 && pw + WP <= E;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        const int sc = pw + (C - 1 - c) * D;     // the first pixel of plane c's chunk
+        if (!inner && (sc + EPC <= 0 || sc >= E)) continue;   // wholly outside the band
+        float v[EPC];
+#pragma unroll
+        for (int i = 0; i < EPC; ++i) {
+            const int j = (C - 1 - c) * D + i;   // window pixel
+            const int sb = FLIP ? C * (WP - 1 - j) + c : C * j + c;
+            v[i] = __fmaf_rn(byte_minus_shift(w[sb >> 2], sb & 3, p.base[c]), p.scale[c], p.bias[c]);
+        }
+        if (lo_a < hi_a || lo_b < hi_b) {
+#pragma unroll
+            for (int i = 0; i < EPC; ++i) {
+                const int j = (C - 1 - c) * D + i;
+                if ((j >= lo_a && j < hi_a) || (j >= lo_b && j < hi_b)) v[i] = 0.0f;
+            }
+        }
+        uint4 ch;
+        if constexpr (OUT_F16 != 0) {
+            ch = make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4 % EPC], v[5 % EPC]),
+                            pack_half2(v[6 % EPC], v[7 % EPC]));
+        } else {
+            ch = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                            __float_as_uint(v[3]));
+        }
+        uint8_t* const q = tile[c] + 16 * g;
+        (void)sout;
+        // (checked build) inside plane c's tile, on its 16-byte frame
+        if (TRFN_CHECK(q >= sout + (size_t)c * p.plane_bytes && q + 16 <= sout + (size_t)(c + 1) * p.plane_bytes &&
+                           ((uintptr_t)q & 15u) == 0,
+                       22))
+            *reinterpret_cast<uint4*>(q) = ch;
+    }
+}
+
+template <int C, int OUT_F16, int D>
+__device__ __forceinline__ void odd_nchw_window(const TiledParams& p, const uint8_t* sin, const uint8_t* sout,
+                                                uint8_t* const (&tile)[C], const UnitRec& rec, int g, int phi0,
+                                                int E, int off_in, bool band_erased) {
+    constexpr int EPC = NchwWindow<C, OUT_F16, D>::EPC;
+    constexpr int WP = NchwWindow<C, OUT_F16, D>::WP;
+    constexpr int GEW = NchwWindow<C, OUT_F16, D>::GEW;
+    constexpr int NWW = NchwWindow<C, OUT_F16, D>::NWW;
+    const int WC = p.W * C;
+    const int pw = EPC * g - phi0 - (C - 1) * D;   // the window's first pixel (band-relative)
+    const int e0 = pw * C;                         // its first source element
+    const bool flip = (rec.flags & 1) != 0;
+    // the row of the window's last element (clamped to the band's last row:
+    // pixels past the band are not stored) and its pixels in the row before
+    // (the last element's index e0 + GEW - 1 = C * (EPC*g - phi0 + EPC) - 1 > 0)
+    int r1 = 0, split_px = 0;
+    if (flip || band_erased) {
+        r1 = min((int)(((uint64_t)(uint32_t)(e0 + GEW - 1) * p.wc_inv) >> 32), rec.rows - 1);
+        const int split = r1 * WC - e0;
+        split_px = split > 0 ? split / C : 0;
+    }
+    uint32_t w[NWW];
+    if (!flip) {
+        const uint8_t* q = sin + off_in + e0;
+        if (smem_read_ok(p, q, 4 * (NWW + 1), 19)) load_bytes_at<NWW>(q, w);
+        else for (int i = 0; i < NWW; ++i) w[i] = 0u;
+    } else {
+        // window pixel j (x = x0b + j in row r1) takes the row's pixel
+        // W-1-x: the WP pixels from W - x0b - WP on, reversed, so that
+        // pixel j's bytes sit at C*(WP-1-j)
+        const int x0b = (e0 - r1 * WC) / C;
+        const uint8_t* qb = sin + off_in + r1 * WC + C * (p.W - x0b - WP);
+        if (smem_read_ok(p, qb, 4 * (NWW + 1), 20)) load_bytes_at<NWW>(qb, w);
+        else for (int i = 0; i < NWW; ++i) w[i] = 0u;
+        if (split_px > 0 && r1 > 0) {
+            // pixels j < split_px lie in row r1 - 1: its mirrored run (same
+            // byte positions) fills the bytes from C*(WP - split_px) on
+            uint32_t wa[NWW];
+            const uint8_t* qa = qb - WC - C * p.W;
+            if (smem_read_ok(p, qa, 4 * (NWW + 1), 21)) load_bytes_at<NWW>(qa, wa);
+            else for (int i = 0; i < NWW; ++i) wa[i] = 0u;
+            const int thr = C * (WP - split_px);
+#pragma unroll
+            for (int i = 0; i < NWW; ++i) {
+                const int m = thr - 4 * i;
+                if (m <= 0) w[i] = wa[i];
+                else if (m < 4) w[i] = __byte_perm(w[i], wa[i], m == 1 ? 0x7650u : m == 2 ? 0x7610u : 0x7210u);
+            }
+        }
+    }
+    // erased window pixels: [lo_a, hi_a) in row r1 - 1, [lo_b, hi_b) in row r1
+    int lo_a = 0, hi_a = 0, lo_b = 0, hi_b = 0;
+    if (band_erased) {
+        const int ya = rec.y_begin + r1 - 1, yb = ya + 1;
+        const int xa = (e0 - (r1 - 1) * WC) / C;
+        const int xb = (e0 - r1 * WC) / C;
+        if (split_px > 0 && ya >= rec.erow_lo && ya < rec.erow_hi) {
+            lo_a = max(rec.ecol_lo - xa, 0);
+            hi_a = min(rec.ecol_hi - xa, split_px);
+        }
+        if (yb >= rec.erow_lo && yb < rec.erow_hi) {
+            lo_b = max(rec.ecol_lo - xb, split_px);
+            hi_b = min(rec.ecol_hi - xb, WP);
+        }
+    }
+    if (flip) odd_nchw_chunks<C, OUT_F16, D, true>(p, w, sout, tile, g, pw, E, lo_a, hi_a, lo_b, hi_b);
+    else odd_nchw_chunks<C, OUT_F16, D, false>(p, w, sout, tile, g, pw, E, lo_a, hi_a, lo_b, hi_b);
+}
+
+template <int C, int OUT_F16, int D, int MODE>
+__device__ __forceinline__ void odd_nchw_band(const TiledParams& p, const uint8_t* sin, uint8_t* sout,
+                                              const UnitRec& rec, int tid, int nthr) {
+    constexpr int OB = OUT_F16 ? 2 : 4;
+    constexpr int EPC = NchwWindow<C, OUT_F16, D>::EPC;
+    const int phi0 = (int)((odd_shift<C, OUT_F16, TR_LAYOUT_NCHW, MODE>(p, rec, 0) / OB) % EPC);
+    // plane c's chunk of window g is its tile's chunk g - (phi0 + c*D) / EPC,
+    // at tile[c] + 16 g
+    uint8_t* tile[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) tile[c] = sout + (size_t)c * p.plane_bytes - 16 * ((phi0 + c * D) / EPC);
+    const int E = rec.rows * p.W;
+    const int off_in = rec.flags >> 8;
+    const int ng = (E - 1 + phi0 + (C - 1) * D) / EPC + 1;
+    const bool band_erased = rec.erow_lo < rec.erow_hi && rec.erow_lo < rec.y_begin + rec.rows &&
+                             rec.erow_hi > rec.y_begin;
+    for (int g = tid; g < ng; g += nthr)
+        odd_nchw_window<C, OUT_F16, D>(p, sin, sout, tile, rec, g, phi0, E, off_in, band_erased);
+}
+
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD, int MODE>
 __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t* sin,
                                              uint8_t* sout, const UnitRec& rec, int tid, int nthr) {
@@ -1104,6 +1261,15 @@ __device__ __forceinline__ void compute_unit(const TiledParams& p, const uint8_t
             // field: nothing of it is read)
             if (rec.rows > 0)
                 odd_nhwc_band<C, OUT_F16>(p, sin, sout, rec, tid, nthr, odd_shift<C, OUT_F16, LAYOUT, MODE>(p, rec, 0));
+            return;
+        }
+    }
+    if constexpr (ODD && LAYOUT == TR_LAYOUT_NCHW && (C == 2 || C == 3)) {
+        if (p.hints & 134217728) {
+            if (rec.rows > 0) {
+                if (p.hints & 268435456) odd_nchw_band<C, OUT_F16, 1, MODE>(p, sin, sout, rec, tid, nthr);
+                else odd_nchw_band<C, OUT_F16, 0, MODE>(p, sin, sout, rec, tid, nthr);
+            }
             return;
         }
     }
@@ -1420,9 +1586,14 @@ __device__ __forceinline__ int first_bands_sampled(const TiledParams& p, uint8_t
 // stage and issues the TMA store of the tile.
 // (An explicit minimum of one CTA per SM lets ptxas use up to 63 registers
 // here, against 61 without it, and measured 0.9 % faster at 256x224x224x3.)
+// The odd-row forms bound by their conversion are compiled for four CTAs per
+// SM (64 registers, no spills): 16-byte NCHW plane runs, NCHW with 2 or 3
+// channels (the plane-aligned windows; binary32 RGB 256x299x299 79.7 ->
+// 65.9 us, 256x227x227 40.5 -> 35.8 us, at three CTAs with 80 registers
+// before) and NHWC with 1 or 3 channels.
 template <int C, int OUT_F16, int LAYOUT, bool CROP, bool ODD>
 constexpr int tiled_min_blocks() {
-    return ((ODD && LAYOUT == TR_LAYOUT_NCHW && Group<C>::P * (OUT_F16 ? 2 : 4) == 16) ||
+    return ((ODD && LAYOUT == TR_LAYOUT_NCHW && (Group<C>::P * (OUT_F16 ? 2 : 4) == 16 || C == 2 || C == 3)) ||
             (ODD && LAYOUT == TR_LAYOUT_NHWC && (C == 1 || C == 3)))
                ? 4
                : 1;
@@ -2383,6 +2554,23 @@ int launch_tiled(const LaunchArgs& a) {
         if (odd && a.out_layout == TR_LAYOUT_NHWC && (a.C == 1 || a.C == 3) && !(p.hints & 1024) && wc >= ge &&
             ((uint64_t)pl.R * wc + ge) * wc < (1ull << 31) && !(tflags & 8388608))
             p.hints |= 16777216;
+    }
+    // odd-row NCHW output with 2 or 3 channels, where each CTA streams enough
+    // bands: windows laid on the plane tiles' 16-byte frames (planes H*W
+    // elements apart must keep their frames 0 or 1 element apart, which
+    // every odd square size does; each row at least one window long;
+    // element indices small enough for the one-multiply row division).
+    // tr_tune_tiled flags bit 26 keeps the per-group plane runs.
+    {
+        const uint64_t wc = (uint64_t)a.W * a.C;
+        const int epc = a.out_dtype == TR_OUT_F16 ? 8 : 4;
+        const int d = (int)(((uint64_t)a.H * a.W) % (uint64_t)epc);
+        const int wp = epc + (a.C - 1) * d;
+        if (odd && a.out_layout == TR_LAYOUT_NCHW && (a.C == 2 || a.C == 3) && d <= 1 && !(p.hints & 1024) &&
+            a.W >= wp && ((uint64_t)pl.R * wc + 64) * wc < (1ull << 31) && !(tflags & 67108864)) {
+            p.hints |= 134217728;
+            if (d == 1) p.hints |= 268435456;
+        }
     }
 
     if (!check_cuda(launch_pdl((const void*)t.fn, (unsigned)t.grid, pl.threads, pl.smem, a.stream, &p),

@@ -648,7 +648,13 @@ int tr_device_status(int* flags, int clear);
  *                    the odd-row form store 16-byte binary16 NCHW plane runs
  *                    (2 or 3 channels) in plain element order (default: each
  *                    lane starts at word (lane / 8) % 4 of its run, so a
- *                    warp's stores fall on distinct banks);
+ *                    warp's stores fall on distinct banks); bit 26 keeps
+ *                    those plane runs where H*W mod 8 is 0 or 1 (every odd
+ *                    square size) and each CTA streams at least five bands
+ *                    (default there: each thread converts the 8 + (C-1) *
+ *                    (H*W mod 8) consecutive pixels that hold one 16-byte
+ *                    chunk of every plane's output tile, and writes each
+ *                    chunk with one aligned store);
  *                    records made on the GPU in the same call
  *                    (tr_fused_norm_sampled_ex with TR_LAUNCH_OVERLAP_PREVIOUS):
  *                    bit 21 makes each CTA read its first bands' records from

@@ -66,7 +66,10 @@ def _run(L, src, aug, dt, layout, ws=None, dst_offset=0):
 
 SHAPES = [(3, 37, 64, 3), (2, 70, 128, 3), (4, 20, 40, 2), (2, 13, 12, 4), (5, 64, 32, 1),   # aligned rows
           (3, 37, 61, 3), (2, 29, 227, 3), (4, 28, 28, 1), (2, 13, 99, 2), (2, 11, 75, 4),   # odd rows
-          (1, 45, 299, 3)]
+          (1, 45, 299, 3),
+          # odd rows whose planes' 16-byte frames stay 0 or 1 element apart
+          # (H*W mod 8 of 0 or 1): binary16 NCHW takes the plane-aligned windows
+          (2, 8, 75, 3), (2, 9, 89, 2), (1, 45, 301, 3)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -85,8 +88,9 @@ def test_tiled_forms_pass_the_checks(shape, dt, layout):
         assert_parity(got, ref, dt, "%s %s" % (shape, kw.keys()))
     assert L.tr_tune_tiled(0, 0, 0, STREAMS) == 0
     try:
-        got, ref = _run(L, src, aug, dt, layout)
-        assert_parity(got, ref, dt, "realigned stores %s" % (shape,))
+        for kw in ({}, {"dst_offset": 2 * (1 + (dt == F32))}):
+            got, ref = _run(L, src, aug, dt, layout, **kw)
+            assert_parity(got, ref, dt, "realigned stores %s %s" % (shape, kw.keys()))
     finally:
         L.tr_tune_tiled(0, 0, 0, 0)
     assert _status(L) == 0, "a bounds check failed (status word %#x)" % _status(L)

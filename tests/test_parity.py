@@ -395,7 +395,8 @@ def test_generic_kernel_beyond_2_31_pixels():
 
 ODD_SHAPES = [(3, 5, 7, 3), (4, 28, 28, 1), (2, 11, 13, 2), (1, 3, 5, 4), (5, 37, 227, 3), (2, 17, 299, 3),
               (3, 9, 10, 1), (2, 64, 12, 4), (7, 3, 33, 3),
-              (1, 1, 1, 1), (2, 1, 4099, 3), (1, 300, 1, 3), (64, 2, 2, 2), (3, 2, 15, 4)]
+              (1, 1, 1, 1), (2, 1, 4099, 3), (1, 300, 1, 3), (64, 2, 2, 2), (3, 2, 15, 4),
+              (2, 9, 33, 3), (2, 8, 13, 2)]
 
 
 @pytest.mark.parametrize("shape", ODD_SHAPES)
@@ -446,14 +447,18 @@ def test_odd_row_full_size(dt, layout):
     assert trfn.tr_device_status() == 0
 
 
-@pytest.mark.parametrize("shape", [(2, 17, 299, 3), (3, 9, 10, 1), (7, 3, 33, 3), (3, 2, 15, 4), (2, 11, 13, 2)])
+@pytest.mark.parametrize("shape", [(2, 17, 299, 3), (3, 9, 10, 1), (7, 3, 33, 3), (3, 2, 15, 4), (2, 11, 13, 2),
+                                   (2, 9, 33, 3), (3, 8, 75, 3), (2, 8, 13, 2), (2, 9, 57, 2)])
 def test_odd_row_output_stores_same_bits(shape):
     """The odd-row form's ways of writing its output tile give the same bits
     in every layout and type, with the output pointer on and off 16: groups
-    laid on the tile's 16-byte frame (NHWC with 1 or 3 channels) or 16-byte
-    stores of register-realigned group outputs (the rest), forced at any size
-    by tr_tune_tiled flags bit 17; the realigned pixel groups for every
-    layout (bits 17 and 23); element stores (bit 10)."""
+    laid on the tile's 16-byte frame (NHWC with 1 or 3 channels), windows
+    laid on the plane tiles' frames (binary16 NCHW with 2 or 3 channels where
+    H*W mod 8 is 0 or 1) or 16-byte stores of register-realigned group outputs
+    (the rest), forced at any size by tr_tune_tiled flags bit 17; the
+    realigned pixel groups for every layout (bits 17 and 23); the rotated
+    plane-run stores instead of the windows (bits 17 and 26); element stores
+    (bit 10)."""
     N, H, W, C = shape
     src = synth.coordinate_image(N, H, W, C)
     mean = np.array([0.5, 0.25, 0.125, 0.0], np.float32)[:C]
@@ -463,15 +468,15 @@ def test_odd_row_output_stores_same_bits(shape):
         for layout in (NHWC, NCHW, NHWC4):
             for dst_off in (0, 2 if dt == F16 else 4, 6 if dt == F16 else 12):
                 outs = []
-                for fl in (STREAMS, STREAMS | (1 << 23), 1024):
+                for fl in (STREAMS, STREAMS | (1 << 23), 1024, STREAMS | (1 << 26)):
                     try:
                         trfn.tr_tune_tiled(0, 0, 0, fl)
                         got, _ = check_case(src, mean, std, aug, dt, layout, variant=TILED, dst_offset=dst_off)
                     finally:
                         trfn.tr_tune_tiled(0, 0, 0, 0)
                     outs.append(got)
-                assert np.array_equal(outs[0], outs[1]), (dt, layout, dst_off)
-                assert np.array_equal(outs[0], outs[2]), (dt, layout, dst_off)
+                for k in (1, 2, 3):
+                    assert np.array_equal(outs[0], outs[k]), (dt, layout, dst_off, k)
     assert trfn.tr_device_status() == 0
 
 

@@ -1097,28 +1097,31 @@ def run_sampled(dev, peak):
 
 
 def run_odd_rows(dev, peak):
-    """256 x 299x299x3 -> f16 NHWC and NCHW, flip + erase: source rows of 897
-    bytes and NCHW output rows of 598, the tiled kernel's odd-row form; per
-    batch overlapping and waiting, three images of the last set against the
-    oracle."""
+    """256 x 299x299x3 -> f16 NHWC, f16 NCHW and f32 NCHW, flip + erase:
+    source rows of 897 bytes and NCHW output rows of 598 / 1196, the tiled
+    kernel's odd-row form; per batch overlapping and waiting, three images of
+    the last set against the oracle."""
     import torch
     import image_preprocessing_gb300 as trfn
     from image_preprocessing_gb300 import synth
     out = {}
     N, H, W, C = 256, 299, 299, 3
-    for layout_name in ("nhwc", "nchw"):
-        cfg = dict(synth.CONFIGS[3], H=H, W=W, layout=layout_name)
-        cfg["name"] = "n256_299x299x3_f16_%s_flip_erase" % layout_name
+    for layout_name, dt_name in (("nhwc", "f16"), ("nchw", "f16"), ("nchw", "f32")):
+        cfg = dict(synth.CONFIGS[3], H=H, W=W, layout=layout_name, out_dtype=dt_name)
+        cfg["name"] = "n256_299x299x3_%s_%s_flip_erase" % (dt_name, layout_name)
         layout = trfn.LAYOUT_NHWC if layout_name == "nhwc" else trfn.LAYOUT_NCHW
+        dt = trfn.OUT_F16 if dt_name == "f16" else trfn.OUT_F32
+        ob = 2 if dt_name == "f16" else 4
         mean = np.array(cfg["mean"], np.float32)
         std = np.array(cfg["std"], np.float32)
         shape = trfn.out_shape(N, H, W, C, layout)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-        nsets = max(2, int(np.ceil(4 * l2 / (N * H * W * C * 3))))
+        nsets = max(2, int(np.ceil(4 * l2 / (N * H * W * C * (1 + ob)))))
         px = synth.pixels_uniform(1299, N, H, W, C)
         src0 = torch.from_numpy(px).to(dev)
         srcs = [src0.clone() for _ in range(nsets)]
-        dsts = [torch.empty(shape, dtype=torch.float16, device=dev) for _ in range(nsets)]
+        dsts = [torch.empty(shape, dtype=torch.float16 if ob == 2 else torch.float32, device=dev)
+                for _ in range(nsets)]
         recs_all, augs, offset = [], [], 0
         for j in range(nsets):
             r, offset = trfn.tr_sample_aug_params(2299, offset, N, H, W, erase_p=cfg["erase_p"])
@@ -1131,12 +1134,12 @@ def run_odd_rows(dev, peak):
 
         def launch(k, overlap):
             j = k % nsets
-            trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=trfn.OUT_F16, layout=layout,
+            trfn.tr_fused_norm(srcs[j], dsts[j], mean, std, augs[j], out_dtype=dt, layout=layout,
                                stream=stream, workspace=wss[k % 2], overlap_previous=overlap)
 
         t = time_graph_modes(stream, launch, G, max(1, -(-120 // G)))
         alg = float(np.mean([algorithmic_bytes(cfg, recs_all[k % nsets]) for k in range(G)]))
-        geo = trfn.tr_fused_norm_geometry(N, H, W, C, out_dtype=trfn.OUT_F16, layout=layout, overlap_previous=True)
+        geo = trfn.tr_fused_norm_geometry(N, H, W, C, out_dtype=dt, layout=layout, overlap_previous=True)
         # geometry's grid is the static schedule's; these launches carry a
         # workspace, so they take every resident slot (or one CTA per band)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -1149,8 +1152,7 @@ def run_odd_rows(dev, peak):
             r[mode] = {"us_per_batch": ms * 1e3, "images_per_s": N / (ms / 1e3), "achieved_gbs": gbs,
                        "frac": gbs / peak, "trials_us_per_batch": [v * 1e3 for v in per]}
         j = (G - 1) % nsets
-        r["parity_sample"] = parity_sample(cfg, [srcs[j]], [dsts[j]], [recs_all[j]], mean, std, trfn.OUT_F16,
-                                           layout, 1)
+        r["parity_sample"] = parity_sample(cfg, [srcs[j]], [dsts[j]], [recs_all[j]], mean, std, dt, layout, 1)
         out[cfg["name"]] = r
         del srcs, dsts
         torch.cuda.empty_cache()

@@ -38,6 +38,9 @@ CASES = [
     # odd-row form streaming many bands: two stages, four CTAs, strides >= 84 % full
     ((256, 299, 299, 3, F16, NHWC, True), dict(rows=10, stages=2, ctas_per_sm=4, odd_form=1)),
     ((256, 299, 299, 3, F32, NHWC, False), dict(rows=5, odd_form=1)),
+    # odd-row NCHW (plane-aligned windows): compiled for four CTAs per SM
+    ((256, 299, 299, 3, F16, NCHW, True), dict(rows=10, stages=2, ctas_per_sm=4, odd_form=1)),
+    ((256, 299, 299, 3, F32, NCHW, True), dict(rows=5, stages=4, ctas_per_sm=4, odd_form=1)),
     # odd-row form with few bands a CTA: the aligned planning, even band heights
     ((256, 75, 75, 3, F16, NHWC, False), dict(rows=38, stages=3, odd_form=1)),
 ]
